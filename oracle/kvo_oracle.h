@@ -1,0 +1,138 @@
+/*
+ * kvo_oracle.h -- plain CPU oracle for the tiered KV-cache hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library is the slow, obviously-correct
+ * statement of what the GPU library computes.  It is linked by the tests, by
+ * the package's smoke check and by the benchmark's CPU-baseline leg, and by
+ * nothing else.  It shares no source, header, table or helper with the CUDA
+ * library: every conversion (fp16/bf16 bit decoding, q8_0 blocks) is written
+ * out again here from its definition.
+ *
+ * Floating point is evaluated in IEEE binary64 ("double"); compile with
+ * -ffp-contract=off so no fused multiply-add changes the rounding between
+ * the x86 development machine and the Arm GPU host.
+ *
+ * Storage formats read by the oracle (raw bytes, exactly what the GPU side
+ * reads):
+ *   dtype 0 = fp16   IEEE binary16, little endian
+ *   dtype 1 = bf16   upper 16 bits of an IEEE binary32, little endian
+ *   dtype 2 = q8_0   34-byte block { uint16 d (fp16 bits); int8 qs[32] },
+ *                    value[i] = d * qs[i]; a cell row holds n_kv_heads heads,
+ *                    each head_dim/32 consecutive blocks.
+ *
+ * Parity pins (checked by the CPU test-suite, against things other than this
+ * file): fp16/bf16 decoding against numpy/torch over all 65,536 patterns;
+ * sub-block pointers against a brute-force enumeration of the (block, j)
+ * grid; swap against numpy slicing and the D2H-then-H2D round trip;
+ * gather against numpy fancy indexing; attention against scipy's softmax with
+ * numpy matmuls, and against closed forms (one cell gives v, q = 0 gives the
+ * mean of v, a constant-per-head V gives the kv-head index, the causal
+ * boundary gives pos/2 for V = position); the fold against the one-shot
+ * softmax over the union of buckets.
+ */
+#ifndef KVO_ORACLE_H
+#define KVO_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_Q8_0 = 2 };
+
+/* Exact decodings of the two 16-bit float formats. */
+double orc_half_to_double(uint16_t bits);
+double orc_bf16_to_double(uint16_t bits);
+
+/* Bytes of one cell row (n_kv_heads heads of head_dim values) in a dtype;
+ * 0 for an unknown dtype or a q8_0 head_dim that is not a multiple of 32. */
+int64_t orc_row_bytes(int dtype, int64_t n_kv_heads, int64_t head_dim);
+
+/* Decode head `head` of one cell row into head_dim doubles. */
+void orc_load_head(const uint8_t *row, int dtype, int64_t head_dim,
+                   int64_t head, double *out);
+
+/* vLLM gpu_worker.py, compute_sub_block_ptrs: pointer of sub-block j of
+ * block b is base + b*row_stride + j*(row_bytes/bpc); the (n_ids x bpc) grid
+ * is flattened row-major and out = flat[skip : skip + n_out].
+ * Returns 0, or -1 on an argument the page's asserts reject
+ * (skip >= bpc, row_bytes % bpc != 0) or on n_out beyond the grid. */
+int orc_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
+                       int64_t blocks_per_chunk, int64_t skip_count,
+                       uint64_t base, int64_t row_stride_bytes,
+                       int64_t row_bytes, uint64_t *out, int64_t n_out);
+
+/* vLLM gpu_worker.py, transfer_async -> swap_blocks_batch: for i in
+ * index order, copy sizes[i] bytes from address src[i] to address dst[i]
+ * (all host addresses here). */
+void orc_swap_blocks(const uint64_t *src, const uint64_t *dst,
+                     const int64_t *sizes, int64_t n);
+
+/* ExLlamaV3 qsa-kv-offload patch, staged gather (index_select of whole
+ * pages): for each sequence s, kv head h and rank r, block sel[s][h][r]
+ * (block_tokens tokens) of plane [s][token][h][:] is copied to
+ * out[s][r*block_tokens + t][h][:] for t < block_tokens.
+ * Planes are [n_seq][seq_stride_tokens][n_kv_heads][head_dim] elements of
+ * elem_bytes; out is [n_seq][n_sel*block_tokens][n_kv_heads][head_dim].
+ * Returns 0, or -1 when a selected block lies outside the plane. */
+int orc_gather_blocks(const uint8_t *plane, int64_t n_seq,
+                      int64_t seq_stride_tokens, int64_t n_kv_heads,
+                      int64_t head_dim, int64_t elem_bytes,
+                      int64_t block_tokens, const int32_t *sel,
+                      int64_t n_sel, uint8_t *out);
+
+/* Tiered cache addressing (llama.cpp PR "tiered KV cache (--kv-vram-cells)"):
+ * cell j of sequence b lives at
+ *   head + (b*head_seq_stride_rows + j) * row_bytes          if j <  n_vram
+ *   tail + (b*tail_seq_stride_rows + j - n_vram) * row_bytes if j >= n_vram
+ */
+typedef struct {
+  const uint8_t *k_head, *v_head, *k_tail, *v_tail;
+  int64_t head_seq_stride_rows, tail_seq_stride_rows;
+  int64_t n_vram;
+  int dtype;
+  int64_t n_kv_heads, head_dim;
+} orc_cache;
+
+/* Softmax attention over cells [c0, c1) of sequence b for one q head
+ * (already decoded to doubles), kv head = q_head / (n_q_heads/n_kv_heads).
+ * Unnormalised partial: m = max_j s_j, l = sum_j exp(s_j - m),
+ * acc[d] = sum_j exp(s_j - m) v_j[d], with s_j = scale * q . k_j.
+ * An empty range gives m = -inf, l = 0, acc = 0. */
+void orc_attn_partial(const orc_cache *c, int64_t b, int64_t kv_head,
+                      const double *q, double scale, int64_t c0, int64_t c1,
+                      double *m, double *l, double *acc);
+
+/* One-step online-softmax fold (ExLlamaV3 qsa-kv-offload patch, the fold of
+ * a bucket's partial (o, m, l) into the running (acc, m, l)):
+ *   m' = max(m, m_b); alpha = exp(m - m') (0 if m = -inf);
+ *   beta = exp(m_b - m') (0 if m_b = -inf);
+ *   acc = alpha*acc + beta*acc_b; l = alpha*l + beta*l_b; m = m'. */
+void orc_fold(double *m, double *l, double *acc, double m_b, double l_b,
+              const double *acc_b, int64_t head_dim);
+
+/* GQA decode: out[b][h][:] = softmax_j(scale * q[b][h] . k_j) v_j over
+ * cells j < ctx_len[b] of sequence b.  q is [batch][n_q_heads][head_dim] of
+ * q_dtype (fp16 or bf16).  out is [batch][n_q_heads][head_dim] doubles. */
+void orc_attn_decode(const orc_cache *c, const uint16_t *q, int q_dtype,
+                     int64_t batch, int64_t n_q_heads,
+                     const int32_t *ctx_len, double scale, double *out);
+
+/* Causal chunked prefill for one sequence: row i of q ([rows][n_q_heads]
+ * [head_dim], bf16 or fp16) sits at position q_pos0 + i and attends cells
+ * j <= q_pos0 + i (and j < ctx_len).  out is [rows][n_q_heads][head_dim]. */
+void orc_attn_prefill(const orc_cache *c, const uint16_t *q, int q_dtype,
+                      int64_t rows, int64_t q_pos0, int64_t n_q_heads,
+                      int64_t ctx_len, double scale, double *out);
+
+/* Worker threads used by orc_attn_decode / orc_attn_prefill (independent
+ * (row, head) outputs are distributed; each is computed exactly as in the
+ * serial loop).  Returns the count in effect; 1 without OpenMP. */
+int orc_set_threads(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
