@@ -1,0 +1,658 @@
+#!/usr/bin/env python3
+"""Benchmark of the tiered KV-cache hot path on GB300 (one JSON line).
+
+Headline: tiered q8_0 decode (48 q heads / 8 kv heads x 128, batch 1, one
+layer) at a 184,320-cell context with cells [0, 8192) in VRAM and the rest
+in pinned host memory -- microseconds per step, host-link GB/s and the
+fraction of the measured pinned-copy peak.  The same line carries every
+other row of the path measured on its own workload: the batched block swap
+(32 layers x K,V, 2048 blocks per direction, 32 KiB and 2 KiB pages), the
+top-k gather from 8 GiB host planes plus the sparse decode over the gathered
+4096 tokens, the other decode contexts and VRAM splits with staging on and
+off, and the tiered chunked prefill (2048 rows over 262,144 cells, staged
+through a 32 MiB arena and direct).
+
+All inputs are seeded synthetic data (host_ram_tiered_gb300.synth).  The
+timed region starts with every input resident where the workload puts it
+(VRAM head, pinned host tail); each timed step is bracketed by CUDA events
+on the launching stream, and L2 is flushed (a 256 MiB device write) between
+timed steps.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from host_ram_tiered_gb300 import synth  # noqa: E402
+
+METRIC = "tiered-KV decode µs/step & host-link GB/s (% of measured pinned-copy peak)"
+HEADLINE = "c3_q8_0_decode_L184320_N8192_direct"
+SEED0 = 1234
+
+
+def torch():
+    import torch as t
+    return t
+
+
+def kvo():
+    from host_ram_tiered_gb300 import kvo as k
+    return k
+
+
+# ----------------------------------------------------------------- buffers
+
+def pinned(nbytes):
+    t = torch()
+    return t.empty(max(int(nbytes), 1), dtype=t.uint8, pin_memory=True)
+
+
+def dev(nbytes):
+    t = torch()
+    return t.empty(max(int(nbytes), 1), dtype=t.uint8, device="cuda")
+
+
+def pinned_i64(a):
+    buf = pinned(a.size * 8)
+    buf.numpy().view(np.int64)[:a.size] = a
+    return buf
+
+
+# ----------------------------------------------------------------- timing
+
+class Timer:
+    """K timed steps on one stream, each bracketed by CUDA events, L2 flushed
+    in between (outside the events)."""
+
+    def __init__(self):
+        t = torch()
+        self.stream = t.cuda.current_stream()
+        self.flush_buf = t.empty(256 << 20, dtype=t.uint8, device="cuda")
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+    def run(self, step, steps, warmup, flush=True):
+        t = torch()
+        for _ in range(warmup):
+            step()
+        t.cuda.synchronize()
+        evs = [(t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in evs:
+            if flush:
+                self.flush()
+            a.record(self.stream)
+            step()
+            b.record(self.stream)
+        t.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        return sum(ms), ms
+
+
+def measure_link_peak(timer):
+    """Pinned-copy peak per direction: cudaMemcpyAsync of 1 GiB, best of 5."""
+    t = torch()
+    n = 1 << 30
+    h = pinned(n)
+    d = dev(n)
+    out = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        _, ms = timer.run(fn, 5, 2, flush=False)
+        out[name] = n / (min(ms) * 1e-3) / 1e9
+    del h, d
+    return out
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.rows, self.proc = [], None
+        dev_idx = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", dev_idx, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for i, nm in enumerate(names):
+                if len(r) > 4 + i and r[4 + i].lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- C2 swap
+
+C2_TENSORS, C2_GPU_BLOCKS, C2_HOST_CHUNKS, C2_BLOCKS, C2_BPC, C2_SKIP = 64, 4096, 640, 2048, 4, 1
+
+
+def c2_setup(page, seed=SEED0 + 1):
+    """vLLM-style CPU offload swap: 64 paged tensors (32 layers x K,V), 2048
+    seeded GPU block ids per direction, host chunks of 4 pages with a row
+    stride of 1.5 x the chunk, skip 1 on the first chunk."""
+    k = kvo()
+    row = C2_BPC * page
+    stride = row * 3 // 2
+    gpu_bytes = C2_GPU_BLOCKS * page
+    host_bytes = C2_HOST_CHUNKS * stride
+    d = dev(C2_TENSORS * gpu_bytes)
+    h = pinned(C2_TENSORS * host_bytes)
+    init = np.empty(C2_TENSORS * gpu_bytes, np.uint8)
+    synth.fill_bytes_large(init, seed, 2)
+    d.copy_(torch().from_numpy(init))
+    synth.fill_bytes_large(h.numpy(), seed, 3)
+    g = synth.rng(seed, 4)
+    gpu_ids = g.permutation(C2_GPU_BLOCKS)[:C2_BLOCKS].astype(np.int64)
+    need = -(-(C2_BLOCKS + C2_SKIP) // C2_BPC)
+    host_ids = g.permutation(C2_HOST_CHUNKS)[:need].astype(np.int64)
+    n_desc = C2_TENSORS * C2_BLOCKS
+    hp = np.empty(n_desc, np.int64)
+    gp = np.empty(n_desc, np.int64)
+    for i in range(C2_TENSORS):
+        k.kvo_sub_block_ptrs(host_ids.ctypes.data, need, C2_BPC, C2_SKIP, h.data_ptr() + i * host_bytes,
+                             stride, row, hp[i * C2_BLOCKS:].ctypes.data, C2_BLOCKS)
+        k.kvo_sub_block_ptrs(gpu_ids.ctypes.data, C2_BLOCKS, 1, 0, d.data_ptr() + i * gpu_bytes,
+                             page, page, gp[i * C2_BLOCKS:].ctypes.data, C2_BLOCKS)
+    sizes = pinned_i64(np.full(n_desc, page, np.int64))
+    st = {"page": page, "dev": d, "host": h, "n_desc": n_desc, "sizes": sizes,
+          "h2d_src": pinned_i64(hp), "h2d_dst": pinned_i64(gp),
+          "d2h_src": pinned_i64(gp), "d2h_dst": pinned_i64(hp),
+          "bytes": n_desc * page, "init_dev": init, "host_ids": host_ids, "gpu_ids": gpu_ids}
+    st["init_dev_sample"] = lambda off, n: init[off:off + n]
+    st["d2h_src_np"], st["d2h_dst_np"] = gp, hp
+    return st
+
+
+def c2_run(st, h2d, flags=0):
+    k = kvo()
+    if h2d:
+        k.kvo_swap_blocks_batch(st["h2d_src"], st["h2d_dst"], st["sizes"], st["n_desc"],
+                                k.KVO_SWAP_H2D | k.KVO_SWAP_SRC_ORDER_ANY | flags)
+    else:
+        k.kvo_swap_blocks_batch(st["d2h_src"], st["d2h_dst"], st["sizes"], st["n_desc"],
+                                k.KVO_SWAP_D2H | flags)
+
+
+# ----------------------------------------------------------------- C3 decode
+
+C3_HQ, C3_HKV, C3_D = 48, 8, 128
+C3_LS = (29696, 96256, 184320)
+C3_NS = (8192, 94208)
+
+
+def c3_setup(seed=SEED0 + 2, l_max=max(C3_LS), n_max=max(C3_NS)):
+    """llama.cpp-style tiered decode, q8_0 K/V (blocks of 32 int8 uniform in
+    [-127, 127] and an fp16 scale ~U(0.001, 0.02)), one layer, batch 1."""
+    t = torch()
+    g = synth.rng(seed, 1)
+    rb = C3_HKV * (C3_D // 32) * 34
+    k_all = pinned(l_max * rb)
+    v_all = pinned(l_max * rb)
+    chunk = 16384
+    for c0 in range(0, l_max, chunk):
+        n = min(chunk, l_max - c0)
+        k_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, C3_HKV, C3_D, g).reshape(-1)
+        v_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, C3_HKV, C3_D, g).reshape(-1)
+    q = synth.normal_bits((1, C3_HQ, C3_D), "f16", g)
+    st = {"rb": rb, "k_host": k_all, "v_host": v_all,
+          "k_dev": k_all[:n_max * rb].cuda(), "v_dev": v_all[:n_max * rb].cuda(),
+          "k_dev_all": k_all.cuda(), "v_dev_all": v_all.cuda(),
+          "q_np": q, "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
+          "out": t.empty(C3_HQ * C3_D, dtype=t.float32, device="cuda"),
+          "stage_k": dev(l_max * rb), "stage_v": dev(l_max * rb)}
+    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(1, C3_HQ, C3_D, l_max)
+    st["ws"] = dev(st["ws_bytes"])
+    st["ctx"] = {}
+    return st
+
+
+def c3_ctx(st, L):
+    t = torch()
+    if L not in st["ctx"]:
+        st["ctx"][L] = t.tensor([L], dtype=t.int32, device="cuda")
+    return st["ctx"][L]
+
+
+def c3_run(st, L, N, staging=False, all_vram=False, q=None, out=None):
+    k = kvo()
+    rb = st["rb"]
+    ws_bytes = k.kvo_attn_decode_workspace_bytes(1, C3_HQ, C3_D, L)
+    if all_vram:
+        kh, vh, kt, vt, n = st["k_dev_all"], st["v_dev_all"], None, None, L
+    else:
+        n = min(N, L)
+        kh, vh = st["k_dev"], st["v_dev"]
+        kt = st["k_host"].data_ptr() + n * rb
+        vt = st["v_host"].data_ptr() + n * rb
+    k.kvo_attn_decode_tiered(q if q is not None else st["q"], k.F16, 1, C3_HQ, C3_HKV, C3_D,
+                             kh, vh, n, kt, vt, L - n, k.Q8_0, c3_ctx(st, L), L, n,
+                             1.0 / math.sqrt(C3_D),
+                             st["stage_k"] if staging else None, st["stage_v"] if staging else None,
+                             out if out is not None else st["out"], st["ws"], ws_bytes)
+
+
+def c3_bytes(L, N):
+    rb2 = 2 * C3_HKV * (C3_D // 32) * 34
+    return max(L - N, 0) * rb2, min(L, N) * rb2
+
+
+# ----------------------------------------------------------------- C4 gather + sparse decode
+
+C4_S, C4_T, C4_HQ, C4_HKV, C4_D, C4_BLK, C4_K = 8, 1 << 20, 16, 4, 128, 64, 64
+
+
+def c4_setup(seed=SEED0 + 3):
+    """QSA-style sparse decode: bf16 K/V planes [8][2^20][4][128] in pinned
+    host memory, 64 of 16,384 blocks per (sequence, kv head) selected
+    without replacement (the last block always), gathered into VRAM, then
+    decode over the 4096 gathered tokens."""
+    t = torch()
+    plane = C4_S * C4_T * C4_HKV * C4_D
+    k_plane = pinned(plane * 2)
+    v_plane = pinned(plane * 2)
+    synth.fill_normal_bits_large(k_plane.numpy().view(np.uint16), "bf16", seed, 1)
+    synth.fill_normal_bits_large(v_plane.numpy().view(np.uint16), "bf16", seed, 2)
+    g = synth.rng(seed, 3)
+    sel = synth.topk_selection(C4_S, C4_HKV, C4_T // C4_BLK, C4_K, g)
+    q = synth.normal_bits((C4_S, C4_HQ, C4_D), "bf16", g)
+    tok = C4_K * C4_BLK
+    out_bytes = C4_S * tok * C4_HKV * C4_D * 2
+    st = {"k_plane": k_plane, "v_plane": v_plane, "sel_np": sel,
+          "sel": t.from_numpy(sel.reshape(-1).copy()).cuda(),
+          "kg": dev(out_bytes), "vg": dev(out_bytes), "q_np": q,
+          "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
+          "ctx": t.full((C4_S,), tok, dtype=t.int32, device="cuda"),
+          "out": t.empty(C4_S * C4_HQ * C4_D, dtype=t.float32, device="cuda"),
+          "gather_bytes": 2 * out_bytes}
+    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(C4_S, C4_HQ, C4_D, tok)
+    st["ws"] = dev(st["ws_bytes"])
+    return st
+
+
+def c4_gather(st):
+    k = kvo()
+    k.kvo_gather_blocks(st["k_plane"], st["v_plane"], C4_S, C4_T, C4_HKV, C4_D, k.BF16, C4_BLK,
+                        st["sel"], C4_K, st["kg"], st["vg"])
+
+
+def c4_decode(st):
+    k = kvo()
+    tok = C4_K * C4_BLK
+    k.kvo_attn_decode_tiered(st["q"], k.BF16, C4_S, C4_HQ, C4_HKV, C4_D, st["kg"], st["vg"], tok,
+                             None, None, 0, k.BF16, st["ctx"], tok, tok, 1.0 / math.sqrt(C4_D),
+                             None, None, st["out"], st["ws"], st["ws_bytes"])
+
+
+# ----------------------------------------------------------------- C5 prefill
+
+C5_R, C5_POS0, C5_L, C5_HQ, C5_HKV, C5_D, C5_N = 2048, 260096, 262144, 32, 8, 128, 65536
+C5_ARENA, C5_RPL = 32 << 20, 1024
+
+
+def c5_setup(seed=SEED0 + 4):
+    """Tiered chunked prefill: 2048 query rows at positions 260,096-262,143,
+    bf16 K/V cells [262,144][8][128], cells [0, 65,536) in VRAM, the tail in
+    pinned host memory; staged through a 32 MiB arena, 1024 rows a launch."""
+    t = torch()
+    rb = C5_HKV * C5_D * 2
+    g_seed = seed
+    k_host = pinned((C5_L - C5_N) * rb)
+    v_host = pinned((C5_L - C5_N) * rb)
+    k_head = np.empty(C5_N * rb // 2, np.uint16)
+    v_head = np.empty(C5_N * rb // 2, np.uint16)
+    synth.fill_normal_bits_large(k_head, "bf16", g_seed, 1)
+    synth.fill_normal_bits_large(v_head, "bf16", g_seed, 2)
+    synth.fill_normal_bits_large(k_host.numpy().view(np.uint16), "bf16", g_seed, 3)
+    synth.fill_normal_bits_large(v_host.numpy().view(np.uint16), "bf16", g_seed, 4)
+    q = synth.normal_bits((C5_R, C5_HQ, C5_D), "bf16", synth.rng(g_seed, 5))
+    st = {"rb": rb, "k_host": k_host, "v_host": v_host, "k_head_np": k_head, "v_head_np": v_head,
+          "k_head": t.from_numpy(k_head.view(np.int16)).cuda(),
+          "v_head": t.from_numpy(v_head.view(np.int16)).cuda(), "q_np": q,
+          "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
+          "arena": dev(C5_ARENA),
+          "out": t.empty(C5_R * C5_HQ * C5_D, dtype=t.float32, device="cuda")}
+    st["ws_bytes"] = kvo().kvo_attn_prefill_workspace_bytes(C5_R, C5_HQ)
+    st["ws"] = dev(st["ws_bytes"])
+    return st
+
+
+def c5_run(st, staged=True, q=None, out=None):
+    k = kvo()
+    k.kvo_attn_prefill_tiered(q if q is not None else st["q"], C5_R, C5_POS0, C5_HQ, C5_HKV, C5_D,
+                              st["k_head"], st["v_head"], st["k_host"], st["v_host"], k.BF16, C5_L,
+                              C5_N, 1.0 / math.sqrt(C5_D),
+                              st["arena"] if staged else None, C5_ARENA if staged else 0, C5_RPL,
+                              out if out is not None else st["out"], st["ws"], st["ws_bytes"])
+
+
+def c5_flops():
+    # causal: row i sees pos0 + i + 1 cells; QK^T and PV are 2 flops per MAC each
+    cells = sum(C5_POS0 + i + 1 for i in range(C5_R))
+    return 4.0 * C5_HQ * C5_D * cells
+
+
+# ----------------------------------------------------------------- CPU oracle arm
+
+def oracle_c3_step(L, heads=C3_HQ):
+    """fp64 oracle decode of the headline workload (q8_0, L cells, N split),
+    on host copies of the same seeded inputs."""
+    import oracle
+    g = synth.rng(SEED0 + 2, 1)
+    rb = C3_HKV * (C3_D // 32) * 34
+    k = np.empty((L, rb), np.uint8)
+    v = np.empty((L, rb), np.uint8)
+    chunk = 16384
+    for c0 in range(0, max(C3_LS), chunk):
+        n = min(chunk, max(C3_LS) - c0)
+        kk = synth.q8_0_rows(n, C3_HKV, C3_D, g)
+        vv = synth.q8_0_rows(n, C3_HKV, C3_D, g)
+        if c0 < L:
+            m = min(n, L - c0)
+            k[c0:c0 + m] = kk[:m]
+            v[c0:c0 + m] = vv[:m]
+    q = synth.normal_bits((1, C3_HQ, C3_D), "f16", g)
+    N = 8192
+    kh, vh = np.ascontiguousarray(k[:N]), np.ascontiguousarray(v[:N])
+    kt, vt = np.ascontiguousarray(k[N:]), np.ascontiguousarray(v[N:])
+    cache = oracle.make_cache(kh, vh, kt, vt, N, L - N, N, oracle.Q8_0, C3_HKV, C3_D)
+    keep = (kh, vh, kt, vt)
+    qs = np.ascontiguousarray(q[:, :heads])
+
+    def step():
+        return oracle.attn_decode(cache, qs, oracle.F16, 1, heads, [L], 1.0 / math.sqrt(C3_D))
+    return step, keep
+
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    threads = oracle.set_threads(os.cpu_count() or 1)
+    L = max(C3_LS)
+    # Bounded sample: the oracle decodes 8 of the 48 query heads per step
+    # (one kv head's worth of GQA rows is 6; 8 keeps the time per step near
+    # a second on 16 Grace cores), scaled to a full step by 48/8.
+    heads = 8
+    step, keep = oracle_c3_step(L, heads)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    us = dt / args.steps * 1e6 * (C3_HQ / heads)
+    host_b, dev_b = c3_bytes(L, 8192)
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": HEADLINE, "L": L, "n_vram_cells": 8192, "q_heads": C3_HQ,
+                       "kv_heads": C3_HKV, "head_dim": C3_D, "kv_dtype": "q8_0", "batch": 1},
+            "cpu_baseline": {"value": us, "unit": "us/step", "cores": threads, "kind": "oracle",
+                             "sample": f"{heads} of {C3_HQ} query heads per step, scaled x{C3_HQ // heads}"},
+            "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "host_gbs_equiv": host_b / (us * 1e-6) / 1e9}
+    return line
+
+
+# ----------------------------------------------------------------- main
+
+def rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    t = torch()
+    import torch.distributed as dist
+    v = t.tensor([x], dtype=t.float64, device="cuda" if t.cuda.is_available() else "cpu")
+    dist.all_reduce(v, op=dist.ReduceOp.MAX)
+    return float(v.item())
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
+    ap.add_argument("--rows", default="all", help="comma list of c2,c3,c4,c5 (default all)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = rank_info()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    t = torch()
+    t.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from host_ram_tiered_gb300 import build
+    build.build()
+    k = kvo()
+    k.load()
+    rows = set(args.rows.split(",")) if args.rows != "all" else {"c2", "c3", "c4", "c5"}
+    timer = Timer()
+    peaks = measure_link_peak(timer)
+    hbm = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6789.0) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 6800.0
+    K, W = args.steps, args.warmup
+    results = {}
+
+    def bar():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        t.cuda.synchronize()
+
+    clocks = Clocks()
+    # ---- headline: C3 decode at L = 184,320, N = 8,192, direct
+    head = None
+    if "c3" in rows or True:
+        st3 = c3_setup()
+        bar()
+        tot, ms = timer.run(lambda: c3_run(st3, 184320, 8192), K, W)
+        tot = max_over_ranks(tot, world)
+        us = tot / K * 1e3
+        hb, db = c3_bytes(184320, 8192)
+        head = {"us": us, "host_bytes": hb, "dev_bytes": db, "ms": ms}
+        results[HEADLINE] = {"us_per_step": us, "host_gbs": hb / (us * 1e-6) / 1e9,
+                             "frac_link_peak": hb / (us * 1e-6) / 1e9 / peaks["h2d"]}
+        # e2e through the C-ABI with host buffers: q from pinned host, out back to pinned host
+        q_h = t.from_numpy(st3["q_np"].view(np.int16).reshape(-1).copy()).pin_memory()
+        o_h = t.empty(C3_HQ * C3_D, dtype=t.float32).pin_memory()
+        q_d = t.empty_like(st3["q"])
+        o_d = t.empty_like(st3["out"])
+
+        def e2e_step():
+            q_d.copy_(q_h, non_blocking=True)
+            c3_run(st3, 184320, 8192, q=q_d, out=o_d)
+            o_h.copy_(o_d, non_blocking=True)
+        tot_e, _ = timer.run(e2e_step, K, W)
+        tot_e = max_over_ranks(tot_e, world)
+        head["e2e_us"] = tot_e / K * 1e3
+        head["e2e_h2d"] = q_h.numel() * 2
+        head["e2e_d2h"] = o_h.numel() * 4
+        if "c3" in rows:
+            for L in C3_LS:
+                for N in C3_NS:
+                    for staging in (False, True):
+                        if L <= N and staging:
+                            continue
+                        tot, _ = timer.run(lambda: c3_run(st3, L, N, staging=staging), K, W)
+                        us_r = max_over_ranks(tot, world) / K * 1e3
+                        hb_r, db_r = c3_bytes(L, N)
+                        if staging:
+                            db_r += 2 * hb_r
+                        key = f"c3_q8_0_decode_L{L}_N{N}_{'staged' if staging else 'direct'}"
+                        t_star = max(hb_r / (peaks['h2d'] * 1e9), db_r / (hbm * 1e9))
+                        results[key] = {"us_per_step": us_r, "host_gbs": hb_r / (us_r * 1e-6) / 1e9,
+                                        "roofline_frac": t_star / (us_r * 1e-6)}
+                tot, _ = timer.run(lambda: c3_run(st3, L, 0, all_vram=True), K, W)
+                us_r = max_over_ranks(tot, world) / K * 1e3
+                db_r = L * 2 * C3_HKV * (C3_D // 32) * 34
+                results[f"c3_q8_0_decode_L{L}_all_vram"] = {
+                    "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
+                    "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
+        del st3
+    # ---- C2 swap
+    if "c2" in rows:
+        for page in (32768, 2048):
+            st2 = c2_setup(page)
+            for h2d in (True, False):
+                tot, _ = timer.run(lambda: c2_run(st2, h2d), K, W)
+                us_r = max_over_ranks(tot, world) / K * 1e3
+                gbs = st2["bytes"] / (us_r * 1e-6) / 1e9
+                pk = peaks["h2d" if h2d else "d2h"]
+                results[f"c2_swap_{page // 1024}KiB_{'h2d' if h2d else 'd2h'}"] = {
+                    "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / pk,
+                    "descriptors": st2["n_desc"], "mode": "sm"}
+            del st2
+            t.cuda.empty_cache()
+    # ---- C4 gather + sparse decode
+    if "c4" in rows:
+        st4 = c4_setup()
+        tot, _ = timer.run(lambda: c4_gather(st4), K, W)
+        us_r = max_over_ranks(tot, world) / K * 1e3
+        gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
+        results["c4_gather"] = {"us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["h2d"]}
+        c4_gather(st4)
+        tot, _ = timer.run(lambda: c4_decode(st4), K, W)
+        us_r = max_over_ranks(tot, world) / K * 1e3
+        gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
+        results["c4_sparse_decode"] = {"us_per_step": us_r, "hbm_gbs": gbs, "roofline_frac": gbs / hbm}
+        del st4
+    # ---- C5 prefill
+    if "c5" in rows:
+        st5 = c5_setup()
+        fl = c5_flops()
+        tail_b = (C5_L - C5_N) * st5["rb"] * 2
+        bf16 = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops", 1932.2) \
+            if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+        for staged in (True, False):
+            steps = K if staged else max(1, min(K, 3))
+            tot, _ = timer.run(lambda: c5_run(st5, staged), steps, min(W, 3))
+            us_r = max_over_ranks(tot, world) / steps * 1e3
+            tfs = fl / (us_r * 1e-6) / 1e12
+            t_star = max(fl / (bf16 * 1e12), tail_b / (peaks["h2d"] * 1e9))
+            results[f"c5_prefill_{'staged' if staged else 'direct'}"] = {
+                "us_per_step": us_r, "tflops": tfs, "tensor_frac": tfs / bf16,
+                "roofline_frac": t_star / (us_r * 1e-6), "tokens_per_s": C5_R / (us_r * 1e-6)}
+        del st5
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    if rank == 0:
+        us = head["us"]
+        achieved = head["host_bytes"] / (us * 1e-6) / 1e9
+        line = {
+            "metric": METRIC, "value": us, "unit": "us/step", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "q8_0 K/V x f16 q, f32 accumulate",
+            "data": "synthetic (seeded)",
+            "config": {"workload": HEADLINE, "L": 184320, "n_vram_cells": 8192, "q_heads": C3_HQ,
+                       "kv_heads": C3_HKV, "head_dim": C3_D, "kv_dtype": "q8_0", "batch": 1,
+                       "staging": False, "l2": "flushed between timed steps (256 MiB write)"},
+            "host_gbs": achieved, "link_peak_gbs": peaks,
+            "roofline": {"bound": "host_link", "achieved": achieved, "peak": peaks["h2d"], "unit": "GB/s",
+                         "frac": achieved / peaks["h2d"], "traffic": None,
+                         "peak_source": "pinned cudaMemcpyAsync H2D 1 GiB, best of 5, measured in this run",
+                         "kernel": "decode_split_kernel + decode_combine_kernel (one C-ABI call)"},
+            "e2e": {"value": head["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": head["e2e_h2d"],
+                    "d2h_bytes_per_step": head["e2e_d2h"]},
+            "gpu_launches": gpu_launch_count(K, rows),
+            "clocks": clk, "cpu_baseline": cpu, "rows": results,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def gpu_launch_count(K, rows):
+    """Kernels of libkvo launched in the timed regions (own kernels only)."""
+    n = 2 * K * 2                                  # headline decode + its e2e: split + combine
+    if "c3" in rows:
+        n += 2 * K * (3 * 2 * 2 - 1 + 3)           # 11 tiered variants + 3 all-VRAM, 2 kernels each
+    if "c2" in rows:
+        n += K * 4                                 # 2 pages x 2 directions, one swap kernel each
+    if "c4" in rows:
+        n += K + 2 * K                             # gather; decode split + combine
+    if "c5" in rows:
+        # staged: head (2 row blocks) + 24 buckets x 2 row blocks; direct: 2 segments x 2 row blocks
+        n += K * (2 + 24 * 2) + min(K, 3) * 4
+    return n
+
+
+def cpu_baseline():
+    """The fp64 oracle timed on this host's cores on a bounded sample of the
+    headline workload (a subset of query heads, scaled to the full step)."""
+    import oracle
+    oracle.build()
+    threads = oracle.set_threads(os.cpu_count() or 1)
+    heads = 8
+    step, keep = oracle_c3_step(max(C3_LS), heads)
+    step()
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < 10.0 and n < 20:
+        step()
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return {"value": dt * 1e6 * (C3_HQ / heads), "unit": "us/step", "cores": threads, "kind": "oracle",
+            "sample": f"{heads} of {C3_HQ} query heads per step over the full 184,320 cells, "
+                      f"{n} steps, scaled x{C3_HQ // heads}"}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,263 @@
+// Tiered GQA decode attention: split-K flash-decoding over a cache whose
+// cells [0, N) are in VRAM and [N, L) in pinned host memory (or a VRAM
+// staging copy of them).  llama.cpp PR "tiered KV cache (--kv-vram-cells)":
+// the arithmetic does not depend on where a cell lives, so a tiered cache
+// gives output bit-identical to an all-VRAM one.
+//
+// Layout of one CTA: one warp per kv head (n_kv_heads warps); lane l owns
+// head dims [l*D/32, (l+1)*D/32) of the warp's G = n_q_heads/n_kv_heads
+// query heads.  A tile of T cell rows (all kv heads, 16-byte aligned rows)
+// is copied into shared memory with 16-byte loads, coalesced across the CTA,
+// from whichever tier holds each cell.  Scores use a fixed butterfly
+// reduction; the softmax is online in the log2 domain; q8_0 blocks are
+// dequantised while a lane reads its dims from shared memory (d * q is exact
+// in fp32).  Each CTA handles one fixed cell range (split) and writes an
+// unnormalised partial (m, l, acc); a second kernel folds the splits of a
+// head in ascending order.  Instantiated per K/V dtype in decode_<dtype>.cu.
+#pragma once
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+namespace dec {
+
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float h2f(uint16_t b, int dt) {
+  if (dt == KVO_BF16) return __uint_as_float((uint32_t)b << 16);
+  return __half2float(__ushort_as_half(b));
+}
+
+// Read this lane's DPL dims of kv head g from a cell row held in shared memory.
+template <int KVT, int D>
+__device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, float *x) {
+  constexpr int DPL = D / 32;
+  if constexpr (KVT == KVO_Q8_0) {
+    constexpr int NB = D / 32;                       // blocks per head
+    constexpr int LPB = 32 / DPL;                    // lanes per block
+    const uint8_t *blk = row + (g * NB + lane / LPB) * 34;
+    const float d = __half2float(__ushort_as_half(*(const uint16_t *)blk));
+    const int8_t *qs = (const int8_t *)(blk + 2) + (lane % LPB) * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; i += 2) {
+      const uint16_t two = *(const uint16_t *)(qs + i);   // 2-byte aligned
+      x[i] = d * (float)(int8_t)(two & 0xff);
+      x[i + 1] = d * (float)(int8_t)(two >> 8);
+    }
+  } else {
+    const uint16_t *h = (const uint16_t *)(row + g * D * 2) + lane * DPL;
+    if constexpr (DPL == 4) {
+      const uint2 u = *(const uint2 *)h;
+      x[0] = h2f(u.x & 0xffff, KVT); x[1] = h2f(u.x >> 16, KVT);
+      x[2] = h2f(u.y & 0xffff, KVT); x[3] = h2f(u.y >> 16, KVT);
+    } else {
+      const uint32_t u = *(const uint32_t *)h;
+      x[0] = h2f(u & 0xffff, KVT); x[1] = h2f(u >> 16, KVT);
+    }
+  }
+}
+
+// Copy cell rows [c0, c0 + n) of sequence b (K and V) into shared memory.
+__device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0, int n,
+                                          uint8_t *sk, uint8_t *sv) {
+  const int64_t rb = a.row_bytes;
+  const int cpr = (int)(rb >> 4);                    // 16-byte chunks per row
+  const int total = n * cpr;
+  const int nthr = blockDim.x;
+  constexpr int kBatch = 8;
+  for (int base = 0; base < 2 * total; base += kBatch * nthr) {
+    int4 v[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * nthr + (int)threadIdx.x;
+      if (i < 2 * total) {
+        const bool is_v = i >= total;
+        const int k = is_v ? i - total : i;
+        const int r = k / cpr, ch = k - r * cpr;
+        const int64_t j = c0 + r;
+        const uint8_t *src;
+        if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
+        else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
+        v[u] = *((const int4 *)src + ch);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * nthr + (int)threadIdx.x;
+      if (i < 2 * total) {
+        const bool is_v = i >= total;
+        const int k = is_v ? i - total : i;
+        *((int4 *)((is_v ? sv : sk)) + k) = v[u];
+      }
+    }
+  }
+}
+
+template <int KVT, int QT, int G, int D, int T>
+__global__ void __launch_bounds__(256)
+decode_split_kernel(const DecodeArgs a) {
+  constexpr int DPL = D / 32;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int split = blockIdx.x, b = blockIdx.y;
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+  const int64_t cs = (int64_t)split * a.split_cells;
+  const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
+  if (cs >= ce) return;                               // split beyond the context: never combined
+  const int64_t rb = a.row_bytes;
+  uint8_t *sk = smem;
+  uint8_t *sv = smem + (size_t)T * rb;
+
+  float qv[G][DPL], acc[G][DPL], m[G], l[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint16_t *qh = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + g * G + h) * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) {
+      qv[h][i] = h2f(qh[i], QT) * a.scale_log2;
+      acc[h][i] = 0.f;
+    }
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+  }
+
+  for (int64_t t0 = cs; t0 < ce; t0 += T) {
+    const int n = ce - t0 < T ? (int)(ce - t0) : T;
+    __syncthreads();                                  // previous tile fully consumed
+    load_tile(a, b, t0, n, sk, sv);
+    __syncthreads();
+    float s_mine[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s_mine[h] = -INFINITY;
+    for (int c = 0; c < n; ++c) {
+      float kd[DPL];
+      lane_dims<KVT, D>(sk + (size_t)c * rb, g, lane, kd);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float p = 0.f;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) p = fmaf(qv[h][i], kd[i], p);
+        p = warp_sum(p);
+        if (lane == c) s_mine[h] = p;
+      }
+    }
+    float p_mine[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float mt = warp_max(s_mine[h]);
+      const float m_new = fmaxf(m[h], mt);
+      const float alpha = exp2f(m[h] - m_new);
+      const float p = lane < n ? exp2f(s_mine[h] - m_new) : 0.f;
+      l[h] = l[h] * alpha + warp_sum(p);
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[h][i] *= alpha;
+      m[h] = m_new;
+      p_mine[h] = p;
+    }
+    for (int c = 0; c < n; ++c) {
+      float vd[DPL];
+      lane_dims<KVT, D>(sv + (size_t)c * rb, g, lane, vd);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float pc = __shfl_sync(0xffffffffu, p_mine[h], c);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(pc, vd[i], acc[h][i]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const int qh = g * G + h;
+    const size_t pi = ((size_t)b * a.n_splits + split) * a.n_q_heads + qh;
+    float *pa = a.part_acc + pi * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) pa[i] = acc[h][i];
+    if (lane == 0) {
+      a.part_ml[pi * 2] = m[h];
+      a.part_ml[pi * 2 + 1] = l[h];
+    }
+  }
+}
+
+// Fold the splits of one (sequence, q head) in ascending split order:
+// weights 2^(m_s - M) with M the maximum, out = acc / max(l, 1e-30).
+static __global__ void decode_combine_kernel(const DecodeArgs a) {
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int D = a.head_dim;
+  const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+  const int ns = ctx > 0 ? (int)((ctx + a.split_cells - 1) / a.split_cells) : 0;
+  const size_t base = (size_t)b * a.n_splits * a.n_q_heads + h;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[(base + (size_t)s * a.n_q_heads) * 2]);
+  float l = 0.f, acc = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const size_t pi = base + (size_t)s * a.n_q_heads;
+    const float w = exp2f(a.part_ml[pi * 2] - M);
+    l = fmaf(w, a.part_ml[pi * 2 + 1], l);
+    acc = fmaf(w, a.part_acc[pi * D + d], acc);
+  }
+  a.out[((size_t)b * a.n_q_heads + h) * D + d] = acc / fmaxf(l, 1e-30f);
+}
+
+template <int KVT, int QT, int G, int D, int T>
+cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
+  const size_t smem = (size_t)2 * T * a.row_bytes;
+  auto k = decode_split_kernel<KVT, QT, G, D, T>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_splits, a.batch);
+  k<<<grid, 32 * a.n_kv_heads, smem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<<<dim3(a.n_q_heads, a.batch), a.head_dim, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int KVT, int QT, int G, int D>
+cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
+  if ((size_t)2 * 32 * a.row_bytes <= 73728) return launch_t<KVT, QT, G, D, 32>(a, st);
+  return launch_t<KVT, QT, G, D, 16>(a, st);
+}
+
+template <int KVT, int QT, int G>
+cudaError_t launch_g(const DecodeArgs &a, cudaStream_t st) {
+  if (a.head_dim == 128) return launch_d<KVT, QT, G, 128>(a, st);
+  return launch_d<KVT, QT, G, 64>(a, st);
+}
+
+template <int KVT, int QT>
+cudaError_t launch_q(const DecodeArgs &a, cudaStream_t st) {
+  switch (a.group) {
+    case 1: return launch_g<KVT, QT, 1>(a, st);
+    case 2: return launch_g<KVT, QT, 2>(a, st);
+    case 3: return launch_g<KVT, QT, 3>(a, st);
+    case 4: return launch_g<KVT, QT, 4>(a, st);
+    case 5: return launch_g<KVT, QT, 5>(a, st);
+    case 6: return launch_g<KVT, QT, 6>(a, st);
+    case 7: return launch_g<KVT, QT, 7>(a, st);
+    default: return launch_g<KVT, QT, 8>(a, st);
+  }
+}
+
+template <int KVT>
+cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
+  if (a.q_dtype == KVO_BF16) return launch_q<KVT, KVO_BF16>(a, st);
+  return launch_q<KVT, KVO_F16>(a, st);
+}
+
+}  // namespace dec
+}  // namespace kvo

@@ -1,0 +1,442 @@
+// libkvo C ABI: argument validation and dispatch.  Declarations, argument
+// meaning, layout and error behaviour are documented in include/kvo.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+static thread_local char g_last_error[512];
+
+int fail(int st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+int cuda_status(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return KVO_OK;
+  return fail(KVO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static int classify_one(const void *p, cudaPointerAttributes *a) {
+  if (cudaPointerGetAttributes(a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return 0;
+  }
+  if (a->type == cudaMemoryTypeDevice || a->type == cudaMemoryTypeManaged) return kDeviceMem;
+  if (a->type == cudaMemoryTypeHost && a->devicePointer == p) return kMappedHost;
+  return 0;
+}
+
+int classify(const void *p, size_t bytes) {
+  if (p == nullptr) return 0;
+  cudaPointerAttributes a, b;
+  int k = classify_one(p, &a);
+  if (!k || bytes <= 1) return k;
+  const char *last = (const char *)p + (bytes - 1);
+  int k2 = classify_one(last, &b);
+  return k2 == k ? k : 0;
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 148;
+  }
+  return cached[dev];
+}
+
+}  // namespace kvo
+
+using namespace kvo;
+
+extern "C" {
+
+const char *kvo_status_string(int status) {
+  switch (status) {
+    case KVO_OK: return "ok";
+    case KVO_ERR_ARG: return "invalid argument";
+    case KVO_ERR_ALIGN: return "misaligned pointer or size";
+    case KVO_ERR_NOT_MAPPED: return "buffer is not device-accessible";
+    case KVO_ERR_UNSUPPORTED: return "unsupported combination";
+    case KVO_ERR_CUDA: return "CUDA error";
+    case KVO_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+const char *kvo_last_error(void) { return g_last_error; }
+
+int kvo_device_errors(uint32_t *bits, int clear) {
+  clear_error();
+  if (!bits) return fail(KVO_ERR_ARG, "kvo_device_errors: bits is NULL");
+  uint32_t *w = device_error_word();
+  if (!w) return fail(KVO_ERR_CUDA, "kvo_device_errors: no device error word");
+  int st = cuda_status(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (st) return st;
+  st = cuda_status(cudaMemcpy(bits, w, sizeof(uint32_t), cudaMemcpyDeviceToHost), "cudaMemcpy");
+  if (st) return st;
+  if (clear) st = cuda_status(cudaMemset(w, 0, sizeof(uint32_t)), "cudaMemset");
+  return st;
+}
+
+// ---------------------------------------------------------------- a1
+int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids, int64_t blocks_per_chunk,
+                       int64_t skip_count, uint64_t base, int64_t row_stride_bytes,
+                       int64_t row_bytes, int64_t *out, int64_t n_out) {
+  clear_error();
+  if (n_ids < 0 || n_out < 0 || row_stride_bytes < 0 || row_bytes < 0)
+    return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: negative size");
+  if (blocks_per_chunk < 1) return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: blocks_per_chunk < 1");
+  if (skip_count < 0 || skip_count >= blocks_per_chunk)
+    return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: skip_count %lld not in [0, blocks_per_chunk)",
+                (long long)skip_count);
+  if (blocks_per_chunk > 1 && row_bytes % blocks_per_chunk != 0)
+    return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: row_bytes %% blocks_per_chunk != 0");
+  if (n_out + skip_count > n_ids * blocks_per_chunk)
+    return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: n_out + skip exceeds n_ids * blocks_per_chunk");
+  if (n_out == 0) return KVO_OK;
+  if (!block_ids || !out) return fail(KVO_ERR_ARG, "kvo_sub_block_ptrs: NULL array");
+  const uint64_t stride = (uint64_t)row_stride_bytes;
+  if (blocks_per_chunk == 1) {
+    for (int64_t i = 0; i < n_out; ++i)
+      out[i] = (int64_t)(base + (uint64_t)block_ids[i] * stride);
+    return KVO_OK;
+  }
+  // Walk the flattened grid from (k, j) = divmod(skip, bpc) without a divide
+  // per element.
+  const uint64_t page = (uint64_t)(row_bytes / blocks_per_chunk);
+  int64_t k = 0, j = skip_count;
+  uint64_t row = base + (uint64_t)block_ids[0] * stride;
+  for (int64_t i = 0; i < n_out; ++i) {
+    out[i] = (int64_t)(row + (uint64_t)j * page);
+    if (++j == blocks_per_chunk) {
+      j = 0;
+      if (++k < n_ids) row = base + (uint64_t)block_ids[k] * stride;
+    }
+  }
+  return KVO_OK;
+}
+
+// ---------------------------------------------------------------- a2
+int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst, const int64_t *sizes,
+                          int64_t n, uint32_t flags, void *stream) {
+  clear_error();
+  cudaStream_t st = (cudaStream_t)stream;
+  if (n < 0) return fail(KVO_ERR_ARG, "kvo_swap_blocks_batch: n < 0");
+  if (n == 0) return KVO_OK;
+  if (!src || !dst || !sizes) return fail(KVO_ERR_ARG, "kvo_swap_blocks_batch: NULL descriptor array");
+  if ((flags & KVO_SWAP_FORCE_SM) && (flags & KVO_SWAP_FORCE_CE))
+    return fail(KVO_ERR_ARG, "kvo_swap_blocks_batch: both FORCE_SM and FORCE_CE");
+  const size_t db = (size_t)n * sizeof(int64_t);
+  int ks = classify(src, db), kd = classify(dst, db), kz = classify(sizes, db);
+  bool use_ce;
+  if (flags & KVO_SWAP_FORCE_CE) {
+    use_ce = true;
+  } else if (flags & KVO_SWAP_FORCE_SM) {
+    use_ce = false;
+  } else {
+    // Measured crossover: the copy engine only pays off when each call moves
+    // enough bytes to hide its ~2.7 us issue cost.  The mean needs the sizes
+    // on the host, which pinned descriptor arrays allow.
+    use_ce = false;
+    if (kz == kMappedHost) {
+      long double total = 0;
+      for (int64_t i = 0; i < n; ++i) total += (long double)sizes[i];
+      use_ce = total / (long double)n >= (long double)KVO_SWAP_CE_MIN_MEAN_BYTES;
+    }
+  }
+  if (use_ce) {
+    if (ks != kMappedHost || kd != kMappedHost || kz != kMappedHost)
+      return fail(KVO_ERR_NOT_MAPPED,
+                  "kvo_swap_blocks_batch: copy-engine mode needs pinned host descriptor arrays");
+    // Merge runs whose source and destination both continue the previous
+    // descriptor: fewer, larger copy-engine calls.
+    int64_t i = 0;
+    while (i < n) {
+      if (sizes[i] < 0) return fail(KVO_ERR_ARG, "kvo_swap_blocks_batch: negative size at %lld", (long long)i);
+      int64_t s = src[i], d = dst[i], len = sizes[i];
+      int64_t j = i + 1;
+      while (j < n && sizes[j] >= 0 && src[j] == s + len && dst[j] == d + len) { len += sizes[j]; ++j; }
+      if (len > 0) {
+        cudaError_t e = cudaMemcpyAsync((void *)(uintptr_t)d, (const void *)(uintptr_t)s, (size_t)len,
+                                        cudaMemcpyDefault, st);
+        if (e != cudaSuccess) return cuda_status(e, "cudaMemcpyAsync");
+      }
+      i = j;
+    }
+    return KVO_OK;
+  }
+  if (!ks || !kd || !kz)
+    return fail(KVO_ERR_NOT_MAPPED,
+                "kvo_swap_blocks_batch: descriptor arrays must be device-accessible (pinned host or device)");
+  return cuda_status(launch_swap_sm(src, dst, sizes, n, (flags & KVO_SWAP_SRC_ORDER_ANY) != 0, st),
+                     "swap kernel launch");
+}
+
+// ---------------------------------------------------------------- a3
+int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
+                      int64_t seq_stride_tokens, int64_t n_kv_heads, int64_t head_dim, int dtype,
+                      int64_t block_tokens, const int32_t *sel, int64_t n_sel, void *k_out,
+                      void *v_out, void *stream) {
+  clear_error();
+  if (n_seq < 0 || seq_stride_tokens < 0 || n_kv_heads < 1 || head_dim < 1 || block_tokens < 1 ||
+      n_sel < 0)
+    return fail(KVO_ERR_ARG, "kvo_gather_blocks: bad size");
+  if (dtype == KVO_Q8_0) return fail(KVO_ERR_UNSUPPORTED, "kvo_gather_blocks: q8_0 planes");
+  if (dtype != KVO_F16 && dtype != KVO_BF16) return fail(KVO_ERR_ARG, "kvo_gather_blocks: dtype");
+  if (n_seq == 0 || n_sel == 0) return KVO_OK;
+  const int64_t head_bytes = head_dim * 2;
+  if (head_bytes % 16) return fail(KVO_ERR_ALIGN, "kvo_gather_blocks: head_dim*2 not a multiple of 16");
+  if (!aligned16(k_plane) || !aligned16(v_plane) || !aligned16(k_out) || !aligned16(v_out))
+    return fail(KVO_ERR_ALIGN, "kvo_gather_blocks: buffers must be 16-byte aligned");
+  const size_t plane_bytes = (size_t)n_seq * seq_stride_tokens * n_kv_heads * head_bytes;
+  const size_t out_bytes = (size_t)n_seq * n_sel * block_tokens * n_kv_heads * head_bytes;
+  if (!classify(k_plane, plane_bytes) || !classify(v_plane, plane_bytes))
+    return fail(KVO_ERR_NOT_MAPPED, "kvo_gather_blocks: planes are not device-accessible");
+  if (!classify(k_out, out_bytes) || !classify(v_out, out_bytes))
+    return fail(KVO_ERR_NOT_MAPPED, "kvo_gather_blocks: outputs are not device-accessible");
+  if (!classify(sel, (size_t)n_seq * n_kv_heads * n_sel * 4))
+    return fail(KVO_ERR_NOT_MAPPED, "kvo_gather_blocks: sel is not device-accessible");
+  uint32_t *err = device_error_word();
+  if (!err) return fail(KVO_ERR_CUDA, "kvo_gather_blocks: device error word unavailable");
+  return cuda_status(launch_gather(k_plane, v_plane, n_seq, seq_stride_tokens, n_kv_heads, head_bytes,
+                                   block_tokens, sel, n_sel, k_out, v_out, err,
+                                   (cudaStream_t)stream),
+                     "gather kernel launch");
+}
+
+// ---------------------------------------------------------------- a4-a6
+size_t kvo_attn_decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t head_dim,
+                                       int64_t max_ctx) {
+  if (batch < 0 || n_q_heads < 0 || head_dim < 0 || max_ctx < 0) return 0;
+  return decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx);
+}
+
+static int64_t kv_row_bytes(int dt, int64_t hkv, int64_t d) {
+  if (dt == KVO_F16 || dt == KVO_BF16) return hkv * d * 2;
+  if (dt == KVO_Q8_0) return (d % 32) ? -1 : hkv * (d / 32) * 34;
+  return -1;
+}
+
+int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_q_heads,
+                           int64_t n_kv_heads, int64_t head_dim, const void *k_vram,
+                           const void *v_vram, int64_t vram_seq_stride_rows, const void *k_host,
+                           const void *v_host, int64_t host_seq_stride_rows, int kv_dtype,
+                           const int32_t *ctx_len, int64_t max_ctx, int64_t n_vram_cells,
+                           float scale, void *staging_k, void *staging_v, float *out,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+  clear_error();
+  cudaStream_t st = (cudaStream_t)stream;
+  if (batch < 0 || max_ctx < 0 || n_vram_cells < 0 || n_q_heads < 1 || n_kv_heads < 1)
+    return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: bad size");
+  if (batch == 0) return KVO_OK;
+  if (q_dtype != KVO_F16 && q_dtype != KVO_BF16)
+    return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_decode_tiered: q dtype must be f16 or bf16");
+  if (n_q_heads % n_kv_heads) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: n_q_heads %% n_kv_heads");
+  const int64_t group = n_q_heads / n_kv_heads;
+  if (group > 8 || n_kv_heads > 8 || (head_dim != 64 && head_dim != 128))
+    return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_decode_tiered: group %lld, kv heads %lld, head_dim %lld",
+                (long long)group, (long long)n_kv_heads, (long long)head_dim);
+  const int64_t rb = kv_row_bytes(kv_dtype, n_kv_heads, head_dim);
+  if (rb < 0) return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_decode_tiered: kv dtype");
+  if (rb % 16) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: cell row bytes %% 16 != 0");
+  if (!out || !q || !ctx_len) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: NULL q/out/ctx_len");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: q/out alignment");
+  const int64_t n_lo = n_vram_cells < max_ctx ? n_vram_cells : max_ctx;   // rows read from VRAM
+  const int64_t n_hi = max_ctx - n_lo;                                     // rows past N
+  if (n_lo > 0) {
+    if (vram_seq_stride_rows < n_lo) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: vram stride < cells");
+    const size_t bytes = (size_t)((batch - 1) * vram_seq_stride_rows + n_lo) * rb;
+    if (!aligned16(k_vram) || !aligned16(v_vram)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: vram alignment");
+    if (classify(k_vram, bytes) != kDeviceMem || classify(v_vram, bytes) != kDeviceMem)
+      return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_decode_tiered: k_vram/v_vram must be device memory");
+  }
+  const bool staged = staging_k != nullptr || staging_v != nullptr;
+  if (n_hi > 0) {
+    if (host_seq_stride_rows < n_hi) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: host stride < tail cells");
+    const size_t bytes = (size_t)((batch - 1) * host_seq_stride_rows + n_hi) * rb;
+    if (!aligned16(k_host) || !aligned16(v_host)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: host alignment");
+    if (!classify(k_host, bytes) || !classify(v_host, bytes))
+      return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_decode_tiered: k_host/v_host not device-accessible");
+    if (staged) {
+      const size_t sb = (size_t)batch * n_hi * rb;
+      if (!staging_k || !staging_v) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: one staging buffer is NULL");
+      if (!aligned16(staging_k) || !aligned16(staging_v)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: staging alignment");
+      if (classify(staging_k, sb) != kDeviceMem || classify(staging_v, sb) != kDeviceMem)
+        return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_decode_tiered: staging buffers must be device memory");
+    }
+  }
+  const size_t need = decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(KVO_ERR_WORKSPACE, "kvo_attn_decode_tiered: workspace needs %zu bytes", need);
+
+  DecodeArgs a;
+  a.q = q; a.q_dtype = q_dtype;
+  a.batch = (int)batch; a.n_q_heads = (int)n_q_heads; a.n_kv_heads = (int)n_kv_heads;
+  a.head_dim = (int)head_dim; a.group = (int)group;
+  a.k_lo = (const uint8_t *)k_vram; a.v_lo = (const uint8_t *)v_vram;
+  a.lo_seq_stride_rows = vram_seq_stride_rows;
+  a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host;
+  a.hi_seq_stride_rows = host_seq_stride_rows;
+  a.kv_dtype = kv_dtype; a.row_bytes = rb;
+  a.ctx_len = ctx_len; a.max_ctx = max_ctx; a.n_vram = n_lo;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  decode_geometry(batch, max_ctx, head_dim, &a.split_cells, &a.n_splits);
+  a.part_acc = (float *)workspace;
+  a.part_ml = a.part_acc + (size_t)batch * a.n_splits * n_q_heads * head_dim;
+
+  if (n_hi > 0 && staged) {
+    // Copy-engine staging of the host rows [N, max_ctx) into VRAM; the kernel
+    // then reads the all-VRAM view.  Same arithmetic, so the same bits.
+    for (int64_t b = 0; b < batch; ++b) {
+      const size_t bytes = (size_t)n_hi * rb;
+      const uint8_t *ks = (const uint8_t *)k_host + (size_t)b * host_seq_stride_rows * rb;
+      const uint8_t *vs = (const uint8_t *)v_host + (size_t)b * host_seq_stride_rows * rb;
+      uint8_t *kd = (uint8_t *)staging_k + (size_t)b * n_hi * rb;
+      uint8_t *vd = (uint8_t *)staging_v + (size_t)b * n_hi * rb;
+      int s1 = cuda_status(cudaMemcpyAsync(kd, ks, bytes, cudaMemcpyDefault, st), "staging copy K");
+      if (s1) return s1;
+      s1 = cuda_status(cudaMemcpyAsync(vd, vs, bytes, cudaMemcpyDefault, st), "staging copy V");
+      if (s1) return s1;
+    }
+    a.k_hi = (const uint8_t *)staging_k; a.v_hi = (const uint8_t *)staging_v;
+    a.hi_seq_stride_rows = n_hi;
+  }
+  return launch_decode(a, st);
+}
+
+// ---------------------------------------------------------------- a7-a8
+size_t kvo_attn_prefill_workspace_bytes(int64_t rows, int64_t n_q_heads) {
+  if (rows < 0 || n_q_heads < 0) return 0;
+  return (size_t)rows * n_q_heads * 2 * sizeof(float);
+}
+
+int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t n_q_heads,
+                            int64_t n_kv_heads, int64_t head_dim, const void *k_vram,
+                            const void *v_vram, const void *k_host, const void *v_host,
+                            int kv_dtype, int64_t ctx_len, int64_t n_vram_cells, float scale,
+                            void *arena, size_t arena_bytes, int64_t rows_per_launch, float *out,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  clear_error();
+  cudaStream_t st = (cudaStream_t)stream;
+  if (rows < 0 || q_pos0 < 0 || ctx_len < 0 || n_vram_cells < 0 || n_q_heads < 1 || n_kv_heads < 1)
+    return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: bad size");
+  if (rows == 0) return KVO_OK;
+  if (kv_dtype != KVO_F16 && kv_dtype != KVO_BF16)
+    return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_prefill_tiered: kv dtype must be f16 or bf16");
+  if (n_q_heads % n_kv_heads) return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: n_q_heads %% n_kv_heads");
+  const int64_t group = n_q_heads / n_kv_heads;
+  if (head_dim != 128 || (group != 1 && group != 2 && group != 4 && group != 8))
+    return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_prefill_tiered: head_dim %lld group %lld",
+                (long long)head_dim, (long long)group);
+  if (rows_per_launch <= 0) rows_per_launch = rows;
+  if (!q || !out) return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: NULL q/out");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: q/out alignment");
+  const int64_t rb = n_kv_heads * head_dim * 2;
+  // Cells any row can see: [0, min(ctx_len, q_pos0 + rows)).
+  const int64_t c_end = ctx_len < q_pos0 + rows ? ctx_len : q_pos0 + rows;
+  const int64_t n_lo = n_vram_cells < c_end ? n_vram_cells : c_end;
+  const int64_t n_hi = c_end - n_lo;
+  if (n_lo > 0) {
+    if (!aligned16(k_vram) || !aligned16(v_vram)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: vram alignment");
+    if (classify(k_vram, (size_t)n_lo * rb) != kDeviceMem || classify(v_vram, (size_t)n_lo * rb) != kDeviceMem)
+      return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: k_vram/v_vram must be device memory");
+  }
+  int64_t bucket = 0;
+  if (n_hi > 0) {
+    if (!aligned16(k_host) || !aligned16(v_host)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: host alignment");
+    if (!classify(k_host, (size_t)n_hi * rb) || !classify(v_host, (size_t)n_hi * rb))
+      return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: k_host/v_host not device-accessible");
+    if (arena) {
+      bucket = (int64_t)(arena_bytes / (2 * (size_t)rb));
+      if (bucket < 1) return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: arena holds no cell row");
+      if (!aligned16(arena)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: arena alignment");
+      if (classify(arena, (size_t)2 * bucket * rb) != kDeviceMem)
+        return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: arena must be device memory");
+    }
+  }
+  const size_t need = kvo_attn_prefill_workspace_bytes(rows, n_q_heads);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(KVO_ERR_WORKSPACE, "kvo_attn_prefill_tiered: workspace needs %zu bytes", need);
+
+  PrefillArgs a;
+  memset(&a, 0, sizeof(a));
+  a.n_q_heads = (int)n_q_heads; a.n_kv_heads = (int)n_kv_heads; a.head_dim = (int)head_dim;
+  a.group = (int)group; a.dtype = kv_dtype; a.row_bytes = rb;
+  a.k_lo = (const uint8_t *)k_vram; a.v_lo = (const uint8_t *)v_vram;
+  a.n_vram = n_lo;
+  a.scale_log2 = scale * 1.4426950408889634f;
+
+  // Segments of the visible cell range, in ascending order: the VRAM head,
+  // then either the whole host tail (direct) or its arena buckets (staged).
+  struct Seg { int64_t c0, c1; };
+  std::vector<Seg> segs;
+  if (n_lo > 0) segs.push_back({0, n_lo});
+  if (n_hi > 0) {
+    if (!arena) segs.push_back({n_lo, c_end});
+    else for (int64_t c = n_lo; c < c_end; c += bucket) segs.push_back({c, c + bucket < c_end ? c + bucket : c_end});
+  }
+  float *ml = (float *)workspace;
+  const uint8_t *k_arena = (const uint8_t *)arena;
+  const uint8_t *v_arena = arena ? (const uint8_t *)arena + (size_t)bucket * rb : nullptr;
+
+  for (size_t si = 0; si < segs.size(); ++si) {
+    const Seg s = segs[si];
+    const bool tail = s.c0 >= n_lo && n_hi > 0;
+    if (tail && arena) {
+      const size_t bytes = (size_t)(s.c1 - s.c0) * rb;
+      const uint8_t *ks = (const uint8_t *)k_host + (size_t)(s.c0 - n_lo) * rb;
+      const uint8_t *vs = (const uint8_t *)v_host + (size_t)(s.c0 - n_lo) * rb;
+      int e = cuda_status(cudaMemcpyAsync((void *)k_arena, ks, bytes, cudaMemcpyDefault, st), "arena copy K");
+      if (e) return e;
+      e = cuda_status(cudaMemcpyAsync((void *)v_arena, vs, bytes, cudaMemcpyDefault, st), "arena copy V");
+      if (e) return e;
+      a.k_hi = k_arena; a.v_hi = v_arena; a.hi_origin = s.c0;
+    } else if (tail) {
+      a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host; a.hi_origin = n_lo;
+    }
+    for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
+      const int64_t r1 = r0 + rows_per_launch < rows ? r0 + rows_per_launch : rows;
+      // Rows of this block see cells < q_pos0 + r1; the segments that can
+      // hold such cells are the ones starting before it.
+      const int64_t vis_end = q_pos0 + r1;
+      if (s.c0 >= vis_end) continue;
+      // The last segment this row block sees finalises it.
+      bool last = true;
+      if (si + 1 < segs.size() && segs[si + 1].c0 < vis_end) last = false;
+      a.q = (const uint16_t *)q + (size_t)r0 * n_q_heads * head_dim;
+      a.rows = (int)(r1 - r0);
+      a.pos0 = q_pos0 + r0;
+      a.c0 = s.c0;
+      a.c1 = s.c1 < vis_end ? s.c1 : vis_end;
+      a.acc = out + (size_t)r0 * n_q_heads * head_dim;
+      a.ml = ml + (size_t)r0 * n_q_heads * 2;
+      a.init = (si == 0);
+      a.finalize = last;
+      int e = launch_prefill(a, st);
+      if (e) return e;
+    }
+  }
+  if (segs.empty()) {
+    // Nothing visible (ctx_len == 0): the result is 0 by the 1e-30 clamp.
+    return cuda_status(cudaMemsetAsync(out, 0, (size_t)rows * n_q_heads * head_dim * sizeof(float), st),
+                       "cudaMemsetAsync");
+  }
+  return KVO_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Internal helpers shared by the libkvo translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/kvo.h"
+
+namespace kvo {
+
+// Record a one-line reason for the failing call (thread-local) and return st.
+int fail(int st, const char *fmt, ...);
+// Clear the thread-local reason at the start of an entry point.
+void clear_error();
+// Map a CUDA error to KVO_ERR_CUDA with its text; KVO_OK for cudaSuccess.
+int cuda_status(cudaError_t e, const char *what);
+
+enum Access { kDeviceMem = 1, kMappedHost = 2 };
+// Classify [p, p + bytes): returns kDeviceMem, kMappedHost or 0 (not
+// device-accessible: unregistered pageable memory, NULL, or a range that ends
+// outside the allocation that holds its first byte).
+int classify(const void *p, size_t bytes);
+
+int num_sms();                       // SMs of the current device (cached)
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Device-side error bits set by kernels that skipped an out-of-range item.
+enum DeviceErrorBits : uint32_t { kErrGatherSel = 1u };
+uint32_t *device_error_word();       // address of the per-device word (nullptr on failure)
+
+// Launchers implemented in the kernel translation units.  They assume the
+// entry point already validated every argument.
+cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes,
+                           int64_t n, bool src_readonly, cudaStream_t st);
+
+cudaError_t launch_gather(const void *k_plane, const void *v_plane, int64_t n_seq,
+                          int64_t seq_stride_tokens, int64_t n_kv_heads, int64_t head_bytes,
+                          int64_t block_tokens, const int32_t *sel, int64_t n_sel,
+                          void *k_out, void *v_out, uint32_t *err, cudaStream_t st);
+
+struct DecodeArgs {
+  const void *q; int q_dtype;
+  int batch, n_q_heads, n_kv_heads, head_dim, group;
+  const uint8_t *k_lo, *v_lo;  int64_t lo_seq_stride_rows;   // cells [0, N)
+  const uint8_t *k_hi, *v_hi;  int64_t hi_seq_stride_rows;   // cells [N, L), row j - N
+  int kv_dtype; int64_t row_bytes;
+  const int32_t *ctx_len; int64_t max_ctx, n_vram;
+  float scale_log2;            // scale * log2(e)
+  float *out;
+  float *part_acc, *part_ml;   // workspace: [B][splits][Hq][D], [B][splits][Hq][2]
+  int split_cells, n_splits;
+};
+// Split geometry for a decode: fixed cell ranges that depend on max_ctx and
+// batch only (never on N or on staging), so tiered and all-VRAM runs match.
+void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *split_cells,
+                     int *n_splits);
+size_t decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t head_dim,
+                              int64_t max_ctx);
+int launch_decode(const DecodeArgs &a, cudaStream_t st);   // kvo_status
+
+struct PrefillArgs {
+  const uint16_t *q;           // [rows][Hq][D] (rows of this launch start at q)
+  int rows;                    // rows in this launch
+  int64_t pos0;                // position of the first row of this launch
+  int n_q_heads, n_kv_heads, head_dim, group, dtype;
+  int64_t row_bytes;
+  const uint8_t *k_lo, *v_lo;  // cells < N: k_lo + j * row_bytes
+  const uint8_t *k_hi, *v_hi;  // cells >= N: k_hi + (j - hi_origin) * row_bytes
+  int64_t hi_origin, n_vram;
+  int64_t c0, c1;              // cell range of this launch
+  float scale_log2;
+  float *acc;                  // [rows][Hq][D] running accumulator / output
+  float *ml;                   // [rows][Hq][2] running (m, l) in log2 units
+  int init, finalize;
+};
+int launch_prefill(const PrefillArgs &a, cudaStream_t st);  // kvo_status
+
+}  // namespace kvo

@@ -1,0 +1,161 @@
+// Batched block swap and top-k block gather: SM copy kernels that read and
+// write pinned host memory through the device mapping (16-byte vectors,
+// coalesced across a warp, several loads in flight per lane).
+//
+// On GB300 the host link (NVLink-C2C) is saturated by SM loads from about
+// one CTA of 256 threads per SM, at the same bandwidth as the copy engine,
+// while a copy-engine call costs ~2.7 us to issue: for page-sized copies a
+// warp-per-descriptor kernel is the fast path.
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+namespace {
+
+constexpr int kSwapThreads = 256;
+constexpr int kUnroll = 4;
+
+// Copy `bytes` from s to d with one warp.  16-byte vectors when both
+// addresses and the size allow, else 8-, 4- or 1-byte units.
+__device__ __forceinline__ void warp_copy(const char *s, char *d, int64_t bytes, int lane) {
+  const uintptr_t mis = ((uintptr_t)s | (uintptr_t)d | (uintptr_t)bytes);
+  if ((mis & 15) == 0) {
+    const int4 *s4 = (const int4 *)s;
+    int4 *d4 = (int4 *)d;
+    const int64_t n = bytes >> 4;
+    int64_t i = lane;
+    for (; i + (kUnroll - 1) * 32 < n; i += kUnroll * 32) {
+      int4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = s4[i + u * 32];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) d4[i + u * 32] = v[u];
+    }
+    for (; i < n; i += 32) d4[i] = s4[i];
+  } else if ((mis & 7) == 0) {
+    const int64_t n = bytes >> 3;
+    for (int64_t i = lane; i < n; i += 32) ((int2 *)d)[i] = ((const int2 *)s)[i];
+  } else if ((mis & 3) == 0) {
+    const int64_t n = bytes >> 2;
+    for (int64_t i = lane; i < n; i += 32) ((int *)d)[i] = ((const int *)s)[i];
+  } else {
+    for (int64_t i = lane; i < bytes; i += 32) d[i] = s[i];
+  }
+}
+
+// One warp per descriptor, grid-stride over descriptors.
+__global__ void __launch_bounds__(kSwapThreads)
+swap_kernel(const int64_t *__restrict__ src, const int64_t *__restrict__ dst,
+            const int64_t *__restrict__ sizes, int64_t n) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kSwapThreads + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * kSwapThreads) >> 5;
+  for (int64_t i = warp; i < n; i += n_warps) {
+    const int64_t bytes = sizes[i];
+    if (bytes <= 0) continue;
+    warp_copy((const char *)(uintptr_t)src[i], (char *)(uintptr_t)dst[i], bytes, lane);
+  }
+}
+
+// Gather: one warp per (plane, seq, kv head, rank) block of block_tokens
+// token rows of head_bytes each; source and destination rows are strided by
+// n_kv_heads * head_bytes.  Index order of work items: rank fastest, so
+// neighbouring warps read neighbouring selections of one (seq, head).
+__global__ void __launch_bounds__(kSwapThreads)
+gather_kernel(const char *__restrict__ k_plane, const char *__restrict__ v_plane, int64_t n_seq,
+              int64_t seq_stride_tokens, int64_t n_kv_heads, int64_t head_bytes,
+              int64_t block_tokens, const int32_t *__restrict__ sel, int64_t n_sel,
+              char *__restrict__ k_out, char *__restrict__ v_out, uint32_t *err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kSwapThreads + threadIdx.x) >> 5;
+  const int64_t n_warps = ((int64_t)gridDim.x * kSwapThreads) >> 5;
+  const int64_t per_plane = n_seq * n_kv_heads * n_sel;
+  const int64_t n_blocks_plane = seq_stride_tokens / block_tokens;
+  const int64_t row_stride = n_kv_heads * head_bytes;        // bytes between token rows
+  const int64_t chunks_per_row = head_bytes >> 4;
+  const int64_t chunks = block_tokens * chunks_per_row;
+  const int64_t out_tokens = n_sel * block_tokens;
+  for (int64_t item = warp; item < 2 * per_plane; item += n_warps) {
+    const bool is_v = item >= per_plane;
+    const int64_t w = is_v ? item - per_plane : item;       // (s, h, r), r fastest
+    const int64_t r = w % n_sel;
+    const int64_t sh = w / n_sel;
+    const int64_t h = sh % n_kv_heads;
+    const int64_t s = sh / n_kv_heads;
+    const int64_t blk = sel[w];
+    if (blk < 0 || blk >= n_blocks_plane) {
+      if (lane == 0) atomicOr(err, (uint32_t)kErrGatherSel);
+      continue;
+    }
+    const char *src = (is_v ? v_plane : k_plane) +
+                      ((s * seq_stride_tokens + blk * block_tokens) * n_kv_heads + h) * head_bytes;
+    char *dst = (is_v ? v_out : k_out) +
+                ((s * out_tokens + r * block_tokens) * n_kv_heads + h) * head_bytes;
+    int64_t c = lane;
+    for (; c + (kUnroll - 1) * 32 < chunks; c += kUnroll * 32) {
+      int4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t cc = c + u * 32;
+        v[u] = *((const int4 *)(src + (cc / chunks_per_row) * row_stride) + cc % chunks_per_row);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t cc = c + u * 32;
+        *((int4 *)(dst + (cc / chunks_per_row) * row_stride) + cc % chunks_per_row) = v[u];
+      }
+    }
+    for (; c < chunks; c += 32)
+      *((int4 *)(dst + (c / chunks_per_row) * row_stride) + c % chunks_per_row) =
+          *((const int4 *)(src + (c / chunks_per_row) * row_stride) + c % chunks_per_row);
+  }
+}
+
+__device__ uint32_t g_device_errors;
+
+}  // namespace
+
+uint32_t *device_error_word() {
+  static uint32_t *cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_errors) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    cached[dev] = (uint32_t *)p;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes, int64_t n,
+                           bool src_readonly, cudaStream_t st) {
+  const int64_t warps_per_cta = kSwapThreads / 32;
+  int64_t grid = (n + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = (int64_t)num_sms() * 8;      // 8 CTAs of 8 warps per SM in flight
+  if (grid > cap) grid = cap;
+  // Every copy here is stream-ordered, which already satisfies both source
+  // access orders; the read-only hint needs no separate kernel.
+  (void)src_readonly;
+  swap_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(src, dst, sizes, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void *k_plane, const void *v_plane, int64_t n_seq,
+                          int64_t seq_stride_tokens, int64_t n_kv_heads, int64_t head_bytes,
+                          int64_t block_tokens, const int32_t *sel, int64_t n_sel, void *k_out,
+                          void *v_out, uint32_t *err, cudaStream_t st) {
+  const int64_t items = 2 * n_seq * n_kv_heads * n_sel;
+  const int64_t warps_per_cta = kSwapThreads / 32;
+  int64_t grid = (items + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (grid > cap) grid = cap;
+  gather_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(
+      (const char *)k_plane, (const char *)v_plane, n_seq, seq_stride_tokens, n_kv_heads, head_bytes,
+      block_tokens, sel, n_sel, (char *)k_out, (char *)v_out, err);
+  return cudaGetLastError();
+}
+
+}  // namespace kvo

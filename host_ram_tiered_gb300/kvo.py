@@ -1,0 +1,161 @@
+"""Thin ctypes binding of libkvo (include/kvo.h), same names as the C ABI.
+
+Argument marshalling only: every step of the path runs in the library's
+CUDA kernels.  Buffers may be passed as torch tensors (their data pointer is
+used) or as integer addresses; streams as ``torch.cuda.Stream`` or a raw
+handle.  A non-zero status raises :class:`KvoError`.  If the library has
+not been built, loading it raises: there is no Python or CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+F16, BF16, Q8_0 = 0, 1, 2
+KVO_SWAP_H2D = 0x1
+KVO_SWAP_D2H = 0x2
+KVO_SWAP_SRC_ORDER_ANY = 0x4
+KVO_SWAP_FORCE_SM = 0x8
+KVO_SWAP_FORCE_CE = 0x10
+KVO_SWAP_CE_MIN_MEAN_BYTES = 1 << 20
+
+STATUS = {0: "KVO_OK", -1: "KVO_ERR_ARG", -2: "KVO_ERR_ALIGN", -3: "KVO_ERR_NOT_MAPPED",
+          -4: "KVO_ERR_UNSUPPORTED", -5: "KVO_ERR_CUDA", -6: "KVO_ERR_WORKSPACE"}
+
+# Every symbol include/kvo.h declares, with (restype, argtypes).
+_i64, _u64, _vp, _u32, _int, _f32, _sz = (ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
+                                          ctypes.c_uint32, ctypes.c_int, ctypes.c_float,
+                                          ctypes.c_size_t)
+SIGNATURES = {
+    "kvo_status_string": (ctypes.c_char_p, [_int]),
+    "kvo_last_error": (ctypes.c_char_p, []),
+    "kvo_device_errors": (_int, [_vp, _int]),
+    "kvo_sub_block_ptrs": (_int, [_vp, _i64, _i64, _i64, _u64, _i64, _i64, _vp, _i64]),
+    "kvo_swap_blocks_batch": (_int, [_vp, _vp, _vp, _i64, _u32, _vp]),
+    "kvo_gather_blocks": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _i64, _vp, _i64, _vp,
+                                 _vp, _vp]),
+    "kvo_attn_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "kvo_attn_decode_tiered": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp,
+                                      _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz,
+                                      _vp]),
+    "kvo_attn_prefill_workspace_bytes": (_sz, [_i64, _i64]),
+    "kvo_attn_prefill_tiered": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                       _int, _i64, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz,
+                                       _vp]),
+}
+
+
+class KvoError(RuntimeError):
+    def __init__(self, status: int, func: str, detail: str):
+        self.status = status
+        super().__init__(f"{func}: {STATUS.get(status, status)}: {detail}")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the in-tree libkvo.so (build it first with build.build())."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise ImportError(f"libkvo.so is not built ({path}); run host_ram_tiered_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(x) -> int | None:
+    """Address of a tensor / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _s(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, name: str) -> None:
+    if st != 0:
+        raise KvoError(st, name, load().kvo_last_error().decode(errors="replace"))
+
+
+def kvo_status_string(status: int) -> str:
+    return load().kvo_status_string(status).decode()
+
+
+def kvo_last_error() -> str:
+    return load().kvo_last_error().decode(errors="replace")
+
+
+def kvo_device_errors(clear: bool = True) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(load().kvo_device_errors(ctypes.addressof(bits), int(clear)), "kvo_device_errors")
+    return bits.value
+
+
+def kvo_sub_block_ptrs(block_ids, n_ids, blocks_per_chunk, skip_count, base, row_stride_bytes,
+                       row_bytes, out, n_out) -> None:
+    _check(load().kvo_sub_block_ptrs(_p(block_ids), n_ids, blocks_per_chunk, skip_count, base,
+                                     row_stride_bytes, row_bytes, _p(out), n_out),
+           "kvo_sub_block_ptrs")
+
+
+def kvo_swap_blocks_batch(src, dst, sizes, n, flags, stream=None) -> None:
+    _check(load().kvo_swap_blocks_batch(_p(src), _p(dst), _p(sizes), n, flags, _s(stream)),
+           "kvo_swap_blocks_batch")
+
+
+def kvo_gather_blocks(k_plane, v_plane, n_seq, seq_stride_tokens, n_kv_heads, head_dim, dtype,
+                      block_tokens, sel, n_sel, k_out, v_out, stream=None) -> None:
+    _check(load().kvo_gather_blocks(_p(k_plane), _p(v_plane), n_seq, seq_stride_tokens, n_kv_heads,
+                                    head_dim, dtype, block_tokens, _p(sel), n_sel, _p(k_out),
+                                    _p(v_out), _s(stream)), "kvo_gather_blocks")
+
+
+def kvo_attn_decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx) -> int:
+    return load().kvo_attn_decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx)
+
+
+def kvo_attn_decode_tiered(q, q_dtype, batch, n_q_heads, n_kv_heads, head_dim, k_vram, v_vram,
+                           vram_seq_stride_rows, k_host, v_host, host_seq_stride_rows, kv_dtype,
+                           ctx_len, max_ctx, n_vram_cells, scale, staging_k, staging_v, out,
+                           workspace, workspace_bytes, stream=None) -> None:
+    _check(load().kvo_attn_decode_tiered(
+        _p(q), q_dtype, batch, n_q_heads, n_kv_heads, head_dim, _p(k_vram), _p(v_vram),
+        vram_seq_stride_rows, _p(k_host), _p(v_host), host_seq_stride_rows, kv_dtype, _p(ctx_len),
+        max_ctx, n_vram_cells, scale, _p(staging_k), _p(staging_v), _p(out), _p(workspace),
+        workspace_bytes, _s(stream)), "kvo_attn_decode_tiered")
+
+
+def kvo_attn_prefill_workspace_bytes(rows, n_q_heads) -> int:
+    return load().kvo_attn_prefill_workspace_bytes(rows, n_q_heads)
+
+
+def kvo_attn_prefill_tiered(q, rows, q_pos0, n_q_heads, n_kv_heads, head_dim, k_vram, v_vram,
+                            k_host, v_host, kv_dtype, ctx_len, n_vram_cells, scale, arena,
+                            arena_bytes, rows_per_launch, out, workspace, workspace_bytes,
+                            stream=None) -> None:
+    _check(load().kvo_attn_prefill_tiered(
+        _p(q), rows, q_pos0, n_q_heads, n_kv_heads, head_dim, _p(k_vram), _p(v_vram), _p(k_host),
+        _p(v_host), kv_dtype, ctx_len, n_vram_cells, scale, _p(arena), arena_bytes,
+        rows_per_launch, _p(out), _p(workspace), workspace_bytes, _s(stream)),
+        "kvo_attn_prefill_tiered")

@@ -1,0 +1,254 @@
+/*
+ * kvo.h -- C ABI of libkvo, a GB300 (sm_103a) library for an LLM KV cache
+ * that lives partly in VRAM and partly in pinned, device-mapped host memory.
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns every buffer.  The library allocates no memory.
+ *   - "device-accessible" means device memory (cudaMalloc / a framework's
+ *     allocator) or pinned host memory that is mapped into the device's
+ *     address space (cudaHostAlloc(..., Mapped) / cudaHostRegister(...,
+ *     Mapped)); both are passed by the same unified virtual address.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All calls except kvo_sub_block_ptrs are stream-ordered and
+ *     asynchronous: they return once the work is enqueued, do no host
+ *     synchronisation, and every buffer must stay valid until the stream has
+ *     passed the enqueued work.
+ *   - Every call returns a kvo_status.  Nothing aborts or throws.  An
+ *     argument the host can check is rejected before anything is enqueued;
+ *     kvo_last_error() then holds a one-line reason (thread-local).
+ *     Asynchronous CUDA faults surface as KVO_ERR_CUDA on a later call or at
+ *     the caller's synchronisation.  Values the host cannot see (selected
+ *     block ids in device memory) are range-checked by the kernels, which
+ *     skip an out-of-range item and set a bit read by kvo_device_errors().
+ *   - There is no CPU fallback: a combination a kernel does not implement
+ *     returns KVO_ERR_UNSUPPORTED.
+ */
+#ifndef KVO_H
+#define KVO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVO_OK = 0,
+  KVO_ERR_ARG = -1,          /* a size, count or pointer is invalid            */
+  KVO_ERR_ALIGN = -2,        /* a pointer or row size breaks a 16-byte rule    */
+  KVO_ERR_NOT_MAPPED = -3,   /* a buffer is not device-accessible              */
+  KVO_ERR_UNSUPPORTED = -4,  /* dtype / head_dim / group size not implemented  */
+  KVO_ERR_CUDA = -5,         /* a CUDA runtime call failed                     */
+  KVO_ERR_WORKSPACE = -6     /* workspace missing or smaller than required     */
+} kvo_status;
+
+typedef enum {
+  KVO_F16 = 0,   /* IEEE binary16                                           */
+  KVO_BF16 = 1,  /* bfloat16                                                */
+  KVO_Q8_0 = 2   /* 34-byte block {fp16 d; int8 qs[32]}, value = d * qs[i];   */
+                 /* a cell row holds n_kv_heads heads of head_dim/32 blocks  */
+} kvo_dtype;
+
+/* Static text for a status code. */
+const char *kvo_status_string(int status);
+
+/* Detail of the last failing call on this host thread ("" if none). */
+const char *kvo_last_error(void);
+
+/* Bits set by kernels that skipped an out-of-range item (bit 0: a gather
+ * selection outside its plane).  Synchronises the device; clears the bits
+ * when `clear` is non-zero.  For tests and debugging, not for hot loops. */
+int kvo_device_errors(uint32_t *bits, int clear);
+
+/* ------------------------------------------------------------------------
+ * kvo_sub_block_ptrs -- host function, synchronous, no CUDA.
+ *
+ * vLLM gpu_worker.py (v1 CPU KV offload), compute_sub_block_ptrs: block b
+ * of a paged tensor is split into blocks_per_chunk sub-blocks of
+ * page = row_bytes / blocks_per_chunk bytes; sub-block j of block b is at
+ *     base + b * row_stride_bytes + j * page.
+ * The (n_ids x blocks_per_chunk) grid is flattened row-major and
+ *     out[i] = flat[skip_count + i],  0 <= i < n_out
+ * i.e. (k, j) = divmod(i + skip_count, blocks_per_chunk), block b = ids[k].
+ * row_stride_bytes may exceed row_bytes (a non-contiguous host tensor).
+ *
+ * block_ids: host int64[n_ids]; out: host int64[n_out] (addresses as int64,
+ * the descriptor type kvo_swap_blocks_batch takes).
+ * Errors: KVO_ERR_ARG if skip_count >= blocks_per_chunk (the page's assert),
+ * row_bytes % blocks_per_chunk != 0 with blocks_per_chunk > 1 (the page's
+ * assert), n_out + skip_count > n_ids * blocks_per_chunk, a negative size,
+ * or a NULL array with a non-zero count.
+ * ---------------------------------------------------------------------- */
+int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
+                       int64_t blocks_per_chunk, int64_t skip_count,
+                       uint64_t base, int64_t row_stride_bytes,
+                       int64_t row_bytes, int64_t *out, int64_t n_out);
+
+/* ------------------------------------------------------------------------
+ * kvo_swap_blocks_batch -- batched block copy between a paged device cache
+ * and pinned host blocks.
+ *
+ * vLLM gpu_worker.py, transfer_async -> swap_blocks_batch(src, dst, sizes,
+ * is_src_access_order_any): for every i < n, copy sizes[i] bytes from
+ * address src[i] to address dst[i].  Ranges must not overlap; the order in
+ * which descriptors are executed is unspecified.
+ *
+ * src, dst, sizes: int64[n] descriptor arrays in pinned host memory (the
+ *   page's pooled pinned buffers).  In SM mode the kernel reads them through
+ *   the device mapping while it runs; in copy-engine mode the host reads them
+ *   during this call.
+ * Each src[i] / dst[i] must be device-accessible.  Any alignment and size
+ *   is accepted; descriptors whose two addresses and size are 16-byte
+ *   multiples take the 16-byte vector path, others an 8-, 4- or 1-byte path.
+ * flags: KVO_SWAP_H2D or KVO_SWAP_D2H (direction, used for the mode
+ *   choice); KVO_SWAP_SRC_ORDER_ANY (the source is not written while the copy
+ *   runs: the SM kernel may read it through the read-only path);
+ *   KVO_SWAP_FORCE_SM / KVO_SWAP_FORCE_CE force a mode.  Default: SM mode
+ *   unless the mean descriptor is at least KVO_SWAP_CE_MIN_MEAN_BYTES, a
+ *   crossover measured on GB300 (copy-engine calls cost ~2.7 us each; SM
+ *   copies reach the same link bandwidth as the copy engine).
+ * n == 0 is a no-op.
+ * Errors: KVO_ERR_ARG (n < 0, NULL arrays, both FORCE flags),
+ *   KVO_ERR_NOT_MAPPED (descriptor arrays not device-accessible in SM mode,
+ *   or not host-readable in copy-engine mode), KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+#define KVO_SWAP_H2D 0x1u
+#define KVO_SWAP_D2H 0x2u
+#define KVO_SWAP_SRC_ORDER_ANY 0x4u
+#define KVO_SWAP_FORCE_SM 0x8u
+#define KVO_SWAP_FORCE_CE 0x10u
+#define KVO_SWAP_CE_MIN_MEAN_BYTES (1 << 20)
+
+int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst,
+                          const int64_t *sizes, int64_t n, uint32_t flags,
+                          void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_gather_blocks -- top-k block gather from host-resident K/V planes.
+ *
+ * ExLlamaV3 qsa-kv-offload patch: K/V planes stay in pinned, mapped host
+ * memory and only the selected blocks are read (the staged prefill copies
+ * them into a VRAM arena with index_select of whole pages).  For sequence s,
+ * kv head h and rank r < n_sel, block sel[s][h][r] (block_tokens tokens) is
+ * copied:
+ *     k_out[s][r*block_tokens + t][h][:] = k_plane[s][sel*block_tokens + t][h][:]
+ * for t < block_tokens, and the same for V.
+ *
+ * k_plane, v_plane: [n_seq][seq_stride_tokens][n_kv_heads][head_dim] of
+ *   dtype (pinned mapped host, or device memory).
+ * sel: device-accessible int32 [n_seq][n_kv_heads][n_sel].
+ * k_out, v_out: device [n_seq][n_sel*block_tokens][n_kv_heads][head_dim].
+ * dtype: KVO_F16 or KVO_BF16; head_dim * 2 must be a multiple of 16 and all
+ *   four buffers 16-byte aligned.
+ * A selection outside [0, seq_stride_tokens / block_tokens) is skipped (its
+ *   destination rows are left as they were) and sets bit 0 of
+ *   kvo_device_errors().
+ * Errors: KVO_ERR_ARG, KVO_ERR_ALIGN, KVO_ERR_NOT_MAPPED,
+ *   KVO_ERR_UNSUPPORTED (q8_0), KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
+                      int64_t seq_stride_tokens, int64_t n_kv_heads,
+                      int64_t head_dim, int dtype, int64_t block_tokens,
+                      const int32_t *sel, int64_t n_sel, void *k_out,
+                      void *v_out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_attn_decode_tiered -- GQA decode attention over a tiered cache.
+ *
+ * llama.cpp PR "tiered KV cache (--kv-vram-cells)": cells [0, N) of each
+ * sequence's K/V sit in VRAM and cells [N, L) in pinned host memory, and the
+ * attention arithmetic does not depend on where a cell lives (output is
+ * bit-identical to an all-VRAM cache).  For sequence b and q head h
+ * (kv head g = h / (n_q_heads / n_kv_heads)):
+ *     out[b][h] = sum_j softmax_j(scale * q[b][h] . k[b][j][g]) v[b][j][g]
+ * over cells j < ctx_len[b], computed as split-K flash-decoding: fixed
+ * cell ranges (a function of max_ctx and batch only) give partial
+ * (m, l, acc) in fp32, combined in ascending split order.  An empty context
+ * gives 0.
+ *
+ * Cell row j of sequence b (n_kv_heads * head_dim values, or n_kv_heads *
+ * head_dim/32 q8_0 blocks):
+ *     j <  N: k_vram + (b * vram_seq_stride_rows + j)     * row_bytes
+ *     j >= N: k_host + (b * host_seq_stride_rows + j - N) * row_bytes
+ * (the same for V).  k_vram/v_vram may be NULL when N == 0.
+ * q: device [batch][n_q_heads][head_dim] of q_dtype (F16 or BF16).
+ * kv_dtype: F16, BF16 or Q8_0.  head_dim: 64 or 128.  Group size
+ *   n_q_heads / n_kv_heads: 1..8.  n_kv_heads <= 8.  row_bytes and every
+ *   base pointer 16-byte aligned.
+ * ctx_len: device int32 [batch], each in [0, max_ctx].
+ * staging_k / staging_v: NULL = the kernel reads host cells directly
+ *   (SM loads through the device mapping).  Otherwise VRAM buffers of
+ *   batch * (max_ctx - N) rows each: the host rows [N, max_ctx) are first
+ *   copied there by the copy engine, and the kernel reads that all-VRAM view.
+ * out: device fp32 [batch][n_q_heads][head_dim].
+ * workspace: device, at least kvo_attn_decode_workspace_bytes(...) bytes,
+ *   16-byte aligned (split partials).
+ * Errors: KVO_ERR_ARG, KVO_ERR_ALIGN, KVO_ERR_NOT_MAPPED,
+ *   KVO_ERR_UNSUPPORTED, KVO_ERR_WORKSPACE, KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t kvo_attn_decode_workspace_bytes(int64_t batch, int64_t n_q_heads,
+                                       int64_t head_dim, int64_t max_ctx);
+
+int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch,
+                           int64_t n_q_heads, int64_t n_kv_heads,
+                           int64_t head_dim, const void *k_vram,
+                           const void *v_vram, int64_t vram_seq_stride_rows,
+                           const void *k_host, const void *v_host,
+                           int64_t host_seq_stride_rows, int kv_dtype,
+                           const int32_t *ctx_len, int64_t max_ctx,
+                           int64_t n_vram_cells, float scale, void *staging_k,
+                           void *staging_v, float *out, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_attn_prefill_tiered -- causal chunked-prefill GQA attention over a
+ * tiered cache (one sequence).
+ *
+ * Query row i (0 <= i < rows) sits at position q_pos0 + i and attends the
+ * cells j <= q_pos0 + i, j < ctx_len:
+ *     out[i][h] = sum_j softmax_j(scale * q[i][h] . k[j][g]) v[j][g],
+ *     g = h / (n_q_heads / n_kv_heads).
+ * Cells [0, N) are read from k_vram/v_vram, cells [N, ctx_len) from
+ * k_host/v_host (row j - N), rows of n_kv_heads * head_dim values.
+ *
+ * Staged mode (arena != NULL; ExLlamaV3 qsa-kv-offload patch,
+ * qsa_sparse_attend_rows_staged): the host tail is walked in buckets of
+ * arena_bytes / (2 * row_bytes) cells (the arena holds one bucket of K and
+ * one of V); each bucket is copied host -> arena by the copy engine once,
+ * every query row is scored against it in launches of rows_per_launch rows,
+ * and each launch folds its partial (m, l, acc) into the running softmax
+ *     m' = max(m, m_b), acc = e^(m-m') acc + e^(m_b-m') acc_b,
+ *     l = e^(m-m') l + e^(m_b-m') l_b
+ * (a bucket a row cannot see contributes nothing); the end result is
+ * acc / max(l, 1e-30).  Each host byte crosses the link once per call.
+ * Direct mode (arena == NULL): the kernel reads the tail from host memory
+ * for every query tile.
+ *
+ * q: device [rows][n_q_heads][head_dim], dtype = kv_dtype (F16 or BF16:
+ *   the tensor-core tiles take one operand type).  head_dim: 128.  Group
+ *   size: 1, 2, 4 or 8.  Rows and base pointers 16-byte aligned.
+ * arena: device, >= 2 cell rows of K and of V, 16-byte aligned.
+ * out: device fp32 [rows][n_q_heads][head_dim]; also used as the running
+ *   accumulator between launches.
+ * workspace: device, kvo_attn_prefill_workspace_bytes(rows, n_q_heads)
+ *   bytes (running m and l).
+ * Errors: KVO_ERR_ARG, KVO_ERR_ALIGN, KVO_ERR_NOT_MAPPED,
+ *   KVO_ERR_UNSUPPORTED, KVO_ERR_WORKSPACE, KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t kvo_attn_prefill_workspace_bytes(int64_t rows, int64_t n_q_heads);
+
+int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0,
+                            int64_t n_q_heads, int64_t n_kv_heads,
+                            int64_t head_dim, const void *k_vram,
+                            const void *v_vram, const void *k_host,
+                            const void *v_host, int kv_dtype, int64_t ctx_len,
+                            int64_t n_vram_cells, float scale, void *arena,
+                            size_t arena_bytes, int64_t rows_per_launch,
+                            float *out, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVO_H */

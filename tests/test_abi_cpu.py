@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+include/kvo.h declares, and its pure host function and host-side argument
+checks behave as documented."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from host_ram_tiered_gb300 import kvo, synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvo.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvo_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_entry_points():
+    syms = declared_symbols()
+    for name in ("kvo_swap_blocks_batch", "kvo_sub_block_ptrs", "kvo_gather_blocks",
+                 "kvo_attn_decode_tiered", "kvo_attn_prefill_tiered"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(kvo_lib):
+    for name in declared_symbols():
+        assert hasattr(kvo_lib, name), name
+        assert name in kvo.SIGNATURES, name
+
+
+def test_status_strings(kvo_lib):
+    assert kvo.kvo_status_string(0) == "ok"
+    assert "argument" in kvo.kvo_status_string(-1)
+    assert kvo.kvo_status_string(12345) == "unknown status"
+
+
+def _c_ptrs(ids, bpc, skip, base, stride, row_bytes, n):
+    ids = np.ascontiguousarray(ids, np.int64)
+    out = np.zeros(n, np.int64)
+    kvo.kvo_sub_block_ptrs(ids.ctypes.data, len(ids), bpc, skip, base, stride, row_bytes,
+                           out.ctypes.data, n)
+    return out.view(np.uint64)
+
+
+@pytest.mark.parametrize("page", [32768, 2048])
+def test_sub_block_ptrs_matches_oracle_at_c2_shape(kvo_lib, page):
+    # 2048 GPU blocks per direction, blocks_per_chunk 4, skip 1, host row stride
+    # 1.5 x (4 pages): the host side consumes cdiv(2048 + 1, 4) = 513 chunk ids.
+    g = synth.rng(1235, 7)
+    host_ids = g.permutation(640)[:513]
+    gpu_ids = g.permutation(4096)[:2048]
+    base = 0x7F1234560000
+    row = 4 * page
+    stride = row * 3 // 2
+    got = _c_ptrs(host_ids, 4, 1, base, stride, row, 2048)
+    exp = oracle.sub_block_ptrs(host_ids, 4, 1, base, stride, row, 2048)
+    assert np.array_equal(got, exp)
+    got1 = _c_ptrs(gpu_ids, 1, 0, base, page, page, 2048)
+    exp1 = oracle.sub_block_ptrs(gpu_ids, 1, 0, base, page, page, 2048)
+    assert np.array_equal(got1, exp1)
+
+
+@pytest.mark.parametrize("bpc,skip,n_ids,n", [(3, 2, 5, 13), (4, 0, 1, 4), (2, 1, 7, 1), (5, 4, 3, 11)])
+def test_sub_block_ptrs_ragged_cases(kvo_lib, bpc, skip, n_ids, n):
+    ids = synth.rng(5, bpc).permutation(100)[:n_ids]
+    got = _c_ptrs(ids, bpc, skip, 4096, 999 * bpc, 64 * bpc, n)
+    assert np.array_equal(got, oracle.sub_block_ptrs(ids, bpc, skip, 4096, 999 * bpc, 64 * bpc, n))
+
+
+def test_sub_block_ptrs_rejects_what_the_page_asserts(kvo_lib):
+    ids = np.arange(4, dtype=np.int64)
+    out = np.zeros(16, np.int64)
+    for args in [(4, 4, 1024, 4), (3, 0, 1024, 4), (4, 1, 1024, 16), (0, 0, 1024, 1)]:
+        bpc, skip, row, n = args
+        with pytest.raises(kvo.KvoError) as e:
+            kvo.kvo_sub_block_ptrs(ids.ctypes.data, 4, bpc, skip, 0, row, row, out.ctypes.data, n)
+        assert e.value.status == -1
+    kvo.kvo_sub_block_ptrs(None, 0, 4, 0, 0, 16, 16, None, 0)      # empty is fine
+
+
+def test_swap_host_side_checks_need_no_gpu(kvo_lib):
+    kvo.kvo_swap_blocks_batch(None, None, None, 0, kvo.KVO_SWAP_H2D)  # n == 0: no-op
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_swap_blocks_batch(None, None, None, -1, 0)
+    assert e.value.status == -1
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_swap_blocks_batch(1, 1, 1, 4, kvo.KVO_SWAP_FORCE_CE | kvo.KVO_SWAP_FORCE_SM)
+    assert e.value.status == -1
+
+
+def test_workspace_sizes_are_deterministic(kvo_lib):
+    assert kvo.kvo_attn_prefill_workspace_bytes(2048, 32) == 2048 * 32 * 2 * 4
+    assert kvo.kvo_attn_prefill_workspace_bytes(-1, 32) == 0

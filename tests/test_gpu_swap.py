@@ -1,0 +1,222 @@
+"""GPU parity of kvo_swap_blocks_batch (and the descriptors kvo_sub_block_ptrs
+builds) against the oracle's memcpy swap: bit-exact, plus the D2H-then-H2D
+round trip and untouched canary bytes."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import pinned, torch
+from host_ram_tiered_gb300 import kvo, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _ptrs(ids, bpc, skip, base, stride, row_bytes, n):
+    ids = np.ascontiguousarray(ids, np.int64)
+    out = np.zeros(n, np.int64)
+    kvo.kvo_sub_block_ptrs(ids.ctypes.data, len(ids), bpc, skip, base, stride, row_bytes,
+                           out.ctypes.data, n)
+    exp = oracle.sub_block_ptrs(ids, bpc, skip, base, stride, row_bytes, n)
+    assert np.array_equal(out.view(np.uint64), exp)
+    return out
+
+
+class Pools:
+    """n_tensors paged device tensors [gpu_blocks][page] and host tensors
+    [host_chunks][row_stride] (row = bpc pages), each its own allocation
+    region inside one device / one pinned slab."""
+
+    def __init__(self, n_tensors, gpu_blocks, host_chunks, page, bpc, row_stride, seed):
+        t = torch()
+        self.n_tensors, self.page, self.bpc, self.row_stride = n_tensors, page, bpc, row_stride
+        self.gpu_bytes = gpu_blocks * page
+        self.host_bytes = host_chunks * row_stride
+        self.dev = t.empty(n_tensors * self.gpu_bytes, dtype=t.uint8, device="cuda")
+        self.host = pinned(n_tensors * self.host_bytes)
+        g = synth.rng(seed, 1)
+        init_dev = np.empty(n_tensors * self.gpu_bytes, np.uint8)
+        synth.fill_bytes_large(init_dev, seed, 2)
+        self.dev.copy_(t.from_numpy(init_dev))
+        synth.fill_bytes_large(self.host.numpy(), seed, 3)
+        self.init_dev = init_dev
+
+    def dev_base(self, i):
+        return self.dev.data_ptr() + i * self.gpu_bytes
+
+    def host_base(self, i):
+        return self.host.data_ptr() + i * self.host_bytes
+
+
+def _descs(pools, gpu_ids, host_ids, skip, h2d, n):
+    """Descriptors of one direction for every tensor (transfer_async order)."""
+    src, dst = [], []
+    for i in range(pools.n_tensors):
+        hp = _ptrs(host_ids, pools.bpc, skip, pools.host_base(i), pools.row_stride,
+                   pools.bpc * pools.page, n)
+        gp = _ptrs(gpu_ids, 1, 0, pools.dev_base(i), pools.page, pools.page, n)
+        src.append(hp if h2d else gp)
+        dst.append(gp if h2d else hp)
+    return np.concatenate(src), np.concatenate(dst)
+
+
+def _pinned_i64(a):
+    buf = pinned(a.size * 8)
+    buf.numpy().view(np.int64)[:a.size] = a
+    return buf
+
+
+def _swap(src, dst, page, flags):
+    n = src.size
+    s, d = _pinned_i64(src), _pinned_i64(dst)
+    z = _pinned_i64(np.full(n, page, np.int64))
+    kvo.kvo_swap_blocks_batch(s, d, z, n, flags)
+    torch().cuda.synchronize()
+
+
+def _host_addr_map(pools):
+    """numpy arrays of the host slab and a device mirror for the oracle."""
+    return pools.host.numpy()
+
+
+def _oracle_swap(src, dst, page, base_map):
+    """Run the oracle memcpy swap on host mirrors: addresses are translated
+    from (device | pinned) ranges to numpy mirror ranges."""
+    (dev_base, dev_mirror), (host_base, host_mirror) = base_map
+
+    def tr(a):
+        out = np.empty_like(a, dtype=np.uint64)
+        in_dev = (a >= dev_base) & (a < dev_base + dev_mirror.size)
+        out[in_dev] = (a[in_dev] - dev_base).astype(np.uint64) + np.uint64(dev_mirror.ctypes.data)
+        out[~in_dev] = (a[~in_dev] - host_base).astype(np.uint64) + np.uint64(host_mirror.ctypes.data)
+        return out
+
+    oracle.swap_blocks(tr(src), tr(dst), np.full(src.size, page, np.int64))
+
+
+@pytest.mark.parametrize("mode", [0, kvo.KVO_SWAP_FORCE_SM, kvo.KVO_SWAP_FORCE_CE])
+def test_c1_swap_64_blocks_round_trip(mode):
+    # 2 layers x K,V; 32 KiB pages (16 tokens x 8 heads x 128 x fp16); pools of 128.
+    page, nt = 32768, 4
+    pools = Pools(nt, 128, 128, page, 1, page, seed=1234)
+    g = synth.rng(1234, 10)
+    gpu_ids = g.permutation(128)[:64]
+    host_ids = g.permutation(128)[:64]
+    dev_mirror = pools.init_dev.copy()
+    host_mirror = pools.host.numpy().copy()
+    bm = ((pools.dev.data_ptr(), dev_mirror), (pools.host.data_ptr(), host_mirror))
+    # D2H
+    src, dst = _descs(pools, gpu_ids, host_ids, 0, False, 64)
+    _swap(src, dst, page, kvo.KVO_SWAP_D2H | mode)
+    _oracle_swap(src, dst, page, bm)
+    assert np.array_equal(pools.host.numpy(), host_mirror)
+    # H2D into a cleared device pool: the blocks come back byte-identical
+    pools.dev.zero_()
+    dev_mirror[:] = 0
+    src, dst = _descs(pools, gpu_ids, host_ids, 0, True, 64)
+    _swap(src, dst, page, kvo.KVO_SWAP_H2D | kvo.KVO_SWAP_SRC_ORDER_ANY | mode)
+    _oracle_swap(src, dst, page, bm)
+    got = pools.dev.cpu().numpy()
+    assert np.array_equal(got, dev_mirror)
+    # round trip: the swapped blocks equal the original device blocks
+    for i in range(nt):
+        o = pools.init_dev[i * pools.gpu_bytes:(i + 1) * pools.gpu_bytes].reshape(128, page)
+        r = got[i * pools.gpu_bytes:(i + 1) * pools.gpu_bytes].reshape(128, page)
+        assert np.array_equal(r[gpu_ids], o[gpu_ids])
+        others = np.setdiff1d(np.arange(128), gpu_ids)
+        assert (r[others] == 0).all()
+
+
+@pytest.mark.parametrize("page,n_tensors,n_blocks", [(2048, 8, 301), (32768, 4, 77)])
+def test_c2_shape_swap_bpc4_skip1(page, n_tensors, n_blocks):
+    # blocks_per_chunk 4, skip 1 on the first chunk, host row stride 1.5 x row;
+    # a ragged block count (not a multiple of 4).
+    bpc = 4
+    need = -(-(n_blocks + 1) // bpc)
+    pools = Pools(n_tensors, 512, need + 20, page, bpc, bpc * page * 3 // 2, seed=1235)
+    g = synth.rng(1235, 11)
+    gpu_ids = g.permutation(512)[:n_blocks]
+    host_ids = g.permutation(need + 20)[:need]
+    dev_mirror = pools.init_dev.copy()
+    host_mirror = pools.host.numpy().copy()
+    bm = ((pools.dev.data_ptr(), dev_mirror), (pools.host.data_ptr(), host_mirror))
+    src, dst = _descs(pools, gpu_ids, host_ids, 1, False, n_blocks)
+    _swap(src, dst, page, kvo.KVO_SWAP_D2H)
+    _oracle_swap(src, dst, page, bm)
+    assert np.array_equal(pools.host.numpy(), host_mirror)      # incl. the untouched 1/3 of rows
+    pools.dev.zero_()
+    dev_mirror[:] = 0
+    src, dst = _descs(pools, gpu_ids, host_ids, 1, True, n_blocks)
+    _swap(src, dst, page, kvo.KVO_SWAP_H2D | kvo.KVO_SWAP_SRC_ORDER_ANY)
+    _oracle_swap(src, dst, page, bm)
+    assert np.array_equal(pools.dev.cpu().numpy(), dev_mirror)
+
+
+def test_unaligned_and_odd_sizes_with_canaries():
+    t = torch()
+    g = synth.rng(9)
+    dev = t.zeros(1 << 20, dtype=t.uint8, device="cuda")
+    host = pinned(1 << 20)
+    hn = host.numpy()
+    hn[:] = g.integers(0, 256, size=hn.size, dtype=np.uint8)
+    sizes = np.array([1, 3, 8, 24, 1000, 4096, 4100, 16, 77, 65536], np.int64)
+    soffs = np.array([5, 64, 131, 256, 1001, 8192, 20000, 30001, 40003, 100000], np.int64)
+    doffs = np.array([0, 17, 40, 200, 4000, 12288, 20480, 30000, 40000, 200000], np.int64)
+    src = soffs + host.data_ptr()
+    dst = doffs + dev.data_ptr()
+    s, d, z = _pinned_i64(src), _pinned_i64(dst), _pinned_i64(sizes)
+    kvo.kvo_swap_blocks_batch(s, d, z, sizes.size, kvo.KVO_SWAP_H2D | kvo.KVO_SWAP_FORCE_SM)
+    t.cuda.synchronize()
+    got = dev.cpu().numpy()
+    exp = np.zeros(1 << 20, np.uint8)
+    oracle.swap_blocks(soffs.astype(np.uint64) + np.uint64(hn.ctypes.data),
+                       doffs.astype(np.uint64) + np.uint64(exp.ctypes.data), sizes)
+    assert np.array_equal(got, exp)
+
+
+def test_copy_engine_merges_contiguous_runs():
+    t = torch()
+    dev = t.zeros(1 << 22, dtype=t.uint8, device="cuda")
+    host = pinned(1 << 22)
+    host.numpy()[:] = synth.rng(3).integers(0, 256, size=1 << 22, dtype=np.uint8)
+    n = 64
+    sizes = np.full(n, 1 << 16, np.int64)
+    src = host.data_ptr() + np.arange(n, dtype=np.int64) * (1 << 16)
+    dst = dev.data_ptr() + np.arange(n, dtype=np.int64) * (1 << 16)
+    kvo.kvo_swap_blocks_batch(_pinned_i64(src), _pinned_i64(dst), _pinned_i64(sizes), n,
+                              kvo.KVO_SWAP_H2D | kvo.KVO_SWAP_FORCE_CE)
+    t.cuda.synchronize()
+    assert np.array_equal(dev.cpu().numpy(), host.numpy())
+
+
+def test_descriptor_arrays_must_be_mapped():
+    t = torch()
+    dev = t.zeros(4096, dtype=t.uint8, device="cuda")
+    pageable = np.array([dev.data_ptr()], np.int64)
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_swap_blocks_batch(pageable.ctypes.data, pageable.ctypes.data, pageable.ctypes.data,
+                                  1, kvo.KVO_SWAP_FORCE_SM)
+    assert e.value.status == -3
+
+
+@pytest.mark.parametrize("page", [32768, 2048])
+def test_c2_full_size_swap_sampled(page):
+    # Full C2: 64 tensors (32 layers x K,V), 2048 blocks per direction, bpc 4,
+    # skip 1, host stride 1.5 x row: the launch configuration the benchmark times.
+    from bench import c2_setup, c2_run
+    st = c2_setup(page, seed=1235)
+    c2_run(st, h2d=False)
+    c2_run(st, h2d=True)
+    torch().cuda.synchronize()
+    g = synth.rng(99, page)
+    host = st["host"].numpy()
+    dev = st["dev"]
+    checks = g.choice(st["n_desc"], size=512, replace=False)
+    for i in checks:
+        # D2H: host sub-block i now holds the device block's original bytes;
+        # H2D wrote it back unchanged.
+        hs = int(st["d2h_dst_np"][i]) - st["host"].data_ptr()
+        ds = int(st["d2h_src_np"][i]) - dev.data_ptr()
+        exp = st["init_dev_sample"](ds, page)
+        assert np.array_equal(host[hs:hs + page], exp)
+        got = dev[ds:ds + page].cpu().numpy()
+        assert np.array_equal(got, exp)
