@@ -193,24 +193,59 @@ decode_split_kernel(const DecodeArgs a) {
   }
 }
 
-// Fold the splits of one (sequence, q head) in ascending split order:
-// weights 2^(m_s - M) with M the maximum, out = acc / max(l, 1e-30).
-static __global__ void decode_combine_kernel(const DecodeArgs a) {
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int D = a.head_dim;
+// Fold the splits of one (sequence, q head): weights 2^(m_s - M) with M the
+// maximum over splits, out = acc / max(l, 1e-30).  Warp w sums the splits
+// s = w, w + 8, w + 16, ... in ascending order and the 8 warp sums are added
+// in warp order: a fixed reduction tree, so the result depends on the
+// partials only (never on timing, the tier split or staging).
+constexpr int kCombineWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+decode_combine_kernel(const DecodeArgs a) {
+  constexpr int DPL = D / 32;
+  __shared__ float red[kCombineWarps][D];
+  __shared__ float red_l[kCombineWarps];
+  __shared__ float red_m[kCombineWarps];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
   const int ns = ctx > 0 ? (int)((ctx + a.split_cells - 1) / a.split_cells) : 0;
   const size_t base = (size_t)b * a.n_splits * a.n_q_heads + h;
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[(base + (size_t)s * a.n_q_heads) * 2]);
-  float l = 0.f, acc = 0.f;
-  for (int s = 0; s < ns; ++s) {
+  for (int s = threadIdx.x; s < ns; s += kCombineWarps * 32)
+    M = fmaxf(M, a.part_ml[(base + (size_t)s * a.n_q_heads) * 2]);
+  M = warp_max(M);
+  if (lane == 0) red_m[warp] = M;
+  __syncthreads();
+  M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
+  float l = 0.f, acc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int s = warp; s < ns; s += kCombineWarps) {
     const size_t pi = base + (size_t)s * a.n_q_heads;
     const float w = exp2f(a.part_ml[pi * 2] - M);
     l = fmaf(w, a.part_ml[pi * 2 + 1], l);
-    acc = fmaf(w, a.part_acc[pi * D + d], acc);
+    const float *pa = a.part_acc + pi * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = fmaf(w, pa[i], acc[i]);
   }
-  a.out[((size_t)b * a.n_q_heads + h) * D + d] = acc / fmaxf(l, 1e-30f);
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) red[warp][lane * DPL + i] = acc[i];
+  if (lane == 0) red_l[warp] = l;
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += kCombineWarps * 32) {
+    float sl = 0.f, sa = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+      sl += red_l[w];
+      sa += red[w][d];
+    }
+    a.out[((size_t)b * a.n_q_heads + h) * D + d] = sa / fmaxf(sl, 1e-30f);
+  }
 }
 
 template <int KVT, int QT, int G, int D, int T>
@@ -223,7 +258,7 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
   k<<<grid, 32 * a.n_kv_heads, smem, st>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<dim3(a.n_q_heads, a.batch), a.head_dim, 0, st>>>(a);
+  decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
 }
 

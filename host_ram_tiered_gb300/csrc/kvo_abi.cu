@@ -427,7 +427,18 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       a.ml = ml + (size_t)r0 * n_q_heads * 2;
       a.init = (si == 0);
       a.finalize = last;
-      int e = launch_prefill(a, st);
+      int e;
+      if (!tail) {
+        // VRAM head: tensor cores fed by TMA
+        a.hi_origin = 0;
+        e = launch_prefill_tc(a, k_vram, v_vram, n_lo, st);
+      } else if (arena) {
+        // arena bucket: tensor cores fed by TMA
+        e = launch_prefill_tc(a, k_arena, v_arena, s.c1 - s.c0, st);
+      } else {
+        // direct: host tail read through the mapping by the mma.sync kernel
+        e = launch_prefill(a, st);
+      }
       if (e) return e;
     }
   }

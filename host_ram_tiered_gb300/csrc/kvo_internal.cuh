@@ -74,6 +74,10 @@ struct PrefillArgs {
   float *ml;                   // [rows][Hq][2] running (m, l) in log2 units
   int init, finalize;
 };
-int launch_prefill(const PrefillArgs &a, cudaStream_t st);  // kvo_status
+int launch_prefill(const PrefillArgs &a, cudaStream_t st);  // kvo_status (mma.sync, any memory)
+// tcgen05 + TMA path for a device-resident segment: cells [a.c0, a.c1) are
+// rows (c - a.hi_origin) of k_seg / v_seg (seg_rows rows).
+int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg, int64_t seg_rows,
+                      cudaStream_t st);
 
 }  // namespace kvo

@@ -10,6 +10,7 @@
 // Cells j < n_vram come from k_lo/v_lo, cells j >= n_vram from
 // k_hi/v_hi (row j - hi_origin): the VRAM head, the host tail (direct) or an
 // arena bucket (staged).
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "kvo_internal.cuh"
@@ -62,6 +63,16 @@ __device__ __forceinline__ void mma16816(float *d, const uint32_t *a, uint32_t b
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (DT == KVO_BF16) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
   }
 }
 
@@ -240,14 +251,23 @@ prefill_mma_kernel(const PrefillArgs a) {
       o[n][2] *= al_hi; o[n][3] *= al_hi;
     }
 
-    // ---- O += P V  (P as A fragments straight from the S accumulators)
+    // ---- O += P V  (P as A fragments straight from the S accumulators).
+    // P is carried as a pair hi + lo of the input type (lo = the rounding
+    // residual of hi), so the product keeps ~16 bits of P instead of 8.
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {                  // 16 cells per k-step
-      uint32_t pa[4];
+      uint32_t pa[4], pl[4];
       pa[0] = pack2<DT>(s[2 * kk][0], s[2 * kk][1]);
       pa[1] = pack2<DT>(s[2 * kk][2], s[2 * kk][3]);
       pa[2] = pack2<DT>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
       pa[3] = pack2<DT>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      {
+        float2 h;
+        h = unpack2<DT>(pa[0]); pl[0] = pack2<DT>(s[2 * kk][0] - h.x, s[2 * kk][1] - h.y);
+        h = unpack2<DT>(pa[1]); pl[1] = pack2<DT>(s[2 * kk][2] - h.x, s[2 * kk][3] - h.y);
+        h = unpack2<DT>(pa[2]); pl[2] = pack2<DT>(s[2 * kk + 1][0] - h.x, s[2 * kk + 1][1] - h.y);
+        h = unpack2<DT>(pa[3]); pl[3] = pack2<DT>(s[2 * kk + 1][2] - h.x, s[2 * kk + 1][3] - h.y);
+      }
 #pragma unroll
       for (int np = 0; np < 8; ++np) {               // pairs of 8-dim n-tiles
         uint32_t b0, b1, b2, b3;
@@ -256,6 +276,8 @@ prefill_mma_kernel(const PrefillArgs a) {
         ldsm_x4_t(smem_u32(sv + swz(r, ch)), b0, b1, b2, b3);
         mma16816<DT>(o[np * 2], pa, b0, b1);
         mma16816<DT>(o[np * 2 + 1], pa, b2, b3);
+        mma16816<DT>(o[np * 2], pl, b0, b1);
+        mma16816<DT>(o[np * 2 + 1], pl, b2, b3);
       }
     }
   }

@@ -1,0 +1,579 @@
+// Tiered causal chunked-prefill attention on the 5th-generation tensor
+// cores (tcgen05): one launch = (row block) x (device-resident cell range:
+// the VRAM head or one arena bucket of the host tail).
+//
+// Per CTA: 128 MMA rows (128/G query positions x the G query heads of one kv
+// head) against the whole cell range in tiles of 128 cells.
+//   warp 0  (one lane): TMA producer, K/V tiles (two 64-dim SW128 boxes each)
+//                       into a 2-stage ring;
+//   warp 1  (one lane): MMA issuer; the warp owns the TMEM allocation;
+//   warps 4-7         : softmax (thread = row = TMEM lane) and epilogue.
+// S = Q K^T goes to one of two TMEM buffers (fp32, 128 columns each) while
+// the softmax reads the other; O = P V accumulates in a third TMEM region.
+// P is written to shared memory (SW128 K-major) as a pair hi + lo of the
+// input type, so the product keeps ~16 bits of P.  The running max is
+// rescaled lazily (only when the tile max exceeds the reference by more
+// than 2^8), which keeps O exact in fp32 and makes rescales rare.
+// The running (m, l, acc) of earlier launches is folded in at the start and
+// written back at the end (ExLlamaV3 qsa-kv-offload patch, the fold of a
+// bucket's partial into the running softmax), or the output normalised by
+// max(l, 1e-30) on the last launch of a row block.
+//
+// Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
+// waiter sets kErrTimeout in the device error word and the CTA winds down.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "kvo_internal.cuh"
+
+namespace kvo {
+
+namespace {
+
+constexpr int BM = 128;                  // MMA rows per CTA
+constexpr int BN = 128;                  // cells per tile
+constexpr int HD = 128;                  // head dim
+constexpr int kThreads = 256;
+constexpr int kHalf = BM * 128;          // one SW128 half tile: 128 rows x 128 B = 16 KiB
+constexpr int kTile = 2 * kHalf;         // 128 rows x 256 B
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr float kLazy = 8.0f;            // rescale when the max grows by > 2^8
+constexpr uint32_t kErrTimeout = 2u;
+
+// shared memory plan (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;                     // kStages K tiles
+constexpr int kOffV = kOffK + kStages * kTile;           // kStages V tiles
+constexpr int kOffPh = kOffV + kStages * kTile;          // P hi
+constexpr int kOffPl = kOffPh + kTile;                   // P lo
+constexpr int kOffBar = kOffPl + kTile;                  // mbarriers
+constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + alignment slack
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false (and the error bit set) after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 255) == 0 && globaltimer() - t0 > 2000000000ull) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// UMMA shared-memory descriptor, SW128 (layout type 2), version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16, fp32 accumulate, M = 128, N = 128.
+template <int DT>
+__host__ __device__ constexpr uint32_t idesc(bool b_mn_major) {
+  return (1u << 4)                                   // D = f32
+         | ((DT == KVO_BF16 ? 1u : 0u) << 7)         // A type
+         | ((DT == KVO_BF16 ? 1u : 0u) << 10)        // B type
+         | ((b_mn_major ? 1u : 0u) << 16)            // B major
+         | ((uint32_t)(BN >> 3) << 17)               // N
+         | ((uint32_t)(BM >> 4) << 24);              // M
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t id,
+                                     uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(id), "r"(accum));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.  The load and its
+// wait are one asm statement, so no use of the registers can be scheduled
+// before the data has arrived.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  if constexpr (DT == KVO_BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int DT>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+  if constexpr (DT == KVO_BF16) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+  }
+}
+
+// Byte offset of 16-byte chunk c (0..15 across the 256-byte row) of row r in
+// a tile made of two SW128 halves of [128 rows][128 B].
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)((c >> 3) * kHalf + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+struct TcParams {
+  PrefillArgs a;
+  uint32_t *err;
+};
+
+template <int DT, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const TcParams P) {
+  constexpr int PB = BM / G;                         // query positions per CTA
+  const PrefillArgs &a = P.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *bar = (uint64_t *)(smem + kOffBar);
+  uint64_t *full = bar;                    // [kStages] TMA -> MMA
+  uint64_t *empty = bar + kStages;         // [kStages] MMA -> TMA
+  uint64_t *s_full = bar + 2 * kStages;    // [2]       MMA -> softmax
+  uint64_t *p_full = bar + 2 * kStages + 2;    // softmax -> MMA (128 arrivals)
+  uint64_t *o_done = bar + 2 * kStages + 3;    // MMA -> softmax (PV finished)
+  uint64_t *fin = bar + 2 * kStages + 4;       // MMA teardown
+  uint32_t *tmem_slot = (uint32_t *)(bar + 2 * kStages + 5);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = blockIdx.y;
+  const int i0 = blockIdx.x * PB;
+  const int n_pos = a.rows - i0 < PB ? a.rows - i0 : PB;
+  const int64_t cta_last = a.pos0 + i0 + n_pos - 1;
+  const int64_t c_end = a.c1 < cta_last + 1 ? a.c1 : cta_last + 1;
+  const int n_tiles = c_end > a.c0 ? (int)((c_end - a.c0 + BN - 1) / BN) : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
+    mbar_init(p_full, 128);
+    mbar_init(o_done, 1);
+    mbar_init(fin, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // Q tile (all threads): MMA row r = position r / G, head g*G + r % G.
+  for (int i = tid; i < BM * 16; i += kThreads) {
+    const int r = i >> 4, c = i & 15;
+    const int pi = r / G, hh = r % G;
+    int4 v = make_int4(0, 0, 0, 0);
+    if (pi < n_pos)
+      v = *((const int4 *)(a.q + ((size_t)(i0 + pi) * a.n_q_heads + g * G + hh) * HD) + c);
+    *(int4 *)(smem + kOffQ + sw128(r, c)) = v;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // Q visible to the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      int issued = 0;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages) ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, P.err);
+        if (!ok) break;
+        const int y = (int)(a.c0 + (int64_t)j * BN - a.hi_origin);   // row in the segment map
+        mbar_expect_tx(&full[s], 2 * kTile);
+        uint8_t *kd = smem + kOffK + s * kTile;
+        uint8_t *vd = smem + kOffV + s * kTile;
+        tma_load_2d(kd, &tmap_k, g * HD, y, &full[s]);
+        tma_load_2d(kd + kHalf, &tmap_k, g * HD + 64, y, &full[s]);
+        tma_load_2d(vd, &tmap_v, g * HD, y, &full[s]);
+        tma_load_2d(vd + kHalf, &tmap_v, g * HD + 64, y, &full[s]);
+        issued = j + 1;
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
+          mbar_wait(&full[j % kStages], (j / kStages) & 1, P.err);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      constexpr uint32_t id_s = idesc<DT>(false);
+      constexpr uint32_t id_o = idesc<DT>(true);
+      const uint32_t q_base = smem_u32(smem + kOffQ);
+      const uint32_t ph_base = smem_u32(smem + kOffPh);
+      const uint32_t pl_base = smem_u32(smem + kOffPl);
+      uint32_t o_acc = a.init ? 0u : 1u;
+      for (int j = 0; j <= n_tiles && ok; ++j) {
+        if (j < n_tiles) {
+          const int s = j % kStages;
+          ok = mbar_wait(&full[s], (j / kStages) & 1, P.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(smem + kOffK + s * kTile);
+          const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+#pragma unroll
+          for (int ks = 0; ks < HD / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+            umma(d_s, sdesc(q_base + off, 16, 1024), sdesc(k_base + off, 16, 1024), id_s, ks > 0);
+          }
+          umma_commit(&s_full[j & 1]);
+        }
+        if (j >= 1) {
+          const int jp = j - 1, s = jp % kStages;
+          ok = mbar_wait(p_full, jp & 1, P.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(smem + kOffV + s * kTile);
+          const uint32_t d_o = tmem + kColO;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+            const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
+            umma(d_o, sdesc(ph_base + aoff, 16, 1024), bd, id_o, (kk > 0) || o_acc);
+          }
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+            const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
+            umma(d_o, sdesc(pl_base + aoff, 16, 1024), bd, id_o, 1u);
+          }
+          o_acc = 1u;
+          umma_commit(o_done);
+          umma_commit(&empty[s]);
+        }
+      }
+      // all issued tensor-core work has finished once this arrives
+      umma_commit(fin);
+      mbar_wait(fin, 0, P.err);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- softmax + epilogue
+    const int r = tid - 128;                                  // row = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int pi = r / G;
+    const bool row_ok = pi < n_pos;
+    const int64_t pos = a.pos0 + i0 + pi;
+    const size_t row_idx = (size_t)(i0 + pi) * a.n_q_heads + g * G + (r % G);
+    float m_used = -INFINITY, l = 0.f;
+    bool o_valid = !a.init;                                   // O holds data (from the state)
+    if (!a.init && row_ok) {
+      m_used = a.ml[row_idx * 2];
+      l = a.ml[row_idx * 2 + 1];
+    }
+    if (!a.init) {
+      // load the running accumulator into TMEM (rows past the launch get zeros)
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + q * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+        tmem_st32(lane_addr + kColO + q * 32, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    const int64_t first_pos = a.pos0 + i0;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, P.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_addr = lane_addr + ((j & 1) ? kColS1 : kColS0);
+      float x[BN];
+#pragma unroll
+      for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+      tmem_wait_ld();
+      const int64_t t0 = a.c0 + (int64_t)j * BN;
+      const bool need_mask = (t0 + BN > c_end) || (t0 + BN - 1 > first_pos) || !row_ok;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        float s = x[i] * a.scale_log2;
+        if (need_mask) {
+          const int64_t cj = t0 + i;
+          if (!row_ok || cj >= c_end || cj > pos) s = -INFINITY;
+        }
+        x[i] = s;
+        mt = fmaxf(mt, s);
+      }
+      // Lazy rescale (warp-uniform: tcgen05.ld/st are warp-collective): a row
+      // whose tile max exceeds its reference by more than 2^8 moves its
+      // reference to the tile max and rescales l and O by 2^(old - new).
+      const bool mine = mt > m_used + kLazy;
+      float alpha = 1.f;
+      if (mine) alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - mt);
+      if (__any_sync(0xffffffffu, mine)) {
+        l *= alpha;
+        if (o_valid) {
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          float v[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            tmem_ld32(lane_addr + kColO + q * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(lane_addr + kColO + q * 32, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      if (mine) m_used = mt;
+      const float ref = m_used == -INFINITY ? 0.f : m_used;
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        x[i] = exp2f(x[i] - ref);
+        sum += x[i];
+      }
+      l += sum;
+      // the P buffer is free once the previous tile's PV has finished
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int c = 0; c < BN / 8; ++c) {
+        uint4 hi, lo;
+        uint32_t *h = &hi.x, *lw = &lo.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = x[c * 8 + 2 * e], p1 = x[c * 8 + 2 * e + 1];
+          h[e] = pack2<DT>(p0, p1);
+          const float2 hf = unpack2<DT>(h[e]);
+          lw[e] = pack2<DT>(p0 - hf.x, p1 - hf.y);
+        }
+        *(uint4 *)(smem + kOffPh + sw128(r, c)) = hi;
+        *(uint4 *)(smem + kOffPl + sw128(r, c)) = lo;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(p_full);
+      o_valid = true;
+    }
+    // ---- epilogue: wait for the last PV, then write state or output
+    if (ok && n_tiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, P.err));
+    tc_fence_after();
+    if (ok) {
+      const float inv = a.finalize ? 1.f / fmaxf(l, 1e-30f) : 1.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float v[32];
+        if (o_valid) {                                       // warp-uniform
+          tmem_ld32(lane_addr + kColO + q * 32, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *(float4 *)(a.acc + row_idx * HD + q * 32 + i) =
+                make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+        }
+      }
+      if (!a.finalize && row_ok) {
+        a.ml[row_idx * 2] = m_used;
+        a.ml[row_idx * 2 + 1] = l;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2D map over [rows][n_kv_heads * 128] elements, boxes of [128 rows][64 elems], SW128.
+int make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64_t row_bytes, int dt) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(KVO_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {64, (cuuint32_t)BN};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dt == KVO_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KVO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return KVO_OK;
+}
+
+template <int DT, int G>
+cudaError_t launch_g(const CUtensorMap &mk, const CUtensorMap &mv, const TcParams &p, cudaStream_t st) {
+  constexpr int PB = BM / G;
+  auto k = prefill_tc_kernel<DT, G>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.a.rows + PB - 1) / PB, p.a.n_kv_heads);
+  k<<<grid, kThreads, kSmemBytes, st>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(const CUtensorMap &mk, const CUtensorMap &mv, const TcParams &p, cudaStream_t st) {
+  switch (p.a.group) {
+    case 1: return launch_g<DT, 1>(mk, mv, p, st);
+    case 2: return launch_g<DT, 2>(mk, mv, p, st);
+    case 4: return launch_g<DT, 4>(mk, mv, p, st);
+    default: return launch_g<DT, 8>(mk, mv, p, st);
+  }
+}
+
+}  // namespace
+
+// Launch over a device-resident segment: cells [a.c0, a.c1) are rows
+// (c - a.hi_origin) of the buffers k_seg / v_seg, which hold seg_rows rows.
+int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg, int64_t seg_rows,
+                      cudaStream_t st) {
+  CUtensorMap mk, mv;
+  const int64_t cols = (int64_t)a.n_kv_heads * HD;
+  int r = make_map(&mk, k_seg, seg_rows, cols, a.row_bytes, a.dtype);
+  if (r) return r;
+  r = make_map(&mv, v_seg, seg_rows, cols, a.row_bytes, a.dtype);
+  if (r) return r;
+  TcParams p;
+  p.a = a;
+  p.err = device_error_word();
+  if (!p.err) return fail(KVO_ERR_CUDA, "device error word unavailable");
+  cudaError_t e = a.dtype == KVO_BF16 ? launch_dt<KVO_BF16>(mk, mv, p, st) : launch_dt<KVO_F16>(mk, mv, p, st);
+  return cuda_status(e, "tcgen05 prefill launch");
+}
+
+}  // namespace kvo

@@ -43,17 +43,30 @@ __device__ __forceinline__ void warp_copy(const char *s, char *d, int64_t bytes,
   }
 }
 
-// One warp per descriptor, grid-stride over descriptors.
+// A warp takes 32 consecutive descriptors: lane i loads descriptor i (three
+// coalesced reads through the mapping instead of 32 dependent ones), then
+// the warp copies them one after another, broadcasting each by shuffle.
 __global__ void __launch_bounds__(kSwapThreads)
 swap_kernel(const int64_t *__restrict__ src, const int64_t *__restrict__ dst,
             const int64_t *__restrict__ sizes, int64_t n) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kSwapThreads + threadIdx.x) >> 5;
   const int64_t n_warps = ((int64_t)gridDim.x * kSwapThreads) >> 5;
-  for (int64_t i = warp; i < n; i += n_warps) {
-    const int64_t bytes = sizes[i];
-    if (bytes <= 0) continue;
-    warp_copy((const char *)(uintptr_t)src[i], (char *)(uintptr_t)dst[i], bytes, lane);
+  for (int64_t base = warp * 32; base < n; base += n_warps * 32) {
+    const int64_t i = base + lane;
+    int64_t s = 0, d = 0, z = 0;
+    if (i < n) {
+      s = src[i];
+      d = dst[i];
+      z = sizes[i];
+    }
+    const int cnt = n - base < 32 ? (int)(n - base) : 32;
+    for (int k = 0; k < cnt; ++k) {
+      const int64_t zk = __shfl_sync(0xffffffffu, z, k);
+      const int64_t sk = __shfl_sync(0xffffffffu, s, k);
+      const int64_t dk = __shfl_sync(0xffffffffu, d, k);
+      if (zk > 0) warp_copy((const char *)(uintptr_t)sk, (char *)(uintptr_t)dk, zk, lane);
+    }
   }
 }
 
@@ -132,8 +145,8 @@ uint32_t *device_error_word() {
 
 cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes, int64_t n,
                            bool src_readonly, cudaStream_t st) {
-  const int64_t warps_per_cta = kSwapThreads / 32;
-  int64_t grid = (n + warps_per_cta - 1) / warps_per_cta;
+  const int64_t desc_per_cta = kSwapThreads;      // 8 warps x 32 descriptors
+  int64_t grid = (n + desc_per_cta - 1) / desc_per_cta;
   const int64_t cap = (int64_t)num_sms() * 8;      // 8 CTAs of 8 warps per SM in flight
   if (grid > cap) grid = cap;
   // Every copy here is stream-ordered, which already satisfies both source
