@@ -447,7 +447,7 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     t = torch()
     import torch.distributed as dist
-    v = t.tensor([x], dtype=t.float64, device="cuda" if t.cuda.is_available() else "cpu")
+    v = t.tensor([x], dtype=t.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
     dist.all_reduce(v, op=dist.ReduceOp.MAX)
     return float(v.item())
 
