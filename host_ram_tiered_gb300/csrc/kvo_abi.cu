@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "kvo_internal.cuh"
@@ -44,6 +45,29 @@ int classify(const void *p, size_t bytes) {
   const char *last = (const char *)p + (bytes - 1);
   int k2 = classify_one(last, &b);
   return k2 == k ? k : 0;
+}
+
+// Copy ring of the staged prefill: a side stream that fills one arena slot
+// while the launch stream scores the other (created once per device).
+struct Ring {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+};
+
+Ring *ring() {
+  static Ring rings[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  Ring &r = rings[dev];
+  if (!r.side) {
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    cudaEvent_t *ev[6] = {&r.fork, &r.join, &r.ready[0], &r.ready[1], &r.freed[0], &r.freed[1]};
+    for (cudaEvent_t *e : ev)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    r.side = s;
+  }
+  return &r;
 }
 
 int num_sms() {
@@ -344,6 +368,8 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
     return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_prefill_tiered: head_dim %lld group %lld",
                 (long long)head_dim, (long long)group);
   if (rows_per_launch <= 0) rows_per_launch = rows;
+  if (!(scale > 0.f) || !(scale < 3.0e38f))
+    return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: scale must be positive and finite");
   if (!q || !out) return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: NULL q/out");
   if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: q/out alignment");
   const int64_t rb = n_kv_heads * head_dim * 2;
@@ -357,15 +383,23 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: k_vram/v_vram must be device memory");
   }
   int64_t bucket = 0;
+  int n_slots = 0;
   if (n_hi > 0) {
     if (!aligned16(k_host) || !aligned16(v_host)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: host alignment");
     if (!classify(k_host, (size_t)n_hi * rb) || !classify(v_host, (size_t)n_hi * rb))
       return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: k_host/v_host not device-accessible");
     if (arena) {
-      bucket = (int64_t)(arena_bytes / (2 * (size_t)rb));
+      // Two slots (copy one bucket while scoring the other) when the arena
+      // holds at least two cell rows of K and V per slot, else one.
+      bucket = (int64_t)(arena_bytes / (4 * (size_t)rb));
+      n_slots = 2;
+      if (bucket < 1) {
+        bucket = (int64_t)(arena_bytes / (2 * (size_t)rb));
+        n_slots = 1;
+      }
       if (bucket < 1) return fail(KVO_ERR_ARG, "kvo_attn_prefill_tiered: arena holds no cell row");
       if (!aligned16(arena)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: arena alignment");
-      if (classify(arena, (size_t)2 * bucket * rb) != kDeviceMem)
+      if (classify(arena, (size_t)2 * n_slots * bucket * rb) != kDeviceMem)
         return fail(KVO_ERR_NOT_MAPPED, "kvo_attn_prefill_tiered: arena must be device memory");
     }
   }
@@ -391,21 +425,40 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
     else for (int64_t c = n_lo; c < c_end; c += bucket) segs.push_back({c, c + bucket < c_end ? c + bucket : c_end});
   }
   float *ml = (float *)workspace;
-  const uint8_t *k_arena = (const uint8_t *)arena;
-  const uint8_t *v_arena = arena ? (const uint8_t *)arena + (size_t)bucket * rb : nullptr;
-
+  // Staged mode: buckets go through the arena slots on a side stream; the
+  // launch stream waits for a slot's copy and releases it after its launches.
+  Ring *rg = nullptr;
+  static std::mutex ring_mu;
+  std::unique_lock<std::mutex> lock(ring_mu, std::defer_lock);
+  if (arena && n_hi > 0) {
+    lock.lock();
+    rg = ring();
+    if (!rg) return fail(KVO_ERR_CUDA, "kvo_attn_prefill_tiered: copy stream unavailable");
+    int e = cuda_status(cudaEventRecord(rg->fork, st), "cudaEventRecord");
+    if (!e) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");
+    if (e) return e;
+  }
+  int64_t bi = 0;                                       // bucket index
   for (size_t si = 0; si < segs.size(); ++si) {
     const Seg s = segs[si];
     const bool tail = s.c0 >= n_lo && n_hi > 0;
+    const uint8_t *k_slot = nullptr, *v_slot = nullptr;
+    int slot = 0;
     if (tail && arena) {
+      slot = (int)(bi % n_slots);
+      k_slot = (const uint8_t *)arena + (size_t)slot * 2 * bucket * rb;
+      v_slot = k_slot + (size_t)bucket * rb;
       const size_t bytes = (size_t)(s.c1 - s.c0) * rb;
       const uint8_t *ks = (const uint8_t *)k_host + (size_t)(s.c0 - n_lo) * rb;
       const uint8_t *vs = (const uint8_t *)v_host + (size_t)(s.c0 - n_lo) * rb;
-      int e = cuda_status(cudaMemcpyAsync((void *)k_arena, ks, bytes, cudaMemcpyDefault, st), "arena copy K");
+      int e = KVO_OK;
+      if (bi >= n_slots) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->freed[slot], 0), "cudaStreamWaitEvent");
+      if (!e) e = cuda_status(cudaMemcpyAsync((void *)k_slot, ks, bytes, cudaMemcpyDefault, rg->side), "arena copy K");
+      if (!e) e = cuda_status(cudaMemcpyAsync((void *)v_slot, vs, bytes, cudaMemcpyDefault, rg->side), "arena copy V");
+      if (!e) e = cuda_status(cudaEventRecord(rg->ready[slot], rg->side), "cudaEventRecord");
+      if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->ready[slot], 0), "cudaStreamWaitEvent");
       if (e) return e;
-      e = cuda_status(cudaMemcpyAsync((void *)v_arena, vs, bytes, cudaMemcpyDefault, st), "arena copy V");
-      if (e) return e;
-      a.k_hi = k_arena; a.v_hi = v_arena; a.hi_origin = s.c0;
+      a.k_hi = k_slot; a.v_hi = v_slot; a.hi_origin = s.c0;
     } else if (tail) {
       a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host; a.hi_origin = n_lo;
     }
@@ -434,13 +487,23 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
         e = launch_prefill_tc(a, k_vram, v_vram, n_lo, st);
       } else if (arena) {
         // arena bucket: tensor cores fed by TMA
-        e = launch_prefill_tc(a, k_arena, v_arena, s.c1 - s.c0, st);
+        e = launch_prefill_tc(a, k_slot, v_slot, s.c1 - s.c0, st);
       } else {
         // direct: host tail read through the mapping by the mma.sync kernel
         e = launch_prefill(a, st);
       }
       if (e) return e;
     }
+    if (tail && arena) {
+      int e = cuda_status(cudaEventRecord(rg->freed[slot], st), "cudaEventRecord");
+      if (e) return e;
+      ++bi;
+    }
+  }
+  if (rg) {
+    int e = cuda_status(cudaEventRecord(rg->join, rg->side), "cudaEventRecord");
+    if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->join, 0), "cudaStreamWaitEvent");
+    if (e) return e;
   }
   if (segs.empty()) {
     // Nothing visible (ctx_len == 0): the result is 0 by the 1e-30 clamp.

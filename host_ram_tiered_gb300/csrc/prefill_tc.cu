@@ -204,6 +204,30 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
   }
 }
 
+// 2^x on the SFU (PTX ex2.approx.ftz.f32; 2^-inf = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Split p0, p1 into a hi pair and a lo pair of the 16-bit input type with
+// p ~= hi + lo to ~2^-16 relative.  bf16: hi is p truncated to its upper 16
+// bits (exact in fp32), lo the rounded residual.  f16: hi rounded, lo the
+// rounded residual.
+template <int DT>
+__device__ __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
+  if constexpr (DT == KVO_BF16) {
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(b0), "r"(b1));
+    lo = pack2<DT>(p0 - __uint_as_float(b0 & 0xffff0000u), p1 - __uint_as_float(b1 & 0xffff0000u));
+  } else {
+    hi = pack2<DT>(p0, p1);
+    const float2 hf = unpack2<DT>(hi);
+    lo = pack2<DT>(p0 - hf.x, p1 - hf.y);
+  }
+}
+
 // Byte offset of 16-byte chunk c (0..15 across the 256-byte row) of row r in
 // a tile made of two SW128 halves of [128 rows][128 B].
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
@@ -392,17 +416,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       tmem_wait_ld();
       const int64_t t0 = a.c0 + (int64_t)j * BN;
       const bool need_mask = (t0 + BN > c_end) || (t0 + BN - 1 > first_pos) || !row_ok;
-      float mt = -INFINITY;
+      if (need_mask) {
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        float s = x[i] * a.scale_log2;
-        if (need_mask) {
+        for (int i = 0; i < BN; ++i) {
           const int64_t cj = t0 + i;
-          if (!row_ok || cj >= c_end || cj > pos) s = -INFINITY;
+          if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
         }
-        x[i] = s;
-        mt = fmaxf(mt, s);
       }
+      // row max of the raw scores (scale > 0), 8 independent chains
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float mt = mraw * a.scale_log2;
       // Lazy rescale (warp-uniform: tcgen05.ld/st are warp-collective): a row
       // whose tile max exceeds its reference by more than 2^8 moves its
       // reference to the tile max and rescales l and O by 2^(old - new).
@@ -430,14 +459,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         }
       }
       if (mine) m_used = mt;
-      const float ref = m_used == -INFINITY ? 0.f : m_used;
-      float sum = 0.f;
+      const float nref = m_used == -INFINITY ? 0.f : -m_used;
+      float sm[8];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        x[i] = exp2f(x[i] - ref);
-        sum += x[i];
+      for (int k = 0; k < 8; ++k) sm[k] = 0.f;
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const float p = x[i] == -INFINITY ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
+          sm[i & 7] += p;
+          x[i] = p;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const float p = ex2(fmaf(x[i], a.scale_log2, nref));
+          sm[i & 7] += p;
+          x[i] = p;
+        }
       }
-      l += sum;
+      l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       // the P buffer is free once the previous tile's PV has finished
       if (j > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
@@ -446,14 +487,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
 #pragma unroll
       for (int c = 0; c < BN / 8; ++c) {
         uint4 hi, lo;
-        uint32_t *h = &hi.x, *lw = &lo.x;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = x[c * 8 + 2 * e], p1 = x[c * 8 + 2 * e + 1];
-          h[e] = pack2<DT>(p0, p1);
-          const float2 hf = unpack2<DT>(h[e]);
-          lw[e] = pack2<DT>(p0 - hf.x, p1 - hf.y);
-        }
+        split2<DT>(x[c * 8 + 0], x[c * 8 + 1], hi.x, lo.x);
+        split2<DT>(x[c * 8 + 2], x[c * 8 + 3], hi.y, lo.y);
+        split2<DT>(x[c * 8 + 4], x[c * 8 + 5], hi.z, lo.z);
+        split2<DT>(x[c * 8 + 6], x[c * 8 + 7], hi.w, lo.w);
         *(uint4 *)(smem + kOffPh + sw128(r, c)) = hi;
         *(uint4 *)(smem + kOffPl + sw128(r, c)) = lo;
       }

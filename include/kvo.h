@@ -213,11 +213,15 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch,
  * k_host/v_host (row j - N), rows of n_kv_heads * head_dim values.
  *
  * Staged mode (arena != NULL; ExLlamaV3 qsa-kv-offload patch,
- * qsa_sparse_attend_rows_staged): the host tail is walked in buckets of
- * arena_bytes / (2 * row_bytes) cells (the arena holds one bucket of K and
- * one of V); each bucket is copied host -> arena by the copy engine once,
- * every query row is scored against it in launches of rows_per_launch rows,
- * and each launch folds its partial (m, l, acc) into the running softmax
+ * qsa_sparse_attend_rows_staged): the host tail is walked in buckets.  The
+ * arena is used as two slots of arena_bytes / (4 * row_bytes) cells of K and
+ * of V (one slot of arena_bytes / (2 * row_bytes) cells if a slot would hold
+ * no row); each bucket is copied host -> slot once by the copy engine on a
+ * library-owned side stream (created on first use, joined back into
+ * `stream` before the call's work ends), so the next bucket's copy overlaps
+ * the current bucket's scoring.  Every query row is scored against a bucket
+ * in launches of rows_per_launch rows, and each launch folds its partial
+ * (m, l, acc) into the running softmax
  *     m' = max(m, m_b), acc = e^(m-m') acc + e^(m_b-m') acc_b,
  *     l = e^(m-m') l + e^(m_b-m') l_b
  * (a bucket a row cannot see contributes nothing); the end result is
