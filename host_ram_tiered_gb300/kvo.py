@@ -20,6 +20,7 @@ KVO_SWAP_SRC_ORDER_ANY = 0x4
 KVO_SWAP_FORCE_SM = 0x8
 KVO_SWAP_FORCE_CE = 0x10
 KVO_SWAP_CE_MIN_MEAN_BYTES = 1 << 20
+KVO_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 STATUS = {0: "KVO_OK", -1: "KVO_ERR_ARG", -2: "KVO_ERR_ALIGN", -3: "KVO_ERR_NOT_MAPPED",
           -4: "KVO_ERR_UNSUPPORTED", -5: "KVO_ERR_CUDA", -6: "KVO_ERR_WORKSPACE"}
@@ -40,6 +41,9 @@ SIGNATURES = {
     "kvo_attn_decode_tiered": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp,
                                       _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz,
                                       _vp]),
+    "kvo_attn_decode_tiered_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp,
+                                              _vp, _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp,
+                                              _vp]),
     "kvo_attn_prefill_workspace_bytes": (_sz, [_i64, _i64]),
     "kvo_attn_prefill_tiered": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                        _int, _i64, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz,
@@ -144,6 +148,19 @@ def kvo_attn_decode_tiered(q, q_dtype, batch, n_q_heads, n_kv_heads, head_dim, k
         vram_seq_stride_rows, _p(k_host), _p(v_host), host_seq_stride_rows, kv_dtype, _p(ctx_len),
         max_ctx, n_vram_cells, scale, _p(staging_k), _p(staging_v), _p(out), _p(workspace),
         workspace_bytes, _s(stream)), "kvo_attn_decode_tiered")
+
+
+def kvo_attn_decode_tiered_noalloc(q, q_dtype, batch, n_q_heads, n_kv_heads, head_dim, k_vram,
+                                   v_vram, vram_seq_stride_rows, k_host, v_host,
+                                   host_seq_stride_rows, kv_dtype, ctx_len, max_ctx, n_vram_cells,
+                                   scale, staging_k, staging_v, out, stream=None) -> None:
+    """kvo_attn_decode_tiered for callers that cannot provide a workspace: the
+    partials go to the library's fixed 8 MiB device scratch array."""
+    _check(load().kvo_attn_decode_tiered_noalloc(
+        _p(q), q_dtype, batch, n_q_heads, n_kv_heads, head_dim, _p(k_vram), _p(v_vram),
+        vram_seq_stride_rows, _p(k_host), _p(v_host), host_seq_stride_rows, kv_dtype, _p(ctx_len),
+        max_ctx, n_vram_cells, scale, _p(staging_k), _p(staging_v), _p(out), _s(stream)),
+        "kvo_attn_decode_tiered_noalloc")
 
 
 def kvo_attn_prefill_workspace_bytes(rows, n_q_heads) -> int:

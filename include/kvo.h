@@ -202,6 +202,47 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch,
                            size_t workspace_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * kvo_attn_decode_tiered_noalloc -- the same decode with no workspace
+ * argument.  The source pages have no counterpart: this entry point exists
+ * for callers that cannot give the library a device buffer, for example a
+ * serving loop whose device memory was reserved up front by a framework's
+ * caching allocator (a separate cudaMalloc there can fail, fragment the
+ * pool or synchronise the device), or a plain C host without a device
+ * allocator of its own.
+ *
+ * Arguments, layouts and errors are those of kvo_attn_decode_tiered, minus
+ * workspace / workspace_bytes.  The split partials live in one file-scope
+ * device array of KVO_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading
+ * the library holds until the process exits; the call itself allocates
+ * nothing (no cudaMalloc, no cudaFree).  The split length is the regular
+ * one, lengthened in 32-cell steps until the partials fit, so results agree
+ * with kvo_attn_decode_tiered within the decode tolerance (not bit for bit
+ * when the lengths differ).
+ *   - batch * n_q_heads * (head_dim + 2) * 4 > KVO_NOALLOC_SCRATCH_BYTES
+ *     returns KVO_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Every call shares the array and leaves its partials there.  Calls
+ *     whose GPU work overlaps (two streams, or two host threads) race on it;
+ *     order them on one stream or serialise them.  No part of the array needs
+ *     clearing: each call writes every partial before reading it.
+ * ---------------------------------------------------------------------- */
+#define KVO_NOALLOC_SCRATCH_BYTES (8 << 20)
+
+int kvo_attn_decode_tiered_noalloc(const void *q, int q_dtype, int64_t batch,
+                                   int64_t n_q_heads, int64_t n_kv_heads,
+                                   int64_t head_dim, const void *k_vram,
+                                   const void *v_vram,
+                                   int64_t vram_seq_stride_rows,
+                                   const void *k_host, const void *v_host,
+                                   int64_t host_seq_stride_rows, int kv_dtype,
+                                   const int32_t *ctx_len, int64_t max_ctx,
+                                   int64_t n_vram_cells, float scale,
+                                   void *staging_k, void *staging_v,
+                                   float *out, void *stream);
+
+/* ------------------------------------------------------------------------
  * kvo_attn_prefill_tiered -- causal chunked-prefill GQA attention over a
  * tiered cache (one sequence).
  *
