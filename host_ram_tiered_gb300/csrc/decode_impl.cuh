@@ -4,16 +4,19 @@
 // the arithmetic does not depend on where a cell lives, so a tiered cache
 // gives output bit-identical to an all-VRAM one.
 //
-// Layout of one CTA: one warp per kv head (n_kv_heads warps); lane l owns
-// head dims [l*D/32, (l+1)*D/32) of the warp's G = n_q_heads/n_kv_heads
-// query heads.  A tile of T cell rows (all kv heads, 16-byte aligned rows)
-// is copied into shared memory with 16-byte loads, coalesced across the CTA,
-// from whichever tier holds each cell.  Scores use a fixed butterfly
-// reduction; the softmax is online in the log2 domain; q8_0 blocks are
-// dequantised while a lane reads its dims from shared memory (d * q is exact
-// in fp32).  Each CTA handles one fixed cell range (split) and writes an
-// unnormalised partial (m, l, acc); a second kernel folds the splits of a
-// head in ascending order.  Instantiated per K/V dtype in decode_<dtype>.cu.
+// One CTA = one fixed cell range (split) of one sequence, one warp per kv
+// head (n_kv_heads warps).  A tile of 32 cell rows (all kv heads, 16-byte
+// chunks, coalesced across the CTA) is copied into shared memory from
+// whichever tier holds each cell, rows padded so that lane-per-row reads hit
+// distinct banks.  Scores: lane c owns cell c of the tile and computes its
+// G dot products against the warp's query heads, which sit in shared memory
+// pre-scaled by scale*log2(e) (for q8_0 the block scale multiplies each
+// 32-value partial; d * q is exact in fp32).  Online softmax in the log2
+// domain with warp-wide max / sum (fixed butterflies).  P*V: lane l owns head
+// dims [l*D/32, (l+1)*D/32) and walks the tile's cells in order with the
+// weights broadcast from shared memory.  Each CTA writes an unnormalised
+// partial (m, l, acc); a second kernel folds the splits of a head in a fixed
+// order.  Instantiated per K/V dtype in decode_<dtype>.cu.
 #pragma once
 #include <cuda_fp16.h>
 #include <math.h>
@@ -70,12 +73,25 @@ __device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, f
   }
 }
 
-// Copy cell rows [c0, c0 + n) of sequence b (K and V) into shared memory.
+constexpr int kTile = 32;                             // cells per tile (one per lane)
+
+// Shared-memory pitch of a cell row: 16 B of padding for 16-byte reads
+// (f16/bf16), 4 B for the 2-byte reads of q8_0 blocks.
+template <int KVT>
+__host__ __device__ constexpr int64_t row_pitch(int64_t rb) {
+  return KVT == KVO_Q8_0 ? rb + 4 : rb + 16;
+}
+
+// Copy cell rows [c0, c0 + n) of sequence b (K and V) into shared memory;
+// V rows n..kTile-1 are zeroed (their weights are 0 and must meet finite
+// values).
+template <int KVT>
 __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0, int n,
                                           uint8_t *sk, uint8_t *sv) {
   const int64_t rb = a.row_bytes;
+  const int64_t pitch = row_pitch<KVT>(rb);
   const int cpr = (int)(rb >> 4);                    // 16-byte chunks per row
-  const int total = n * cpr;
+  const int total = kTile * cpr;                     // per tensor, full tile
   const int nthr = blockDim.x;
   constexpr int kBatch = 8;
   for (int base = 0; base < 2 * total; base += kBatch * nthr) {
@@ -83,15 +99,18 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * nthr + (int)threadIdx.x;
+      v[u] = make_int4(0, 0, 0, 0);
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
         const int r = k / cpr, ch = k - r * cpr;
-        const int64_t j = c0 + r;
-        const uint8_t *src;
-        if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
-        else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
-        v[u] = *((const int4 *)src + ch);
+        if (r < n) {
+          const int64_t j = c0 + r;
+          const uint8_t *src;
+          if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
+          else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
+          v[u] = *((const int4 *)src + ch);
+        }
       }
     }
 #pragma unroll
@@ -100,13 +119,79 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
-        *((int4 *)((is_v ? sv : sk)) + k) = v[u];
+        const int r = k / cpr, ch = k - r * cpr;
+        uint8_t *dst = (is_v ? sv : sk) + r * pitch + ch * 16;
+        if constexpr (KVT == KVO_Q8_0) {
+          uint32_t *d4 = (uint32_t *)dst;             // pitch is a multiple of 4 only
+          d4[0] = (uint32_t)v[u].x; d4[1] = (uint32_t)v[u].y;
+          d4[2] = (uint32_t)v[u].z; d4[3] = (uint32_t)v[u].w;
+        } else {
+          *(int4 *)dst = v[u];
+        }
       }
     }
   }
 }
 
-template <int KVT, int QT, int G, int D, int T>
+// Dot products of one cell's kv head g (row in shared memory) with the G
+// query heads (qs: [G][D] fp32, pre-scaled), into s[G].
+template <int KVT, int G, int D>
+__device__ __forceinline__ void cell_scores(const uint8_t *row, int g, const float *qs, float *s) {
+#pragma unroll
+  for (int h = 0; h < G; ++h) s[h] = 0.f;
+  if constexpr (KVT == KVO_Q8_0) {
+    constexpr int NB = D / 32;
+#pragma unroll
+    for (int bk = 0; bk < NB; ++bk) {
+      const uint8_t *blk = row + (g * NB + bk) * 34;
+      const float d = __half2float(__ushort_as_half(*(const uint16_t *)blk));
+      float sb[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) sb[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        const uint16_t w0 = *(const uint16_t *)(blk + 2 + i);
+        const uint16_t w1 = *(const uint16_t *)(blk + 4 + i);
+        const float k0 = (float)(int8_t)(w0 & 0xff), k1 = (float)(int8_t)(w0 >> 8);
+        const float k2 = (float)(int8_t)(w1 & 0xff), k3 = (float)(int8_t)(w1 >> 8);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 q = *(const float4 *)(qs + h * D + bk * 32 + i);
+          sb[h] = fmaf(q.x, k0, sb[h]);
+          sb[h] = fmaf(q.y, k1, sb[h]);
+          sb[h] = fmaf(q.z, k2, sb[h]);
+          sb[h] = fmaf(q.w, k3, sb[h]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] = fmaf(d, sb[h], s[h]);
+    }
+  } else {
+    const uint8_t *hrow = row + g * D * 2;
+#pragma unroll 4
+    for (int dc = 0; dc < D / 8; ++dc) {
+      const uint4 u = *(const uint4 *)(hrow + dc * 16);
+      float k[8];
+      k[0] = h2f(u.x & 0xffff, KVT); k[1] = h2f(u.x >> 16, KVT);
+      k[2] = h2f(u.y & 0xffff, KVT); k[3] = h2f(u.y >> 16, KVT);
+      k[4] = h2f(u.z & 0xffff, KVT); k[5] = h2f(u.z >> 16, KVT);
+      k[6] = h2f(u.w & 0xffff, KVT); k[7] = h2f(u.w >> 16, KVT);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float4 q0 = *(const float4 *)(qs + h * D + dc * 8);
+        const float4 q1 = *(const float4 *)(qs + h * D + dc * 8 + 4);
+        float t = s[h];
+        t = fmaf(q0.x, k[0], t); t = fmaf(q0.y, k[1], t);
+        t = fmaf(q0.z, k[2], t); t = fmaf(q0.w, k[3], t);
+        t = fmaf(q1.x, k[4], t); t = fmaf(q1.y, k[5], t);
+        t = fmaf(q1.z, k[6], t); t = fmaf(q1.w, k[7], t);
+        s[h] = t;
+      }
+    }
+  }
+}
+
+template <int KVT, int QT, int G, int D>
 __global__ void __launch_bounds__(256)
 decode_split_kernel(const DecodeArgs a) {
   constexpr int DPL = D / 32;
@@ -117,64 +202,62 @@ decode_split_kernel(const DecodeArgs a) {
   const int64_t cs = (int64_t)split * a.split_cells;
   const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
   if (cs >= ce) return;                               // split beyond the context: never combined
-  const int64_t rb = a.row_bytes;
-  uint8_t *sk = smem;
-  uint8_t *sv = smem + (size_t)T * rb;
+  const int64_t pitch = row_pitch<KVT>(a.row_bytes);
+  float *qs_all = (float *)smem;                                    // [Hq][D]
+  float *ps_all = qs_all + (size_t)a.n_q_heads * D;                 // [Hkv][G][kTile]
+  uint8_t *sk = (uint8_t *)(ps_all + (size_t)a.n_kv_heads * G * kTile);
+  uint8_t *sv = sk + (size_t)kTile * pitch;
+  float *qs = qs_all + (size_t)g * G * D;
+  float *ps = ps_all + (size_t)g * G * kTile;
 
-  float qv[G][DPL], acc[G][DPL], m[G], l[G];
+  // query heads of this sequence, pre-scaled, into shared memory
+  for (int i = threadIdx.x; i < a.n_q_heads * D; i += blockDim.x)
+    qs_all[i] = h2f(((const uint16_t *)a.q)[(size_t)b * a.n_q_heads * D + i], QT) * a.scale_log2;
+
+  float acc[G][DPL], m[G], l[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const uint16_t *qh = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + g * G + h) * D + lane * DPL;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      qv[h][i] = h2f(qh[i], QT) * a.scale_log2;
-      acc[h][i] = 0.f;
-    }
+    for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
     m[h] = -INFINITY;
     l[h] = 0.f;
   }
 
-  for (int64_t t0 = cs; t0 < ce; t0 += T) {
-    const int n = ce - t0 < T ? (int)(ce - t0) : T;
+  for (int64_t t0 = cs; t0 < ce; t0 += kTile) {
+    const int n = ce - t0 < kTile ? (int)(ce - t0) : kTile;
     __syncthreads();                                  // previous tile fully consumed
-    load_tile(a, b, t0, n, sk, sv);
+    load_tile<KVT>(a, b, t0, n, sk, sv);
     __syncthreads();
-    float s_mine[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) s_mine[h] = -INFINITY;
-    for (int c = 0; c < n; ++c) {
-      float kd[DPL];
-      lane_dims<KVT, D>(sk + (size_t)c * rb, g, lane, kd);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float p = 0.f;
-#pragma unroll
-        for (int i = 0; i < DPL; ++i) p = fmaf(qv[h][i], kd[i], p);
-        p = warp_sum(p);
-        if (lane == c) s_mine[h] = p;
-      }
-    }
-    float p_mine[G];
+    float sc[G];
+    cell_scores<KVT, G, D>(sk + (size_t)lane * pitch, g, qs, sc);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float mt = warp_max(s_mine[h]);
-      const float m_new = fmaxf(m[h], mt);
+      const float sv_h = lane < n ? sc[h] : -INFINITY;
+      const float m_new = fmaxf(m[h], warp_max(sv_h));
       const float alpha = exp2f(m[h] - m_new);
-      const float p = lane < n ? exp2f(s_mine[h] - m_new) : 0.f;
+      const float p = lane < n ? exp2f(sv_h - m_new) : 0.f;
       l[h] = l[h] * alpha + warp_sum(p);
 #pragma unroll
       for (int i = 0; i < DPL; ++i) acc[h][i] *= alpha;
       m[h] = m_new;
-      p_mine[h] = p;
+      ps[h * kTile + lane] = p;
     }
-    for (int c = 0; c < n; ++c) {
-      float vd[DPL];
-      lane_dims<KVT, D>(sv + (size_t)c * rb, g, lane, vd);
+    __syncwarp();
+    for (int c = 0; c < kTile; c += 4) {
+      if (c >= n) break;
+      float4 p4[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float pc = __shfl_sync(0xffffffffu, p_mine[h], c);
+      for (int h = 0; h < G; ++h) p4[h] = *(const float4 *)(ps + h * kTile + c);
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(pc, vd[i], acc[h][i]);
+      for (int cc = 0; cc < 4; ++cc) {
+        float vd[DPL];
+        lane_dims<KVT, D>(sv + (size_t)(c + cc) * pitch, g, lane, vd);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pc = cc == 0 ? p4[h].x : cc == 1 ? p4[h].y : cc == 2 ? p4[h].z : p4[h].w;
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(pc, vd[i], acc[h][i]);
+        }
       }
     }
   }
@@ -248,10 +331,11 @@ decode_combine_kernel(const DecodeArgs a) {
   }
 }
 
-template <int KVT, int QT, int G, int D, int T>
-cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
-  const size_t smem = (size_t)2 * T * a.row_bytes;
-  auto k = decode_split_kernel<KVT, QT, G, D, T>;
+template <int KVT, int QT, int G, int D>
+cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
+  const size_t smem = (size_t)a.n_q_heads * D * 4 + (size_t)a.n_kv_heads * G * kTile * 4 +
+                      (size_t)2 * kTile * row_pitch<KVT>(a.row_bytes);
+  auto k = decode_split_kernel<KVT, QT, G, D>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_splits, a.batch);
@@ -260,12 +344,6 @@ cudaError_t launch_t(const DecodeArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
   return cudaGetLastError();
-}
-
-template <int KVT, int QT, int G, int D>
-cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
-  if ((size_t)2 * 32 * a.row_bytes <= 73728) return launch_t<KVT, QT, G, D, 32>(a, st);
-  return launch_t<KVT, QT, G, D, 16>(a, st);
 }
 
 template <int KVT, int QT, int G>
