@@ -75,11 +75,42 @@ __device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, f
 
 constexpr int kTile = 32;                             // cells per tile (one per lane)
 
-// Shared-memory pitch of a cell row: 16 B of padding for 16-byte reads
-// (f16/bf16), 4 B for the 2-byte reads of q8_0 blocks.
+// Shared-memory pitch of a cell row: 16 bytes of padding, so 16-byte rows
+// stay aligned and lane-per-row reads spread over the banks.
 template <int KVT>
 __host__ __device__ constexpr int64_t row_pitch(int64_t rb) {
-  return KVT == KVO_Q8_0 ? rb + 4 : rb + 16;
+  return rb + 16;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Tile of cell rows [c0, c0 + n) of sequence b (K and V) that lies wholly in
+// device memory: every 16-byte chunk is an asynchronous copy (cp.async,
+// bypassing L1), all in flight at once; V rows n..kTile-1 are zero-filled.
+template <int KVT>
+__device__ __forceinline__ void load_tile_async(const DecodeArgs &a, int b, int64_t c0, int n,
+                                                uint8_t *sk, uint8_t *sv) {
+  const int64_t rb = a.row_bytes;
+  const int64_t pitch = row_pitch<KVT>(rb);
+  const int cpr = (int)(rb >> 4);
+  const int total = kTile * cpr;
+  for (int i = threadIdx.x; i < 2 * total; i += blockDim.x) {
+    const bool is_v = i >= total;
+    const int k = is_v ? i - total : i;
+    const int r = k / cpr, ch = k - r * cpr;
+    const int64_t j = c0 + (r < n ? r : 0);
+    const uint8_t *src;
+    if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
+    else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
+    const uint32_t dst = smem_addr((is_v ? sv : sk) + r * pitch + ch * 16);
+    const uint32_t bytes = r < n ? 16u : 0u;            // 0: zero-fill, nothing read
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                 "l"((const int4 *)src + ch), "r"(bytes)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
 // Copy cell rows [c0, c0 + n) of sequence b (K and V) into shared memory;
@@ -120,14 +151,7 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
         const int r = k / cpr, ch = k - r * cpr;
-        uint8_t *dst = (is_v ? sv : sk) + r * pitch + ch * 16;
-        if constexpr (KVT == KVO_Q8_0) {
-          uint32_t *d4 = (uint32_t *)dst;             // pitch is a multiple of 4 only
-          d4[0] = (uint32_t)v[u].x; d4[1] = (uint32_t)v[u].y;
-          d4[2] = (uint32_t)v[u].z; d4[3] = (uint32_t)v[u].w;
-        } else {
-          *(int4 *)dst = v[u];
-        }
+        *(int4 *)((is_v ? sv : sk) + r * pitch + ch * 16) = v[u];
       }
     }
   }
@@ -209,6 +233,9 @@ decode_split_kernel(const DecodeArgs a) {
   uint8_t *sv = sk + (size_t)kTile * pitch;
   float *qs = qs_all + (size_t)g * G * D;
   float *ps = ps_all + (size_t)g * G * kTile;
+  // Cells wholly in device memory are fetched with asynchronous copies;
+  // host-mapped cells with plain 16-byte loads.  Same bytes either way.
+  const bool dev_split = ce <= a.n_vram || a.hi_device;
 
   // query heads of this sequence, pre-scaled, into shared memory
   for (int i = threadIdx.x; i < a.n_q_heads * D; i += blockDim.x)
@@ -226,7 +253,8 @@ decode_split_kernel(const DecodeArgs a) {
   for (int64_t t0 = cs; t0 < ce; t0 += kTile) {
     const int n = ce - t0 < kTile ? (int)(ce - t0) : kTile;
     __syncthreads();                                  // previous tile fully consumed
-    load_tile<KVT>(a, b, t0, n, sk, sv);
+    if (dev_split) load_tile_async<KVT>(a, b, t0, n, sk, sv);
+    else load_tile<KVT>(a, b, t0, n, sk, sv);
     __syncthreads();
     float sc[G];
     cell_scores<KVT, G, D>(sk + (size_t)lane * pitch, g, qs, sc);

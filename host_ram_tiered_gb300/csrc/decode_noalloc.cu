@@ -119,6 +119,7 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
   a.lo_seq_stride_rows = vram_seq_stride_rows;
   a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host;
   a.hi_seq_stride_rows = host_seq_stride_rows;
+  a.hi_device = (n_hi > 0 && classify(k_host, 1) == kDeviceMem && classify(v_host, 1) == kDeviceMem) ? 1 : 0;
   a.kv_dtype = kv_dtype; a.row_bytes = rb;
   a.ctx_len = ctx_len; a.max_ctx = max_ctx; a.n_vram = n_lo;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -144,6 +145,7 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
     }
     a.k_hi = (const uint8_t *)staging_k; a.v_hi = (const uint8_t *)staging_v;
     a.hi_seq_stride_rows = n_hi;
+    a.hi_device = 1;
   }
   return launch_decode(a, st);
 }

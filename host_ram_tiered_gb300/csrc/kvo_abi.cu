@@ -47,11 +47,15 @@ int classify(const void *p, size_t bytes) {
   return k2 == k ? k : 0;
 }
 
-// Copy ring of the staged prefill: a side stream that fills one arena slot
-// while the launch stream scores the other (created once per device).
+// Streams of the prefill: a side stream that fills one arena slot while the
+// caller's stream scores the other, and a second launch stream so that two
+// row blocks run concurrently (their CTAs fill each other's partial last
+// wave).  Created once per device; every use forks from and joins back into
+// the caller's stream.
 struct Ring {
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr};
+  cudaStream_t side = nullptr, comp2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
+  cudaEvent_t ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr}, done2[2] = {nullptr, nullptr};
 };
 
 Ring *ring() {
@@ -60,11 +64,14 @@ Ring *ring() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   Ring &r = rings[dev];
   if (!r.side) {
-    cudaStream_t s = nullptr;
+    cudaStream_t s = nullptr, s2 = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    cudaEvent_t *ev[6] = {&r.fork, &r.join, &r.ready[0], &r.ready[1], &r.freed[0], &r.freed[1]};
+    if (cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    cudaEvent_t *ev[9] = {&r.fork, &r.join, &r.join2, &r.ready[0], &r.ready[1],
+                          &r.freed[0], &r.freed[1], &r.done2[0], &r.done2[1]};
     for (cudaEvent_t *e : ev)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    r.comp2 = s2;
     r.side = s;
   }
   return &r;
@@ -315,6 +322,7 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
   a.lo_seq_stride_rows = vram_seq_stride_rows;
   a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host;
   a.hi_seq_stride_rows = host_seq_stride_rows;
+  a.hi_device = (n_hi > 0 && classify(k_host, 1) == kDeviceMem && classify(v_host, 1) == kDeviceMem) ? 1 : 0;
   a.kv_dtype = kv_dtype; a.row_bytes = rb;
   a.ctx_len = ctx_len; a.max_ctx = max_ctx; a.n_vram = n_lo;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -339,6 +347,7 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
     }
     a.k_hi = (const uint8_t *)staging_k; a.v_hi = (const uint8_t *)staging_v;
     a.hi_seq_stride_rows = n_hi;
+    a.hi_device = 1;
   }
   return launch_decode(a, st);
 }
@@ -425,17 +434,22 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
     else for (int64_t c = n_lo; c < c_end; c += bucket) segs.push_back({c, c + bucket < c_end ? c + bucket : c_end});
   }
   float *ml = (float *)workspace;
-  // Staged mode: buckets go through the arena slots on a side stream; the
-  // launch stream waits for a slot's copy and releases it after its launches.
+  // Staged mode: buckets go through the arena slots on the side stream; the
+  // launch streams wait for a slot's copy and release it after their
+  // launches.  Row blocks alternate between the caller's stream and comp2.
+  const int64_t n_blocks = (rows + rows_per_launch - 1) / rows_per_launch;
+  const bool staged = arena && n_hi > 0;
+  const bool two = n_blocks > 1;
   Ring *rg = nullptr;
   static std::mutex ring_mu;
   std::unique_lock<std::mutex> lock(ring_mu, std::defer_lock);
-  if (arena && n_hi > 0) {
+  if (staged || two) {
     lock.lock();
     rg = ring();
-    if (!rg) return fail(KVO_ERR_CUDA, "kvo_attn_prefill_tiered: copy stream unavailable");
+    if (!rg) return fail(KVO_ERR_CUDA, "kvo_attn_prefill_tiered: library streams unavailable");
     int e = cuda_status(cudaEventRecord(rg->fork, st), "cudaEventRecord");
-    if (!e) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");
+    if (!e && staged) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");
+    if (!e && two) e = cuda_status(cudaStreamWaitEvent(rg->comp2, rg->fork, 0), "cudaStreamWaitEvent");
     if (e) return e;
   }
   int64_t bi = 0;                                       // bucket index
@@ -457,6 +471,7 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       if (!e) e = cuda_status(cudaMemcpyAsync((void *)v_slot, vs, bytes, cudaMemcpyDefault, rg->side), "arena copy V");
       if (!e) e = cuda_status(cudaEventRecord(rg->ready[slot], rg->side), "cudaEventRecord");
       if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->ready[slot], 0), "cudaStreamWaitEvent");
+      if (!e && two) e = cuda_status(cudaStreamWaitEvent(rg->comp2, rg->ready[slot], 0), "cudaStreamWaitEvent");
       if (e) return e;
       a.k_hi = k_slot; a.v_hi = v_slot; a.hi_origin = s.c0;
     } else if (tail) {
@@ -464,6 +479,7 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
     }
     for (int64_t r0 = 0; r0 < rows; r0 += rows_per_launch) {
       const int64_t r1 = r0 + rows_per_launch < rows ? r0 + rows_per_launch : rows;
+      cudaStream_t ls = (two && ((r0 / rows_per_launch) & 1)) ? rg->comp2 : st;
       // Rows of this block see cells < q_pos0 + r1; the segments that can
       // hold such cells are the ones starting before it.
       const int64_t vis_end = q_pos0 + r1;
@@ -484,25 +500,37 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       if (!tail) {
         // VRAM head: tensor cores fed by TMA
         a.hi_origin = 0;
-        e = launch_prefill_tc(a, k_vram, v_vram, n_lo, st);
+        e = launch_prefill_tc(a, k_vram, v_vram, n_lo, ls);
       } else if (arena) {
         // arena bucket: tensor cores fed by TMA
-        e = launch_prefill_tc(a, k_slot, v_slot, s.c1 - s.c0, st);
+        e = launch_prefill_tc(a, k_slot, v_slot, s.c1 - s.c0, ls);
       } else {
         // direct: host tail read through the mapping by the mma.sync kernel
-        e = launch_prefill(a, st);
+        e = launch_prefill(a, ls);
       }
       if (e) return e;
     }
     if (tail && arena) {
-      int e = cuda_status(cudaEventRecord(rg->freed[slot], st), "cudaEventRecord");
+      int e = KVO_OK;
+      if (two) {
+        e = cuda_status(cudaEventRecord(rg->done2[slot], rg->comp2), "cudaEventRecord");
+        if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->done2[slot], 0), "cudaStreamWaitEvent");
+      }
+      if (!e) e = cuda_status(cudaEventRecord(rg->freed[slot], st), "cudaEventRecord");
       if (e) return e;
       ++bi;
     }
   }
   if (rg) {
-    int e = cuda_status(cudaEventRecord(rg->join, rg->side), "cudaEventRecord");
-    if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->join, 0), "cudaStreamWaitEvent");
+    int e = KVO_OK;
+    if (staged) {
+      e = cuda_status(cudaEventRecord(rg->join, rg->side), "cudaEventRecord");
+      if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->join, 0), "cudaStreamWaitEvent");
+    }
+    if (!e && two) {
+      e = cuda_status(cudaEventRecord(rg->join2, rg->comp2), "cudaEventRecord");
+      if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->join2, 0), "cudaStreamWaitEvent");
+    }
     if (e) return e;
   }
   if (segs.empty()) {

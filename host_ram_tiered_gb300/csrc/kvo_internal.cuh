@@ -44,6 +44,7 @@ struct DecodeArgs {
   int batch, n_q_heads, n_kv_heads, head_dim, group;
   const uint8_t *k_lo, *v_lo;  int64_t lo_seq_stride_rows;   // cells [0, N)
   const uint8_t *k_hi, *v_hi;  int64_t hi_seq_stride_rows;   // cells [N, L), row j - N
+  int hi_device;               // k_hi / v_hi are device memory (staging, or a device tail)
   int kv_dtype; int64_t row_bytes;
   const int32_t *ctx_len; int64_t max_ctx, n_vram;
   float scale_log2;            // scale * log2(e)

@@ -4,10 +4,13 @@
 //
 // Per CTA: 128 MMA rows (128/G query positions x the G query heads of one kv
 // head) against the whole cell range in tiles of 128 cells.
-//   warp 0  (one lane): TMA producer, K/V tiles (two 64-dim SW128 boxes each)
+//   warps 0-7         : softmax and epilogue; warps w and w+4 share the TMEM
+//                       lanes (rows) 32*(w%4).., each taking half of the 128
+//                       columns of a row, and exchange their row maxima
+//                       through shared memory once per tile;
+//   warp 8  (one lane): TMA producer, K/V tiles (two 64-dim SW128 boxes each)
 //                       into a 2-stage ring;
-//   warp 1  (one lane): MMA issuer; the warp owns the TMEM allocation;
-//   warps 4-7         : softmax (thread = row = TMEM lane) and epilogue.
+//   warp 9  (one lane): MMA issuer; the warp owns the TMEM allocation.
 // S = Q K^T goes to one of two TMEM buffers (fp32, 128 columns each) while
 // the softmax reads the other; O = P V accumulates in a third TMEM region.
 // P is written to shared memory (SW128 K-major) as a pair hi + lo of the
@@ -34,7 +37,9 @@ namespace {
 constexpr int BM = 128;                  // MMA rows per CTA
 constexpr int BN = 128;                  // cells per tile
 constexpr int HD = 128;                  // head dim
-constexpr int kThreads = 256;
+constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kSoftmaxThreads = 256;
+constexpr int kHalfCols = BN / 2;  // S / O columns per softmax thread
 constexpr int kHalf = BM * 128;          // one SW128 half tile: 128 rows x 128 B = 16 KiB
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 B
 constexpr int kStages = 2;
@@ -49,8 +54,11 @@ constexpr int kOffK = kOffQ + kTile;                     // kStages K tiles
 constexpr int kOffV = kOffK + kStages * kTile;           // kStages V tiles
 constexpr int kOffPh = kOffV + kStages * kTile;          // P hi
 constexpr int kOffPl = kOffPh + kTile;                   // P lo
-constexpr int kOffBar = kOffPl + kTile;                  // mbarriers
-constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + alignment slack
+constexpr int kOffBar = kOffPl + kTile;                  // mbarriers (9 x 8 B) + TMEM slot
+constexpr int kOffX = kOffBar + 128;                     // row-max exchange [2][2][128], flags
+constexpr int kSlack = 768;                              // room to align the base to 1024 B
+constexpr int kSmemBytes = kOffX + 4 * BM * 4 + 16 + kSlack;
+static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -245,13 +253,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                   const TcParams P) {
   constexpr int PB = BM / G;                         // query positions per CTA
   const PrefillArgs &a = P.a;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // SW128 tiles want a 1024-byte aligned base; the slack covers up to
+  // kSlack bytes of misalignment, beyond which the CTA reports and exits.
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > (uint32_t)kSlack) {
+    if (threadIdx.x == 0) atomicOr(P.err, kErrTimeout);
+    return;
+  }
+  uint8_t *smem = smem_raw + pad;
   uint64_t *bar = (uint64_t *)(smem + kOffBar);
   uint64_t *full = bar;                    // [kStages] TMA -> MMA
   uint64_t *empty = bar + kStages;         // [kStages] MMA -> TMA
   uint64_t *s_full = bar + 2 * kStages;    // [2]       MMA -> softmax
-  uint64_t *p_full = bar + 2 * kStages + 2;    // softmax -> MMA (128 arrivals)
+  uint64_t *p_full = bar + 2 * kStages + 2;    // softmax -> MMA (256 arrivals)
   uint64_t *o_done = bar + 2 * kStages + 3;    // MMA -> softmax (PV finished)
   uint64_t *fin = bar + 2 * kStages + 4;       // MMA teardown
   uint32_t *tmem_slot = (uint32_t *)(bar + 2 * kStages + 5);
@@ -271,12 +286,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);
+    mbar_init(p_full, kSoftmaxThreads);
     mbar_init(o_done, 1);
     mbar_init(fin, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) {
+  if (warp == 9) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
@@ -299,7 +314,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp == 0) {
+  float *xmax = (float *)(smem + kOffX);                 // [2 parity][2 halves][BM]
+  // abort flags by tile parity: a timeout seen before tile j's exchange
+  // barrier sets flag[j & 1], one seen after it sets flag[(j + 1) & 1]; both
+  // are read only after the barrier they belong to, so all 256 softmax
+  // threads take the same decision.
+  volatile int *abort_flag = (int *)(smem + kOffX + 4 * BM * 4);
+  if (tid == 0) abort_flag[0] = abort_flag[1] = 0;
+  __syncthreads();
+  if (warp == 8) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n_tiles > 0) {
       int issued = 0;
@@ -323,7 +346,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           mbar_wait(&full[j % kStages], (j / kStages) & 1, P.err);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t id_s = idesc<DT>(false);
@@ -375,66 +398,82 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       umma_commit(fin);
       mbar_wait(fin, 0, P.err);
     }
-  } else if (warp >= 4) {
+  } else {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int r = tid - 128;                                  // row = TMEM lane
+    // Thread (warp w, lane) owns row r = 32*(w%4) + lane and the columns
+    // [hf*64, hf*64 + 64) of it, hf = w / 4.  Waits are bounded; a timeout
+    // sets an abort flag that every softmax thread reads after the next
+    // exchange barrier, so all 256 leave the loop together.
+    const int r = (warp & 3) * 32 + lane;                     // row = TMEM lane
+    const int hf = warp >> 2;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t o_addr = lane_addr + kColO + hf * kHalfCols;
     const int pi = r / G;
     const bool row_ok = pi < n_pos;
     const int64_t pos = a.pos0 + i0 + pi;
     const size_t row_idx = (size_t)(i0 + pi) * a.n_q_heads + g * G + (r % G);
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f;                        // l: this half's sum
     bool o_valid = !a.init;                                   // O holds data (from the state)
     if (!a.init && row_ok) {
       m_used = a.ml[row_idx * 2];
-      l = a.ml[row_idx * 2 + 1];
+      l = hf == 0 ? a.ml[row_idx * 2 + 1] : 0.f;
     }
     if (!a.init) {
-      // load the running accumulator into TMEM (rows past the launch get zeros)
+      // load this half of the running accumulator into TMEM (zeros past the launch)
       float v[32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kHalfCols / 32; ++q) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + q * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + hf * kHalfCols + q * 32 + i)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
           v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
         }
-        tmem_st32(lane_addr + kColO + q * 32, v);
+        tmem_st32(o_addr + q * 32, v);
       }
       tmem_wait_st();
     }
     tc_fence_before();
     const int64_t first_pos = a.pos0 + i0;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, P.err));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t s_addr = lane_addr + ((j & 1) ? kColS1 : kColS0);
-      float x[BN];
+    for (int j = 0; j < n_tiles; ++j) {
+      bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, P.err));
+      float x[kHalfCols];
+      float mloc = -INFINITY;
+      const int64_t t0 = a.c0 + (int64_t)j * BN + hf * kHalfCols;
+      const bool need_mask = (t0 + kHalfCols > c_end) || (t0 + kHalfCols - 1 > first_pos) || !row_ok;
+      if (okw) {
+        tc_fence_after();
+        const uint32_t s_addr = lane_addr + ((j & 1) ? kColS1 : kColS0) + hf * kHalfCols;
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
-      tmem_wait_ld();
-      const int64_t t0 = a.c0 + (int64_t)j * BN;
-      const bool need_mask = (t0 + BN > c_end) || (t0 + BN - 1 > first_pos) || !row_ok;
-      if (need_mask) {
+        for (int q = 0; q < kHalfCols / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+        if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
-          const int64_t cj = t0 + i;
-          if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
+          for (int i = 0; i < kHalfCols; ++i) {
+            const int64_t cj = t0 + i;
+            if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
+          }
         }
+        // half-row max of the raw scores (scale > 0), 8 independent chains
+        float mx[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < kHalfCols; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+        mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      } else if (lane == 0) {
+        abort_flag[j & 1] = 1;
       }
-      // row max of the raw scores (scale > 0), 8 independent chains
-      float mx[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = x[k];
-#pragma unroll
-      for (int i = 8; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      const float mraw = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // exchange the half-row maxima (double-buffered by tile parity)
+      xmax[((j & 1) * 2 + hf) * BM + r] = mloc;
+      asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+      if (abort_flag[j & 1]) break;
+      const float mraw = fmaxf(mloc, xmax[((j & 1) * 2 + (hf ^ 1)) * BM + r]);
       const float mt = mraw * a.scale_log2;
       // Lazy rescale (warp-uniform: tcgen05.ld/st are warp-collective): a row
       // whose tile max exceeds its reference by more than 2^8 moves its
       // reference to the tile max and rescales l and O by 2^(old - new).
+      // Both halves of a row see the same mt and take the same decision.
       const bool mine = mt > m_used + kLazy;
       float alpha = 1.f;
       if (mine) alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - mt);
@@ -442,20 +481,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         l *= alpha;
         if (o_valid) {
           if (j > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
-            if (!ok) break;
+            okw = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
             tc_fence_after();
           }
-          float v[32];
+          if (okw) {
+            float v[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            tmem_ld32(lane_addr + kColO + q * 32, v);
-            tmem_wait_ld();
+            for (int q = 0; q < kHalfCols / 32; ++q) {
+              tmem_ld32(o_addr + q * 32, v);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(lane_addr + kColO + q * 32, v);
+              for (int i = 0; i < 32; ++i) v[i] *= alpha;
+              tmem_st32(o_addr + q * 32, v);
+            }
+            tmem_wait_st();
           }
-          tmem_wait_st();
         }
       }
       if (mine) m_used = mt;
@@ -465,14 +504,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
       if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
+        for (int i = 0; i < kHalfCols; ++i) {
           const float p = x[i] == -INFINITY ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
           sm[i & 7] += p;
           x[i] = p;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) {
+        for (int i = 0; i < kHalfCols; ++i) {
           const float p = ex2(fmaf(x[i], a.scale_log2, nref));
           sm[i & 7] += p;
           x[i] = p;
@@ -480,19 +519,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       // the P buffer is free once the previous tile's PV has finished
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
-        if (!ok) break;
-      }
+      if (j > 0 && okw) okw = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
+      if (!okw && lane == 0) abort_flag[(j + 1) & 1] = 1;    // leave after the next exchange
 #pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
+      for (int c = 0; c < kHalfCols / 8; ++c) {
         uint4 hi, lo;
         split2<DT>(x[c * 8 + 0], x[c * 8 + 1], hi.x, lo.x);
         split2<DT>(x[c * 8 + 2], x[c * 8 + 3], hi.y, lo.y);
         split2<DT>(x[c * 8 + 4], x[c * 8 + 5], hi.z, lo.z);
         split2<DT>(x[c * 8 + 6], x[c * 8 + 7], hi.w, lo.w);
-        *(uint4 *)(smem + kOffPh + sw128(r, c)) = hi;
-        *(uint4 *)(smem + kOffPl + sw128(r, c)) = lo;
+        *(uint4 *)(smem + kOffPh + sw128(r, hf * 8 + c)) = hi;
+        *(uint4 *)(smem + kOffPl + sw128(r, hf * 8 + c)) = lo;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
@@ -500,16 +537,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       o_valid = true;
     }
     // ---- epilogue: wait for the last PV, then write state or output
-    if (ok && n_tiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, P.err));
+    bool okw = !(abort_flag[0] | abort_flag[1]);
+    if (okw && n_tiles > 0) okw = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, P.err));
     tc_fence_after();
-    if (ok) {
-      const float inv = a.finalize ? 1.f / fmaxf(l, 1e-30f) : 1.f;
+    // the row's total l = sum of both halves' sums (the exchange buffer is
+    // reused once every thread has finished reading its last row maximum)
+    asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+    xmax[hf * BM + r] = l;
+    asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
+    const float l_row = xmax[r] + xmax[BM + r];
+    if (okw) {
+      const float inv = a.finalize ? 1.f / fmaxf(l_row, 1e-30f) : 1.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kHalfCols / 32; ++q) {
         float v[32];
         if (o_valid) {                                       // warp-uniform
-          tmem_ld32(lane_addr + kColO + q * 32, v);
-          tmem_wait_ld();
+          tmem_ld32(o_addr + q * 32, v);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -517,19 +560,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *(float4 *)(a.acc + row_idx * HD + q * 32 + i) =
+            *(float4 *)(a.acc + row_idx * HD + hf * kHalfCols + q * 32 + i) =
                 make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
         }
       }
-      if (!a.finalize && row_ok) {
+      if (!a.finalize && row_ok && hf == 0) {
         a.ml[row_idx * 2] = m_used;
-        a.ml[row_idx * 2 + 1] = l;
+        a.ml[row_idx * 2 + 1] = l_row;
       }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
