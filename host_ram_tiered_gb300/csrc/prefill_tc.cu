@@ -2,25 +2,25 @@
 // cores (tcgen05): one launch = (row block) x (device-resident cell range:
 // the VRAM head or one arena bucket of the host tail).
 //
-// Per CTA: 128 MMA rows (128/G query positions x the G query heads of one kv
-// head) against the whole cell range in tiles of 128 cells.
-//   warps 0-7         : softmax and epilogue; warps w and w+4 share the TMEM
-//                       lanes (rows) 32*(w%4).., each taking half of the 128
-//                       columns of a row, and exchange their row maxima
-//                       through shared memory once per tile;
-//   warp 8  (one lane): TMA producer, K/V tiles (two 64-dim SW128 boxes each)
-//                       into a 2-stage ring;
-//   warp 9  (one lane): MMA issuer; the warp owns the TMEM allocation.
-// S = Q K^T goes to one of two TMEM buffers (fp32, 128 columns each) while
-// the softmax reads the other; O = P V accumulates in a third TMEM region.
-// P is written to shared memory (SW128 K-major) as a pair hi + lo of the
-// input type, so the product keeps ~16 bits of P.  The running max is
-// rescaled lazily (only when the tile max exceeds the reference by more
-// than 2^8), which keeps O exact in fp32 and makes rescales rare.
-// The running (m, l, acc) of earlier launches is folded in at the start and
-// written back at the end (ExLlamaV3 qsa-kv-offload patch, the fold of a
-// bucket's partial into the running softmax), or the output normalised by
-// max(l, 1e-30) on the last launch of a row block.
+// Per CTA: two query tiles A and B of 128 MMA rows each (128/G query
+// positions x the G query heads of one kv head), against the whole cell range
+// in tiles of 128 cells.
+//   warps 0-3          : softmax + epilogue of tile A (thread = row = TMEM lane)
+//   warps 4-7          : softmax + epilogue of tile B
+//   warp 8  (one lane) : TMA producer, K and V tiles (two 64-dim SW128 boxes
+//                        each) into separate 2-stage rings
+//   warp 9  (one lane) : MMA issuer; the warp owns the TMEM allocation.
+// TMEM: S_A, S_B (fp32, 128 columns each) and O_A, O_B (fp32, 128 each).
+// The softmax writes P back over its S columns as a pair hi + lo of the input
+// type (so the product keeps ~16 bits of P), and O += P V is issued with P
+// read from TMEM.  Issue order S_A S_B | PV_A S_A' PV_B S_B' | ... keeps the
+// tensor core busy with one tile while the other tile's softmax runs.
+// The running max is rescaled lazily (only when the tile max exceeds the
+// reference by more than 2^8).  The running (m, l, acc) of earlier launches
+// is folded in at the start and written back at the end (ExLlamaV3
+// qsa-kv-offload patch, the fold of a bucket's partial into the running
+// softmax), or the output normalised by max(l, 1e-30) on the last launch of
+// a row block.
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
 // waiter sets kErrTimeout in the device error word and the CTA winds down.
@@ -34,30 +34,26 @@ namespace kvo {
 
 namespace {
 
-constexpr int BM = 128;                  // MMA rows per CTA
+constexpr int BM = 128;                  // MMA rows per query tile
+constexpr int NQ = 2;                    // query tiles per CTA
 constexpr int BN = 128;                  // cells per tile
 constexpr int HD = 128;                  // head dim
-constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
-constexpr int kSoftmaxThreads = 256;
-constexpr int kHalfCols = BN / 2;  // S / O columns per softmax thread
+constexpr int kThreads = 320;            // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr int kHalf = BM * 128;          // one SW128 half tile: 128 rows x 128 B = 16 KiB
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 B
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr uint32_t kColS = 0, kColO = 256;   // S_q at q*128, O_q at 256 + q*128
 constexpr float kLazy = 8.0f;            // rescale when the max grows by > 2^8
 constexpr uint32_t kErrTimeout = 2u;
 
 // shared memory plan (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;                     // kStages K tiles
+constexpr int kOffQ = 0;                                 // NQ query tiles
+constexpr int kOffK = kOffQ + NQ * kTile;                // kStages K tiles
 constexpr int kOffV = kOffK + kStages * kTile;           // kStages V tiles
-constexpr int kOffPh = kOffV + kStages * kTile;          // P hi
-constexpr int kOffPl = kOffPh + kTile;                   // P lo
-constexpr int kOffBar = kOffPl + kTile;                  // mbarriers (9 x 8 B) + TMEM slot
-constexpr int kOffX = kOffBar + 128;                     // row-max exchange [2][2][128], flags
-constexpr int kSlack = 768;                              // room to align the base to 1024 B
-constexpr int kSmemBytes = kOffX + 4 * BM * 4 + 16 + kSlack;
+constexpr int kOffBar = kOffV + kStages * kTile;         // mbarriers + TMEM slot
+constexpr int kSlack = 1024;                             // room to align the base to 1024 B
+constexpr int kSmemBytes = kOffBar + 256 + kSlack;
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -141,6 +137,15 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       "l"(a), "l"(b), "r"(id), "r"(accum));
 }
 
+// As umma, with matrix A read from TMEM (M lanes x K columns of packed pairs).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t id,
+                                        uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(id), "r"(accum));
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
@@ -188,6 +193,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -251,43 +267,38 @@ template <int DT, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const TcParams P) {
-  constexpr int PB = BM / G;                         // query positions per CTA
+  constexpr int PB = BM / G;                         // query positions per tile
   const PrefillArgs &a = P.a;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // SW128 tiles want a 1024-byte aligned base; the slack covers up to
-  // kSlack bytes of misalignment, beyond which the CTA reports and exits.
+  // SW128 tiles want a 1024-byte aligned base; the slack covers the
+  // misalignment, beyond which the CTA reports and exits.
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  if (pad > (uint32_t)kSlack) {
+  if (pad > (uint32_t)(kSlack - 256)) {
     if (threadIdx.x == 0) atomicOr(P.err, kErrTimeout);
     return;
   }
   uint8_t *smem = smem_raw + pad;
   uint64_t *bar = (uint64_t *)(smem + kOffBar);
-  uint64_t *full = bar;                    // [kStages] TMA -> MMA
-  uint64_t *empty = bar + kStages;         // [kStages] MMA -> TMA
-  uint64_t *s_full = bar + 2 * kStages;    // [2]       MMA -> softmax
-  uint64_t *p_full = bar + 2 * kStages + 2;    // softmax -> MMA (256 arrivals)
-  uint64_t *o_done = bar + 2 * kStages + 3;    // MMA -> softmax (PV finished)
-  uint64_t *fin = bar + 2 * kStages + 4;       // MMA teardown
-  uint32_t *tmem_slot = (uint32_t *)(bar + 2 * kStages + 5);
+  uint64_t *full_k = bar;                  // [kStages] TMA -> MMA
+  uint64_t *empty_k = bar + 2;             // [kStages] MMA -> TMA
+  uint64_t *full_v = bar + 4;
+  uint64_t *empty_v = bar + 6;
+  uint64_t *s_full = bar + 8;              // [NQ] MMA -> softmax (S of tile q ready)
+  uint64_t *p_full = bar + 10;             // [NQ] softmax -> MMA (128 arrivals)
+  uint64_t *o_done = bar + 12;             // [NQ] MMA -> softmax (PV of tile q finished)
+  uint64_t *fin = bar + 14;                // MMA teardown
+  uint32_t *tmem_slot = (uint32_t *)(bar + 15);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
-  const int i0 = blockIdx.x * PB;
-  const int n_pos = a.rows - i0 < PB ? a.rows - i0 : PB;
+  const int i0 = blockIdx.x * (NQ * PB);             // first query row of the CTA
+  const int n_pos = a.rows - i0 < NQ * PB ? a.rows - i0 : NQ * PB;
   const int64_t cta_last = a.pos0 + i0 + n_pos - 1;
   const int64_t c_end = a.c1 < cta_last + 1 ? a.c1 : cta_last + 1;
   const int n_tiles = c_end > a.c0 ? (int)((c_end - a.c0 + BN - 1) / BN) : 0;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, kSoftmaxThreads);
-    mbar_init(o_done, 1);
+    for (int i = 0; i < 14; ++i) mbar_init(&bar[i], (i == 10 || i == 11) ? BM : 1);
     mbar_init(fin, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -298,52 +309,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Q tile (all threads): MMA row r = position r / G, head g*G + r % G.
-  for (int i = tid; i < BM * 16; i += kThreads) {
-    const int r = i >> 4, c = i & 15;
-    const int pi = r / G, hh = r % G;
+  // Query tiles (all threads): row r of tile q = position q*PB + r/G, head g*G + r%G.
+  for (int i = tid; i < NQ * BM * 16; i += kThreads) {
+    const int q = i / (BM * 16), rr = (i >> 4) % BM, c = i & 15;
+    const int pi = q * PB + rr / G, hh = rr % G;
     int4 v = make_int4(0, 0, 0, 0);
     if (pi < n_pos)
       v = *((const int4 *)(a.q + ((size_t)(i0 + pi) * a.n_q_heads + g * G + hh) * HD) + c);
-    *(int4 *)(smem + kOffQ + sw128(r, c)) = v;
+    *(int4 *)(smem + kOffQ + q * kTile + sw128(rr, c)) = v;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // Q visible to the tensor core
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  bool ok = true;
 
-  float *xmax = (float *)(smem + kOffX);                 // [2 parity][2 halves][BM]
-  // abort flags by tile parity: a timeout seen before tile j's exchange
-  // barrier sets flag[j & 1], one seen after it sets flag[(j + 1) & 1]; both
-  // are read only after the barrier they belong to, so all 256 softmax
-  // threads take the same decision.
-  volatile int *abort_flag = (int *)(smem + kOffX + 4 * BM * 4);
-  if (tid == 0) abort_flag[0] = abort_flag[1] = 0;
-  __syncthreads();
   if (warp == 8) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n_tiles > 0) {
-      int issued = 0;
+      bool ok = true;
+      int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int s = j % kStages;
-        if (j >= kStages) ok = mbar_wait(&empty[s], ((j / kStages) - 1) & 1, P.err);
-        if (!ok) break;
         const int y = (int)(a.c0 + (int64_t)j * BN - a.hi_origin);   // row in the segment map
-        mbar_expect_tx(&full[s], 2 * kTile);
+        if (j >= kStages) ok = mbar_wait(&empty_k[s], ((j / kStages) - 1) & 1, P.err);
+        if (!ok) break;
+        mbar_expect_tx(&full_k[s], kTile);
         uint8_t *kd = smem + kOffK + s * kTile;
+        tma_load_2d(kd, &tmap_k, g * HD, y, &full_k[s]);
+        tma_load_2d(kd + kHalf, &tmap_k, g * HD + 64, y, &full_k[s]);
+        issued_k = j + 1;
+        if (j >= kStages) ok = mbar_wait(&empty_v[s], ((j / kStages) - 1) & 1, P.err);
+        if (!ok) break;
+        mbar_expect_tx(&full_v[s], kTile);
         uint8_t *vd = smem + kOffV + s * kTile;
-        tma_load_2d(kd, &tmap_k, g * HD, y, &full[s]);
-        tma_load_2d(kd + kHalf, &tmap_k, g * HD + 64, y, &full[s]);
-        tma_load_2d(vd, &tmap_v, g * HD, y, &full[s]);
-        tma_load_2d(vd + kHalf, &tmap_v, g * HD + 64, y, &full[s]);
-        issued = j + 1;
+        tma_load_2d(vd, &tmap_v, g * HD, y, &full_v[s]);
+        tma_load_2d(vd + kHalf, &tmap_v, g * HD + 64, y, &full_v[s]);
+        issued_v = j + 1;
       }
       if (!ok) {
         // let the copies already issued land before the CTA exits
-        for (int j = issued - kStages < 0 ? 0 : issued - kStages; j < issued; ++j)
-          mbar_wait(&full[j % kStages], (j / kStages) & 1, P.err);
+        for (int j = issued_k - kStages < 0 ? 0 : issued_k - kStages; j < issued_k; ++j)
+          mbar_wait(&full_k[j % kStages], (j / kStages) & 1, P.err);
+        for (int j = issued_v - kStages < 0 ? 0 : issued_v - kStages; j < issued_v; ++j)
+          mbar_wait(&full_v[j % kStages], (j / kStages) & 1, P.err);
       }
     }
   } else if (warp == 9) {
@@ -351,47 +360,68 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t id_s = idesc<DT>(false);
       constexpr uint32_t id_o = idesc<DT>(true);
-      const uint32_t q_base = smem_u32(smem + kOffQ);
-      const uint32_t ph_base = smem_u32(smem + kOffPh);
-      const uint32_t pl_base = smem_u32(smem + kOffPl);
       uint32_t o_acc = a.init ? 0u : 1u;
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {
-          const int s = j % kStages;
-          ok = mbar_wait(&full[s], (j / kStages) & 1, P.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(smem + kOffK + s * kTile);
-          const uint32_t d_s = tmem + ((j & 1) ? kColS1 : kColS0);
+      bool ok = true;
+      // S_q(j) = Q_q K_j^T into the S columns of tile q
+      auto issue_s = [&](int q, int j) {
+        const uint32_t q_base = smem_u32(smem + kOffQ + q * kTile);
+        const uint32_t k_base = smem_u32(smem + kOffK + (j % kStages) * kTile);
 #pragma unroll
-          for (int ks = 0; ks < HD / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-            umma(d_s, sdesc(q_base + off, 16, 1024), sdesc(k_base + off, 16, 1024), id_s, ks > 0);
-          }
-          umma_commit(&s_full[j & 1]);
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
+          umma(tmem + kColS + q * 128, sdesc(q_base + off, 16, 1024), sdesc(k_base + off, 16, 1024),
+               id_s, ks > 0);
         }
-        if (j >= 1) {
-          const int jp = j - 1, s = jp % kStages;
-          ok = mbar_wait(p_full, jp & 1, P.err);
+        umma_commit(&s_full[q]);
+      };
+      // O_q += P_q V_j with P_q (hi and lo pairs over the S columns) read from TMEM
+      auto issue_pv = [&](int q, int j) {
+        const uint32_t v_base = smem_u32(smem + kOffV + (j % kStages) * kTile);
+        const uint32_t d_o = tmem + kColO + q * 128;
+        // cells 16kk..16kk+15: hi pairs at columns 32*(kk/2) + 8*(kk%2), lo 16 further
+        const uint32_t p_base = tmem + kColS + q * 128;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
+          umma_ts(d_o, p_base + 32 * (kk >> 1) + 8 * (kk & 1), bd, id_o, (kk > 0) || o_acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
+          umma_ts(d_o, p_base + 32 * (kk >> 1) + 16 + 8 * (kk & 1), bd, id_o, 1u);
+        }
+        umma_commit(&o_done[q]);
+      };
+      ok = mbar_wait(&full_k[0], 0, P.err);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(&empty_k[0]);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int jn = j + 1;
+        ok = mbar_wait(&full_v[j % kStages], (j / kStages) & 1, P.err);
+        if (!ok) break;
+        ok = mbar_wait(&p_full[0], j & 1, P.err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (jn < n_tiles) {
+          ok = mbar_wait(&full_k[jn % kStages], (jn / kStages) & 1, P.err);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v_base = smem_u32(smem + kOffV + s * kTile);
-          const uint32_t d_o = tmem + kColO;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
-            umma(d_o, sdesc(ph_base + aoff, 16, 1024), bd, id_o, (kk > 0) || o_acc);
-          }
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
-            umma(d_o, sdesc(pl_base + aoff, 16, 1024), bd, id_o, 1u);
-          }
-          o_acc = 1u;
-          umma_commit(o_done);
-          umma_commit(&empty[s]);
+          issue_s(0, jn);
+        }
+        ok = mbar_wait(&p_full[1], j & 1, P.err);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        o_acc = 1u;
+        umma_commit(&empty_v[j % kStages]);
+        if (jn < n_tiles) {
+          issue_s(1, jn);
+          umma_commit(&empty_k[jn % kStages]);
         }
       }
       // all issued tensor-core work has finished once this arrives
@@ -400,80 +430,69 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     }
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
-    // Thread (warp w, lane) owns row r = 32*(w%4) + lane and the columns
-    // [hf*64, hf*64 + 64) of it, hf = w / 4.  Waits are bounded; a timeout
-    // sets an abort flag that every softmax thread reads after the next
-    // exchange barrier, so all 256 leave the loop together.
+    const int q = warp >> 2;                                  // query tile
     const int r = (warp & 3) * 32 + lane;                     // row = TMEM lane
-    const int hf = warp >> 2;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t o_addr = lane_addr + kColO + hf * kHalfCols;
-    const int pi = r / G;
+    const uint32_t s_addr = lane_addr + kColS + q * 128;
+    const uint32_t o_addr = lane_addr + kColO + q * 128;
+    const int pi = q * PB + r / G;
     const bool row_ok = pi < n_pos;
     const int64_t pos = a.pos0 + i0 + pi;
     const size_t row_idx = (size_t)(i0 + pi) * a.n_q_heads + g * G + (r % G);
-    float m_used = -INFINITY, l = 0.f;                        // l: this half's sum
+    float m_used = -INFINITY, l = 0.f;
     bool o_valid = !a.init;                                   // O holds data (from the state)
     if (!a.init && row_ok) {
       m_used = a.ml[row_idx * 2];
-      l = hf == 0 ? a.ml[row_idx * 2 + 1] : 0.f;
+      l = a.ml[row_idx * 2 + 1];
     }
     if (!a.init) {
-      // load this half of the running accumulator into TMEM (zeros past the launch)
+      // load the running accumulator into TMEM (rows past the launch get zeros)
       float v[32];
 #pragma unroll
-      for (int q = 0; q < kHalfCols / 32; ++q) {
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + hf * kHalfCols + q * 32 + i)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + c * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
           v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
         }
-        tmem_st32(o_addr + q * 32, v);
+        tmem_st32(o_addr + c * 32, v);
       }
       tmem_wait_st();
     }
     tc_fence_before();
-    const int64_t first_pos = a.pos0 + i0;
-    for (int j = 0; j < n_tiles; ++j) {
-      bool okw = __all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1, P.err));
-      float x[kHalfCols];
-      float mloc = -INFINITY;
-      const int64_t t0 = a.c0 + (int64_t)j * BN + hf * kHalfCols;
-      const bool need_mask = (t0 + kHalfCols > c_end) || (t0 + kHalfCols - 1 > first_pos) || !row_ok;
-      if (okw) {
-        tc_fence_after();
-        const uint32_t s_addr = lane_addr + ((j & 1) ? kColS1 : kColS0) + hf * kHalfCols;
+    // first position of this tile's rows: cells at or before it are visible to all of them
+    const int64_t first_pos = a.pos0 + i0 + q * PB;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[q], j & 1, P.err));
+      if (!ok) break;
+      tc_fence_after();
+      const int64_t t0 = a.c0 + (int64_t)j * BN;
+      const bool need_mask = (t0 + BN > c_end) || (t0 + BN - 1 > first_pos) || !row_ok;
+      // pass 1: row max of the raw scores (scale > 0), 8 independent chains,
+      // 32 columns at a time
+      float mx[8];
 #pragma unroll
-        for (int q = 0; q < kHalfCols / 32; ++q) tmem_ld32(s_addr + q * 32, x + q * 32);
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(s_addr + c * 32, x);
         if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < kHalfCols; ++i) {
-            const int64_t cj = t0 + i;
+          for (int i = 0; i < 32; ++i) {
+            const int64_t cj = t0 + c * 32 + i;
             if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
           }
         }
-        // half-row max of the raw scores (scale > 0), 8 independent chains
-        float mx[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = x[k];
-#pragma unroll
-        for (int i = 8; i < kHalfCols; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-        mloc = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      } else if (lane == 0) {
-        abort_flag[j & 1] = 1;
+        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
       }
-      // exchange the half-row maxima (double-buffered by tile parity)
-      xmax[((j & 1) * 2 + hf) * BM + r] = mloc;
-      asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
-      if (abort_flag[j & 1]) break;
-      const float mraw = fmaxf(mloc, xmax[((j & 1) * 2 + (hf ^ 1)) * BM + r]);
-      const float mt = mraw * a.scale_log2;
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
       // Lazy rescale (warp-uniform: tcgen05.ld/st are warp-collective): a row
       // whose tile max exceeds its reference by more than 2^8 moves its
       // reference to the tile max and rescales l and O by 2^(old - new).
-      // Both halves of a row see the same mt and take the same decision.
       const bool mine = mt > m_used + kLazy;
       float alpha = 1.f;
       if (mine) alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - mt);
@@ -481,78 +500,69 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         l *= alpha;
         if (o_valid) {
           if (j > 0) {
-            okw = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[q], (j - 1) & 1, P.err));
+            if (!ok) break;
             tc_fence_after();
           }
-          if (okw) {
-            float v[32];
+          float v[32];
 #pragma unroll
-            for (int q = 0; q < kHalfCols / 32; ++q) {
-              tmem_ld32(o_addr + q * 32, v);
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(o_addr + c * 32, v);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              tmem_st32(o_addr + q * 32, v);
-            }
-            tmem_wait_st();
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(o_addr + c * 32, v);
           }
+          tmem_wait_st();
         }
       }
       if (mine) m_used = mt;
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
+      // pass 2: P = 2^(s*scale - ref), written back over the S columns it
+      // came from: chunk c (cells 32c..32c+31) -> hi pairs in columns
+      // 32c..32c+15, lo pairs in 32c+16..32c+31.  The PV of the previous tile
+      // read these columns before this tile's S was written into them.
       float sm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
-      if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < kHalfCols; ++i) {
-          const float p = x[i] == -INFINITY ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
-          sm[i & 7] += p;
-          x[i] = p;
-        }
-      } else {
+      for (int c = 0; c < BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(s_addr + c * 32, x);
+        if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < kHalfCols; ++i) {
-          const float p = ex2(fmaf(x[i], a.scale_log2, nref));
-          sm[i & 7] += p;
-          x[i] = p;
+          for (int i = 0; i < 32; ++i) {
+            const int64_t cj = t0 + c * 32 + i;
+            const bool off = !row_ok || cj >= c_end || cj > pos;
+            x[i] = off ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = ex2(fmaf(x[i], a.scale_log2, nref));
         }
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          sm[e & 7] += x[2 * e] + x[2 * e + 1];
+          split2<DT>(x[2 * e], x[2 * e + 1], w[e], w[16 + e]);
+        }
+        tmem_st32u(s_addr + c * 32, w);
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-      // the P buffer is free once the previous tile's PV has finished
-      if (j > 0 && okw) okw = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, P.err));
-      if (!okw && lane == 0) abort_flag[(j + 1) & 1] = 1;    // leave after the next exchange
-#pragma unroll
-      for (int c = 0; c < kHalfCols / 8; ++c) {
-        uint4 hi, lo;
-        split2<DT>(x[c * 8 + 0], x[c * 8 + 1], hi.x, lo.x);
-        split2<DT>(x[c * 8 + 2], x[c * 8 + 3], hi.y, lo.y);
-        split2<DT>(x[c * 8 + 4], x[c * 8 + 5], hi.z, lo.z);
-        split2<DT>(x[c * 8 + 6], x[c * 8 + 7], hi.w, lo.w);
-        *(uint4 *)(smem + kOffPh + sw128(r, hf * 8 + c)) = hi;
-        *(uint4 *)(smem + kOffPl + sw128(r, hf * 8 + c)) = lo;
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[q]);
       o_valid = true;
     }
     // ---- epilogue: wait for the last PV, then write state or output
-    bool okw = !(abort_flag[0] | abort_flag[1]);
-    if (okw && n_tiles > 0) okw = __all_sync(0xffffffffu, mbar_wait(o_done, (n_tiles - 1) & 1, P.err));
+    if (ok && n_tiles > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[q], (n_tiles - 1) & 1, P.err));
     tc_fence_after();
-    // the row's total l = sum of both halves' sums (the exchange buffer is
-    // reused once every thread has finished reading its last row maximum)
-    asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
-    xmax[hf * BM + r] = l;
-    asm volatile("bar.sync 1, %0;" ::"r"(kSoftmaxThreads) : "memory");
-    const float l_row = xmax[r] + xmax[BM + r];
-    if (okw) {
-      const float inv = a.finalize ? 1.f / fmaxf(l_row, 1e-30f) : 1.f;
+    if (ok) {
+      const float inv = a.finalize ? 1.f / fmaxf(l, 1e-30f) : 1.f;
 #pragma unroll
-      for (int q = 0; q < kHalfCols / 32; ++q) {
+      for (int c = 0; c < 4; ++c) {
         float v[32];
         if (o_valid) {                                       // warp-uniform
-          tmem_ld32(o_addr + q * 32, v);
+          tmem_ld32(o_addr + c * 32, v);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -560,13 +570,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
-            *(float4 *)(a.acc + row_idx * HD + hf * kHalfCols + q * 32 + i) =
+            *(float4 *)(a.acc + row_idx * HD + c * 32 + i) =
                 make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
         }
       }
-      if (!a.finalize && row_ok && hf == 0) {
+      if (!a.finalize && row_ok) {
         a.ml[row_idx * 2] = m_used;
-        a.ml[row_idx * 2 + 1] = l_row;
+        a.ml[row_idx * 2 + 1] = l;
       }
     }
   }
@@ -617,7 +627,7 @@ int make_map(CUtensorMap *m, const void *base, int64_t rows, int64_t cols, int64
 
 template <int DT, int G>
 cudaError_t launch_g(const CUtensorMap &mk, const CUtensorMap &mv, const TcParams &p, cudaStream_t st) {
-  constexpr int PB = BM / G;
+  constexpr int PB = NQ * BM / G;                    // query positions per CTA
   auto k = prefill_tc_kernel<DT, G>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
