@@ -44,6 +44,23 @@ __device__ __forceinline__ float h2f(uint16_t b, int dt) {
   return __half2float(__ushort_as_half(b));
 }
 
+// Four int8 values packed in a word -> four exact floats without the
+// conversion pipe: x ^ 0x80 is x + 128 as an unsigned byte; placed in the low
+// mantissa byte of 2^23 it reads as 2^23 + x + 128, and subtracting
+// 2^23 + 128 leaves x (all steps exact in fp32).
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
+  const uint32_t u = w ^ 0x80808080u;
+  f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.f;
+  f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.f;
+  f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.f;
+  f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.f;
+}
+
+// Four int8 values at a 2-byte aligned shared-memory address.
+__device__ __forceinline__ uint32_t ld_i8x4(const uint8_t *p) {
+  return __byte_perm(*(const uint16_t *)p, *(const uint16_t *)(p + 2), 0x5410);
+}
+
 // Read this lane's DPL dims of kv head g from a cell row held in shared memory.
 template <int KVT, int D>
 __device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, float *x) {
@@ -53,13 +70,12 @@ __device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, f
     constexpr int LPB = 32 / DPL;                    // lanes per block
     const uint8_t *blk = row + (g * NB + lane / LPB) * 34;
     const float d = __half2float(__ushort_as_half(*(const uint16_t *)blk));
-    const int8_t *qs = (const int8_t *)(blk + 2) + (lane % LPB) * DPL;
+    const uint8_t *qs = blk + 2 + (lane % LPB) * DPL;  // 2-byte aligned
+    float f[4];
+    if constexpr (DPL == 4) i8x4_to_f32(ld_i8x4(qs), f);
+    else i8x4_to_f32(*(const uint16_t *)qs, f);
 #pragma unroll
-    for (int i = 0; i < DPL; i += 2) {
-      const uint16_t two = *(const uint16_t *)(qs + i);   // 2-byte aligned
-      x[i] = d * (float)(int8_t)(two & 0xff);
-      x[i + 1] = d * (float)(int8_t)(two >> 8);
-    }
+    for (int i = 0; i < DPL; ++i) x[i] = d * f[i];
   } else {
     const uint16_t *h = (const uint16_t *)(row + g * D * 2) + lane * DPL;
     if constexpr (DPL == 4) {
@@ -174,10 +190,9 @@ __device__ __forceinline__ void cell_scores(const uint8_t *row, int g, const flo
       for (int h = 0; h < G; ++h) sb[h] = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        const uint16_t w0 = *(const uint16_t *)(blk + 2 + i);
-        const uint16_t w1 = *(const uint16_t *)(blk + 4 + i);
-        const float k0 = (float)(int8_t)(w0 & 0xff), k1 = (float)(int8_t)(w0 >> 8);
-        const float k2 = (float)(int8_t)(w1 & 0xff), k3 = (float)(int8_t)(w1 >> 8);
+        float kf[4];
+        i8x4_to_f32(ld_i8x4(blk + 2 + i), kf);
+        const float k0 = kf[0], k1 = kf[1], k2 = kf[2], k3 = kf[3];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           const float4 q = *(const float4 *)(qs + h * D + bk * 32 + i);
