@@ -68,6 +68,12 @@ def lib():
         L.orc_fold.argtypes = [vp, vp, vp, dbl, dbl, vp, i64]
         L.orc_attn_decode.argtypes = [ctypes.POINTER(Cache), vp, ctypes.c_int, i64, i64, vp, dbl, vp]
         L.orc_attn_prefill.argtypes = [ctypes.POINTER(Cache), vp, ctypes.c_int, i64, i64, i64, i64, dbl, vp]
+        L.orc_float_to_half_bits.argtypes = [ctypes.c_float]
+        L.orc_float_to_half_bits.restype = ctypes.c_uint16
+        L.orc_quantize_q8_0_block.argtypes = [vp, vp]
+        L.orc_append_kv.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i64, vp, vp, vp, vp,
+                                    ctypes.c_int, i64]
+        L.orc_append_kv.restype = ctypes.c_int
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -142,6 +148,29 @@ def make_cache(k_head, v_head, k_tail, v_tail, head_seq_stride_rows, tail_seq_st
         return None if a is None else _ptr(a)
     return Cache(p(k_head), p(v_head), p(k_tail), p(v_tail), head_seq_stride_rows,
                  tail_seq_stride_rows, n_vram, dtype, n_kv_heads, head_dim)
+
+
+def float_to_half_bits(x: float) -> int:
+    return lib().orc_float_to_half_bits(x)
+
+
+def quantize_q8_0_block(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float32)
+    assert x.size == 32
+    out = np.empty(34, np.uint8)
+    lib().orc_quantize_q8_0_block(_ptr(x), _ptr(out))
+    return out
+
+
+def append_kv(k_new, v_new, src_dtype, n_new, pos0, n_kv_heads, head_dim, k_head, v_head,
+              k_tail, v_tail, dtype, n_vram) -> None:
+    """Writes through the given numpy buffers (None where a tier is absent)."""
+    def p(a):
+        return None if a is None else _ptr(a)
+    rc = lib().orc_append_kv(_ptr(k_new), _ptr(v_new), src_dtype, n_new, pos0, n_kv_heads,
+                             head_dim, p(k_head), p(v_head), p(k_tail), p(v_tail), dtype, n_vram)
+    if rc != 0:
+        raise ValueError("orc_append_kv: unsupported dtype pair")
 
 
 def attn_partial(cache: Cache, b, kv_head, q: np.ndarray, scale, c0, c1):

@@ -238,6 +238,101 @@ void orc_attn_prefill(const orc_cache *c, const uint16_t *q, int q_dtype,
   }
 }
 
+uint16_t orc_float_to_half_bits(float x) {
+  /* decompose |x| = m * 2^e exactly in binary64, then round m to the
+   * binary16 grid at that exponent */
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double a = fabs((double)x);
+  int e;
+  double m, q, r;
+  long long n;
+  if (isnan(x)) return (uint16_t)(sign | 0x7e00u);
+  if (isinf(x)) return (uint16_t)(sign | 0x7c00u);
+  if (a == 0.0) return sign;
+  frexp(a, &e);                      /* a = f * 2^e, f in [0.5, 1) */
+  /* binary16 spacing: 2^(e-11) for normals (e >= -13), 2^-24 below */
+  {
+    int ulp_exp = e - 11;
+    if (ulp_exp < -24) ulp_exp = -24;
+    m = ldexp(a, -ulp_exp);          /* a in units of the spacing */
+    q = floor(m);
+    r = m - q;
+    n = (long long)q;
+    if (r > 0.5 || (r == 0.5 && (n & 1))) n += 1;
+    a = ldexp((double)n, ulp_exp);   /* rounded magnitude */
+  }
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7c00u);  /* overflow */
+  if (a < ldexp(1.0, -14)) {         /* subnormal (or rounded up to min normal) */
+    n = (long long)ldexp(a, 24);
+    return (uint16_t)(sign | (uint16_t)n);
+  }
+  frexp(a, &e);
+  {
+    int be = e - 1 + 15;             /* biased exponent */
+    long long frac = (long long)ldexp(a, 11 - e) - 1024;  /* 10 fraction bits */
+    return (uint16_t)(sign | (uint16_t)(be << 10) | (uint16_t)frac);
+  }
+}
+
+void orc_quantize_q8_0_block(const float *x, uint8_t *blk) {
+  float amax = 0.0f, d, id;
+  uint16_t dh;
+  int i;
+  for (i = 0; i < 32; ++i) {
+    float ax = fabsf(x[i]);
+    if (ax > amax) amax = ax;
+  }
+  d = amax / 127.0f;
+  id = d != 0.0f ? 1.0f / d : 0.0f;
+  dh = orc_float_to_half_bits(d);
+  blk[0] = (uint8_t)(dh & 0xff);
+  blk[1] = (uint8_t)(dh >> 8);
+  for (i = 0; i < 32; ++i) {
+    float v = x[i] * id;
+    blk[2 + i] = (uint8_t)(int8_t)roundf(v);
+  }
+}
+
+int orc_append_kv(const uint8_t *k_new, const uint8_t *v_new, int src_dtype,
+                  int64_t n_new, int64_t pos0, int64_t n_kv_heads,
+                  int64_t head_dim, uint8_t *k_head, uint8_t *v_head,
+                  uint8_t *k_tail, uint8_t *v_tail, int dtype,
+                  int64_t n_vram) {
+  int64_t t, h, b, d;
+  int64_t src_row = n_kv_heads * head_dim * 2;
+  int64_t rb = orc_row_bytes(dtype, n_kv_heads, head_dim);
+  if (src_dtype != ORC_F16 && src_dtype != ORC_BF16) return -1;
+  if (dtype != ORC_Q8_0 && dtype != src_dtype) return -1;
+  if (rb == 0) return -1;
+  for (t = 0; t < n_new; ++t) {
+    int64_t j = pos0 + t;
+    int which;
+    for (which = 0; which < 2; ++which) {
+      const uint8_t *src = (which ? v_new : k_new) + t * src_row;
+      uint8_t *dst = j < n_vram ? (which ? v_head : k_head) + j * rb
+                                : (which ? v_tail : k_tail) + (j - n_vram) * rb;
+      if (dtype != ORC_Q8_0) {
+        memcpy(dst, src, (size_t)rb);
+        continue;
+      }
+      for (h = 0; h < n_kv_heads; ++h) {
+        for (b = 0; b < head_dim / 32; ++b) {
+          float x[32];
+          for (d = 0; d < 32; ++d) {
+            const uint8_t *e = src + (h * head_dim + b * 32 + d) * 2;
+            uint16_t bits = (uint16_t)(e[0] | (e[1] << 8));
+            /* exact: every fp16 / bf16 value is a binary32 value */
+            x[d] = (float)(src_dtype == ORC_F16 ? orc_half_to_double(bits)
+                                                : orc_bf16_to_double(bits));
+          }
+          orc_quantize_q8_0_block(x, dst + (h * (head_dim / 32) + b) * 34);
+        }
+      }
+    }
+  }
+  return 0;
+}
+
 int orc_set_threads(int n) {
 #ifdef _OPENMP
   if (n > 0) omp_set_num_threads(n);

@@ -127,6 +127,31 @@ void orc_attn_prefill(const orc_cache *c, const uint16_t *q, int q_dtype,
                       int64_t rows, int64_t q_pos0, int64_t n_q_heads,
                       int64_t ctx_len, double scale, double *out);
 
+/* IEEE binary32 -> binary16 bits, round to nearest, ties to even (with
+ * subnormals, overflow to infinity, NaN kept quiet). */
+uint16_t orc_float_to_half_bits(float x);
+
+/* q8_0 quantisation of one 32-value block (the usual q8_0 rule; the pages
+ * name the format but not the rounding, so this is a stated reading),
+ * evaluated in binary32): amax = max|x|, d = amax / 127, id = d ? 1/d : 0,
+ * qs[i] = round-half-away-from-zero(x[i] * id); the block stores d as fp16.
+ * Writes 34 bytes {fp16 d; int8 qs[32]}. */
+void orc_quantize_q8_0_block(const float *x, uint8_t *blk);
+
+/* Append (write path of the tiered cache): tokens t < n_new of k_new / v_new
+ * ([n_new][n_kv_heads][head_dim], src dtype fp16 or bf16) become cells
+ * pos0 + t of one sequence: cell j < n_vram goes to head row j, cell
+ * j >= n_vram to tail row j - n_vram, stored in the cache dtype (a copy for
+ * fp16/bf16 equal to the source dtype; q8_0 quantised per 32-value block of
+ * each head).  The cache pointers are those of an orc_cache (k_head ...
+ * v_tail), written through.  Returns 0, or -1 on a dtype pair the cache
+ * cannot hold. */
+int orc_append_kv(const uint8_t *k_new, const uint8_t *v_new, int src_dtype,
+                  int64_t n_new, int64_t pos0, int64_t n_kv_heads,
+                  int64_t head_dim, uint8_t *k_head, uint8_t *v_head,
+                  uint8_t *k_tail, uint8_t *v_tail, int dtype,
+                  int64_t n_vram);
+
 /* Worker threads used by orc_attn_decode / orc_attn_prefill (independent
  * (row, head) outputs are distributed; each is computed exactly as in the
  * serial loop).  Returns the count in effect; 1 without OpenMP. */

@@ -366,3 +366,77 @@ def test_prefill_matches_scipy_with_mask():
             s[~mask] = -np.inf
             np.testing.assert_allclose(out[i, h], scipy.special.softmax(s) @ V[:, h // 2, :],
                                        rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- q8_0 write path
+
+def test_half_rounding_matches_numpy_on_many_values():
+    g = synth.rng(31)
+    x = np.concatenate([g.standard_normal(20000).astype(np.float32) * s
+                        for s in (1e-6, 1e-3, 1.0, 100.0, 30000.0)])
+    x = np.concatenate([x, np.float32([65504.0, 65519.0, 65520.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26])])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.float_to_half_bits(float(v)) for v in x], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_q8_0_quantise_hand_block():
+    # amax 127 gives d = 1 exactly: the codes are the values themselves
+    x = np.arange(-16, 16, dtype=np.float32) * 4.0
+    x[0] = -127.0
+    blk = oracle.quantize_q8_0_block(x)
+    assert blk[0:2].view(np.uint16)[0] == 0x3C00                        # fp16 1.0
+    assert np.array_equal(blk[2:].view(np.int8), x.astype(np.int8))
+    zero = oracle.quantize_q8_0_block(np.zeros(32, np.float32))
+    assert (zero == 0).all()
+    # ties round away from zero: x = 0.5 * d
+    x = np.zeros(32, np.float32)
+    x[0], x[1], x[2] = 127.0, 0.5, -0.5
+    q = oracle.quantize_q8_0_block(x)[2:].view(np.int8)
+    assert q[1] == 1 and q[2] == -1
+
+
+def test_q8_0_quantise_error_bound_and_scale():
+    g = synth.rng(32)
+    for _ in range(200):
+        x = (g.standard_normal(32) * g.uniform(1e-3, 50)).astype(np.float32)
+        blk = oracle.quantize_q8_0_block(x)
+        d16 = float(blk[0:2].view(np.float16)[0])
+        q = blk[2:].view(np.int8).astype(np.float64)
+        amax = float(np.abs(x).max())
+        assert np.abs(q).max() == 127                                    # the max hits the end code
+        assert abs(d16 - amax / 127) <= 2 ** -11 * amax / 127            # fp16 rounding of d
+        d32 = np.float32(amax) / np.float32(127)
+        assert np.all(np.abs(x - d32 * q) <= 0.5 * d32 * (1 + 1e-6))     # half a step
+
+
+def test_append_places_cells_in_their_tiers():
+    g = synth.rng(33)
+    H, D, N, cap, n_new, pos0 = 2, 64, 10, 30, 8, 6
+    for dt in (oracle.F16, oracle.BF16, oracle.Q8_0):
+        src_dt = oracle.BF16 if dt == oracle.Q8_0 else dt
+        name = "bf16" if src_dt == oracle.BF16 else "f16"
+        kn = synth.normal_bits((n_new, H * D), name, g).view(np.uint8).reshape(n_new, -1).copy()
+        vn = synth.normal_bits((n_new, H * D), name, g).view(np.uint8).reshape(n_new, -1).copy()
+        rb = oracle.row_bytes(dt, H, D)
+        kh = np.zeros((N, rb), np.uint8); vh = np.zeros((N, rb), np.uint8)
+        kt = np.zeros((cap - N, rb), np.uint8); vt = np.zeros((cap - N, rb), np.uint8)
+        oracle.append_kv(kn, vn, src_dt, n_new, pos0, H, D, kh, vh, kt, vt, dt, N)
+        # untouched rows stay zero; written rows decode back to the inputs
+        assert (kh[:pos0] == 0).all() and (kt[pos0 + n_new - N:] == 0).all()
+        for t in range(n_new):
+            j = pos0 + t
+            row = kh[j] if j < N else kt[j - N]
+            for h in range(H):
+                got = oracle.load_head(row, dt, D, h)
+                src = (kn[t].view(np.uint16)[h * D:(h + 1) * D])
+                x = (src.view(np.float16).astype(np.float64) if src_dt == oracle.F16 else
+                     torch.from_numpy(src.view(np.int16).copy()).view(torch.bfloat16).double().numpy())
+                if dt == oracle.Q8_0:
+                    # half a quantisation step, plus the fp16 rounding of d times |q| <= 127
+                    step = np.abs(x).reshape(-1, 32).max(axis=1) / 127
+                    bound = (0.5 + 127 * 2.0 ** -11) * step[:, None] + 1e-12
+                    assert np.all(np.abs(got - x).reshape(-1, 32) <= bound)
+                else:
+                    assert np.array_equal(got, x)
