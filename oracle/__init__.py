@@ -74,6 +74,9 @@ def lib():
         L.orc_append_kv.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, i64, vp, vp, vp, vp,
                                     ctypes.c_int, i64]
         L.orc_append_kv.restype = ctypes.c_int
+        L.orc_copy_plan.argtypes = [vp] * 6 + [i64, ctypes.c_int, vp, vp, vp, i64]
+        L.orc_copy_plan.restype = i64
+        L.orc_fragment_ptrs.argtypes = [vp, vp, i64, vp, vp, vp, i64, vp, vp, vp]
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -148,6 +151,33 @@ def make_cache(k_head, v_head, k_tail, v_tail, head_seq_stride_rows, tail_seq_st
         return None if a is None else _ptr(a)
     return Cache(p(k_head), p(v_head), p(k_tail), p(v_tail), head_seq_stride_rows,
                  tail_seq_stride_rows, n_vram, dtype, n_kv_heads, head_dim)
+
+
+def copy_plan(runs, gpu_to_cpu: bool):
+    """runs: list of (local_offset, local_stride, canonical_offset,
+    canonical_stride, num_fragments, fragment_size)."""
+    cols = [np.ascontiguousarray([r[k] for r in runs], np.int64) for k in range(6)]
+    cap = int(sum(r[4] for r in runs)) + 1
+    fs, fd, fz = (np.zeros(cap, np.int64) for _ in range(3))
+    n = lib().orc_copy_plan(*[_ptr(c) for c in cols], len(runs), int(gpu_to_cpu), _ptr(fs), _ptr(fd),
+                            _ptr(fz), cap)
+    if n < 0:
+        raise ValueError("orc_copy_plan: capacity")
+    return fs[:n].copy(), fd[:n].copy(), fz[:n].copy()
+
+
+def fragment_ptrs(src_bases, dst_bases, frag_src, frag_dst, frag_sizes):
+    sb = np.ascontiguousarray(src_bases, np.uint64)
+    db = np.ascontiguousarray(dst_bases, np.uint64)
+    fs = np.ascontiguousarray(frag_src, np.int64)
+    fd = np.ascontiguousarray(frag_dst, np.int64)
+    fz = np.ascontiguousarray(frag_sizes, np.int64)
+    nb, nf = sb.size, fs.size
+    os_, od, oz = np.zeros(nb * nf, np.uint64), np.zeros(nb * nf, np.uint64), np.zeros(nb * nf, np.int64)
+    if nb * nf:
+        lib().orc_fragment_ptrs(_ptr(sb), _ptr(db), nb, _ptr(fs), _ptr(fd), _ptr(fz), nf, _ptr(os_),
+                                _ptr(od), _ptr(oz))
+    return os_, od, oz
 
 
 def float_to_half_bits(x: float) -> int:

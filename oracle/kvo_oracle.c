@@ -135,6 +135,41 @@ int orc_gather_blocks(const uint8_t *plane, int64_t n_seq,
   return 0;
 }
 
+int64_t orc_copy_plan(const int64_t *local_offset, const int64_t *local_stride,
+                      const int64_t *canonical_offset,
+                      const int64_t *canonical_stride,
+                      const int64_t *num_fragments,
+                      const int64_t *fragment_size, int64_t n_runs,
+                      int gpu_to_cpu, int64_t *frag_src, int64_t *frag_dst,
+                      int64_t *frag_sizes, int64_t cap) {
+  int64_t r, i, n = 0;
+  for (r = 0; r < n_runs; ++r)
+    for (i = 0; i < num_fragments[r]; ++i) {
+      int64_t local = local_offset[r] + i * local_stride[r];
+      int64_t canonical = canonical_offset[r] + i * canonical_stride[r];
+      if (n >= cap) return -1;
+      frag_src[n] = gpu_to_cpu ? local : canonical;
+      frag_dst[n] = gpu_to_cpu ? canonical : local;
+      frag_sizes[n] = fragment_size[r];
+      ++n;
+    }
+  return n;
+}
+
+void orc_fragment_ptrs(const uint64_t *src_bases, const uint64_t *dst_bases,
+                       int64_t n_blocks, const int64_t *frag_src,
+                       const int64_t *frag_dst, const int64_t *frag_sizes,
+                       int64_t n_frags, uint64_t *out_src, uint64_t *out_dst,
+                       int64_t *out_sizes) {
+  int64_t b, f;
+  for (b = 0; b < n_blocks; ++b)
+    for (f = 0; f < n_frags; ++f) {
+      out_src[b * n_frags + f] = src_bases[b] + (uint64_t)frag_src[f];
+      out_dst[b * n_frags + f] = dst_bases[b] + (uint64_t)frag_dst[f];
+      out_sizes[b * n_frags + f] = frag_sizes[f];
+    }
+}
+
 static const uint8_t *cell_row(const orc_cache *c, const uint8_t *head,
                                const uint8_t *tail, int64_t b, int64_t j) {
   int64_t rb = orc_row_bytes(c->dtype, c->n_kv_heads, c->head_dim);

@@ -83,6 +83,30 @@ int orc_gather_blocks(const uint8_t *plane, int64_t n_seq,
                       int64_t block_tokens, const int32_t *sel,
                       int64_t n_sel, uint8_t *out);
 
+/* vLLM gpu_worker.py, _build_copy_plan: run r of a ref's mapping has
+ * num_fragments[r] fragments of fragment_size[r] bytes; fragment i sits at
+ * local_offset[r] + i*local_stride[r] in the worker's block and at
+ * canonical_offset[r] + i*canonical_stride[r] in the canonical block.
+ * Fragments are listed run by run; source/destination offsets are (local,
+ * canonical) for a GPU->CPU transfer and (canonical, local) otherwise.
+ * Returns the fragment count, or -1 if it exceeds cap. */
+int64_t orc_copy_plan(const int64_t *local_offset, const int64_t *local_stride,
+                      const int64_t *canonical_offset,
+                      const int64_t *canonical_stride,
+                      const int64_t *num_fragments,
+                      const int64_t *fragment_size, int64_t n_runs,
+                      int gpu_to_cpu, int64_t *frag_src, int64_t *frag_dst,
+                      int64_t *frag_sizes, int64_t cap);
+
+/* vLLM gpu_worker.py, _fill_canonical_ops (step 3): one descriptor per
+ * (block, fragment), block-major: out[b*n_frags + f] = base[b] + offset[f],
+ * sizes[b*n_frags + f] = frag_sizes[f]. */
+void orc_fragment_ptrs(const uint64_t *src_bases, const uint64_t *dst_bases,
+                       int64_t n_blocks, const int64_t *frag_src,
+                       const int64_t *frag_dst, const int64_t *frag_sizes,
+                       int64_t n_frags, uint64_t *out_src, uint64_t *out_dst,
+                       int64_t *out_sizes);
+
 /* Tiered cache addressing (llama.cpp PR "tiered KV cache (--kv-vram-cells)"):
  * cell j of sequence b lives at
  *   head + (b*head_seq_stride_rows + j) * row_bytes          if j <  n_vram

@@ -440,3 +440,36 @@ def test_append_places_cells_in_their_tiers():
                     assert np.all(np.abs(got - x).reshape(-1, 32) <= bound)
                 else:
                     assert np.array_equal(got, x)
+
+
+# ---------------------------------------------------------------- canonical fragments
+
+def _brute_plan(runs, gpu_to_cpu):
+    out = []
+    for lo, ls, co, cs, nf, fz in runs:
+        for i in range(nf):
+            local, canon = lo + i * ls, co + i * cs
+            out.append((local, canon, fz) if gpu_to_cpu else (canon, local, fz))
+    return out
+
+
+@pytest.mark.parametrize("gpu_to_cpu", [True, False])
+def test_copy_plan_unrolls_runs_in_order(gpu_to_cpu):
+    # two runs: 4 head slices of 256 B spread by 1 KiB locally and packed canonically,
+    # then one 512 B tail fragment
+    runs = [(0, 1024, 0, 256, 4, 256), (4096, 0, 1024, 0, 1, 512)]
+    fs, fd, fz = oracle.copy_plan(runs, gpu_to_cpu)
+    assert list(zip(fs.tolist(), fd.tolist(), fz.tolist())) == _brute_plan(runs, gpu_to_cpu)
+
+
+def test_fragment_ptrs_broadcast_block_major():
+    g = synth.rng(34)
+    sb = g.integers(0, 1 << 40, size=5).astype(np.uint64)
+    db = g.integers(0, 1 << 40, size=5).astype(np.uint64)
+    fs, fd, fz = np.array([0, 300, 900]), np.array([10, 20, 30]), np.array([300, 600, 100])
+    os_, od, oz = oracle.fragment_ptrs(sb, db, fs, fd, fz)
+    for b in range(5):
+        for f in range(3):
+            i = b * 3 + f
+            assert os_[i] == sb[b] + np.uint64(fs[f]) and od[i] == db[b] + np.uint64(fd[f])
+            assert oz[i] == fz[f]
