@@ -162,6 +162,60 @@ class Clocks:
                 "samples": len(sm)}
 
 
+# ----------------------------------------------------------------- C1 tiny
+
+def c1_setup(seed=SEED0):
+    """Tiny case: 2 layers x K,V paged fp16 (16 tokens x 8 heads x 128 = 32 KiB
+    pages), 64 seeded blocks swapped between 128-block pools; decode for one
+    sequence, 32 q / 8 kv heads, 1024 cells with 512 in VRAM."""
+    t = torch()
+    k = kvo()
+    g = synth.rng(seed, 1)
+    page, nt, pool, nb = 32768, 4, 128, 64
+    d = dev(nt * pool * page)
+    h = pinned(nt * pool * page)
+    synth.fill_bytes_large(h.numpy(), seed, 2)
+    gids = g.permutation(pool)[:nb].astype(np.int64)
+    hids = g.permutation(pool)[:nb].astype(np.int64)
+    gp = np.empty(nt * nb, np.int64)
+    hp = np.empty(nt * nb, np.int64)
+    for i in range(nt):
+        k.kvo_sub_block_ptrs(gids.ctypes.data, nb, 1, 0, d.data_ptr() + i * pool * page, page, page,
+                             gp[i * nb:].ctypes.data, nb)
+        k.kvo_sub_block_ptrs(hids.ctypes.data, nb, 1, 0, h.data_ptr() + i * pool * page, page, page,
+                             hp[i * nb:].ctypes.data, nb)
+    st = {"dev": d, "host": h, "n_desc": nt * nb, "bytes": nt * nb * page,
+          "sizes": pinned_i64(np.full(nt * nb, page, np.int64)),
+          "h2d_src": pinned_i64(hp), "h2d_dst": pinned_i64(gp),
+          "d2h_src": pinned_i64(gp), "d2h_dst": pinned_i64(hp)}
+    L, N, hq, hkv, D = 1024, 512, 32, 8, 128
+    rb = hkv * D * 2
+    kc = synth.normal_bits((L, hkv * D), "f16", g).view(np.uint8).reshape(L, rb)
+    vc = synth.normal_bits((L, hkv * D), "f16", g).view(np.uint8).reshape(L, rb)
+    q = synth.normal_bits((1, hq, D), "f16", g)
+    st.update({"k_head": t.from_numpy(kc[:N].copy().reshape(-1)).cuda(),
+               "v_head": t.from_numpy(vc[:N].copy().reshape(-1)).cuda(),
+               "k_tail": t.from_numpy(kc[N:].copy().reshape(-1)).pin_memory(),
+               "v_tail": t.from_numpy(vc[N:].copy().reshape(-1)).pin_memory(),
+               "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
+               "ctx": t.tensor([L], dtype=t.int32, device="cuda"),
+               "out": t.empty(hq * D, dtype=t.float32, device="cuda"),
+               "stage_k": dev((L - N) * rb), "stage_v": dev((L - N) * rb),
+               "L": L, "N": N, "hq": hq, "hkv": hkv, "rb": rb})
+    st["ws_bytes"] = k.kvo_attn_decode_workspace_bytes(1, hq, D, L)
+    st["ws"] = dev(st["ws_bytes"])
+    return st
+
+
+def c1_decode(st, staging):
+    k = kvo()
+    L, N = st["L"], st["N"]
+    k.kvo_attn_decode_tiered(st["q"], k.F16, 1, st["hq"], st["hkv"], 128, st["k_head"], st["v_head"], N,
+                             st["k_tail"], st["v_tail"], L - N, k.F16, st["ctx"], L, N,
+                             1.0 / math.sqrt(128), st["stage_k"] if staging else None,
+                             st["stage_v"] if staging else None, st["out"], st["ws"], st["ws_bytes"])
+
+
 # ----------------------------------------------------------------- C2 swap
 
 C2_TENSORS, C2_GPU_BLOCKS, C2_HOST_CHUNKS, C2_BLOCKS, C2_BPC, C2_SKIP = 64, 4096, 640, 2048, 4, 1
@@ -372,6 +426,41 @@ def c5_flops():
     return 4.0 * C5_HQ * C5_D * cells
 
 
+# ----------------------------------------------------------------- write path (append)
+
+def c6_setup(seed=SEED0 + 5):
+    """Appends into the host tails of the C3 (q8_0) and C5 (bf16) caches: one
+    decode token (q8_0) and one 2048-token prefill chunk (q8_0 and bf16)."""
+    t = torch()
+    g = synth.rng(seed, 1)
+    n = 2048
+    st = {"n": n}
+    for name, hkv in (("q8", C3_HKV), ("bf", C5_HKV)):
+        x = synth.normal_bits((n, hkv * 128), "bf16" if name == "bf" else "f16", g)
+        st[name + "_k"] = t.from_numpy(x.view(np.int16).reshape(-1).copy()).cuda()
+        st[name + "_v"] = t.from_numpy(x[::-1].copy().view(np.int16).reshape(-1)).cuda()
+    st["q8_rb"] = C3_HKV * 4 * 34
+    st["bf_rb"] = C5_HKV * 128 * 2
+    cap = 8192 + 4096
+    st["cap"] = cap
+    st["q8_tail_k"] = pinned((cap - 8192) * st["q8_rb"])
+    st["q8_tail_v"] = pinned((cap - 8192) * st["q8_rb"])
+    st["bf_tail_k"] = pinned((cap - 8192) * st["bf_rb"])
+    st["bf_tail_v"] = pinned((cap - 8192) * st["bf_rb"])
+    st["q8_head"] = dev(8192 * st["q8_rb"])
+    st["bf_head"] = dev(8192 * st["bf_rb"])
+    return st
+
+
+def c6_run(st, which, n_tokens):
+    k = kvo()
+    q8 = which == "q8"
+    k.kvo_append_kv_tiered(st[which + "_k"], st[which + "_v"], k.F16 if q8 else k.BF16, n_tokens,
+                           8192 + 1000, C3_HKV if q8 else C5_HKV, 128, st[which + "_head"],
+                           st[which + "_head"], st[which + "_tail_k"], st[which + "_tail_v"],
+                           k.Q8_0 if q8 else k.BF16, 8192, st["cap"])
+
+
 # ----------------------------------------------------------------- CPU oracle arm
 
 def oracle_c3_step(L, heads=C3_HQ):
@@ -459,7 +548,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of head (headline decode only), c2, c3, c4, c5 (default all)")
+                    help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append) "
+                         "(default all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -479,7 +569,7 @@ def main(argv=None):
     build.build()
     k = kvo()
     k.load()
-    rows = set(args.rows.split(",")) if args.rows != "all" else {"head", "c2", "c3", "c4", "c5"}
+    rows = set(args.rows.split(",")) if args.rows != "all" else {"head", "c1", "c2", "c3", "c4", "c5", "c6"}
     timer = Timer()
     peaks = measure_link_peak(timer)
     hbm = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6789.0) \
@@ -543,6 +633,19 @@ def main(argv=None):
                     "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
                     "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
         del st3
+    # ---- C1 tiny (latency-bound: microseconds, fractions not meaningful)
+    if "c1" in rows:
+        st1 = c1_setup()
+        for h2d in (True, False):
+            tot, _ = timer.run(lambda: c2_run(st1, h2d), K, W)
+            us_r = max_over_ranks(tot, world) / K * 1e3
+            results[f"c1_swap_64blocks_{'h2d' if h2d else 'd2h'}"] = {
+                "us_per_step": us_r, "host_gbs": st1["bytes"] / (us_r * 1e-6) / 1e9}
+        for staging in (False, True):
+            tot, _ = timer.run(lambda: c1_decode(st1, staging), K, W)
+            us_r = max_over_ranks(tot, world) / K * 1e3
+            results[f"c1_f16_decode_L1024_N512_{'staged' if staging else 'direct'}"] = {"us_per_step": us_r}
+        del st1
     # ---- C2 swap
     if "c2" in rows:
         for page in (32768, 2048):
@@ -570,6 +673,18 @@ def main(argv=None):
         gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
         results["c4_sparse_decode"] = {"us_per_step": us_r, "hbm_gbs": gbs, "roofline_frac": gbs / hbm}
         del st4
+    # ---- write path: appends into the host tail
+    if "c6" in rows:
+        st6 = c6_setup()
+        for which, n_tok in (("q8", 1), ("q8", 2048), ("bf", 2048)):
+            tot, _ = timer.run(lambda: c6_run(st6, which, n_tok), K, W)
+            us_r = max_over_ranks(tot, world) / K * 1e3
+            host_b = 2 * n_tok * st6[which + "_rb"]
+            gbs = host_b / (us_r * 1e-6) / 1e9
+            results[f"append_{'q8_0' if which == 'q8' else 'bf16'}_{n_tok}tok_host"] = {
+                "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["d2h"],
+                "host_bytes": host_b}
+        del st6
     # ---- C5 prefill
     if "c5" in rows:
         st5 = c5_setup()
@@ -609,7 +724,10 @@ def main(argv=None):
                        "staging": False, "l2": "flushed between timed steps (256 MiB write)"},
             "host_gbs": achieved, "link_peak_gbs": peaks,
             "roofline": {"bound": "host_link", "achieved": achieved, "peak": peaks["h2d"], "unit": "GB/s",
-                         "frac": achieved / peaks["h2d"], "traffic": None,
+                         "frac": achieved / peaks["h2d"], "traffic": profiled_traffic(),
+                         "traffic_note": "dram__bytes_read+write of decode_split_kernel per launch (ncu, "
+                                         "profiles/decode_split_kernel_c3_headline.md); host-link bytes "
+                                         "are not DRAM traffic",
                          "peak_source": "pinned cudaMemcpyAsync H2D 1 GiB, best of 5, measured in this run",
                          "kernel": "decode_split_kernel + decode_combine_kernel (one C-ABI call)"},
             "e2e": {"value": head["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": head["e2e_h2d"],
@@ -624,6 +742,19 @@ def main(argv=None):
     return 0
 
 
+def profiled_traffic():
+    """DRAM bytes per launch of the headline decode kernel, as recorded by the
+    committed ncu summary (None if the summary is missing)."""
+    path = os.path.join(ROOT, "profiles", "decode_split_kernel_c3_headline.md")
+    try:
+        for line in open(path):
+            if line.startswith("traffic_bytes_per_launch:"):
+                return int(line.split(":")[1])
+    except OSError:
+        pass
+    return None
+
+
 def gpu_launch_count(K, rows):
     """Kernels of libkvo launched in the timed regions (own kernels only)."""
     n = 0
@@ -631,10 +762,14 @@ def gpu_launch_count(K, rows):
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
     if "c3" in rows:
         n += 2 * K * (3 * 2 * 2 - 1 + 3)           # 11 tiered variants + 3 all-VRAM, 2 kernels each
+    if "c1" in rows:
+        n += K * 2 + K * 2 * 2                     # swap both ways; decode direct + staged (2 kernels)
     if "c2" in rows:
         n += K * 4                                 # 2 pages x 2 directions, one swap kernel each
     if "c4" in rows:
         n += K + 2 * K                             # gather; decode split + combine
+    if "c6" in rows:
+        n += 3 * K                                 # three appends, one kernel each
     if "c5" in rows:
         # staged: VRAM head (2 row blocks) + 48 arena buckets of 4096 cells x 2 row blocks;
         # direct: head + host tail, 2 row blocks each

@@ -161,6 +161,65 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids, int64_t blocks_p
   return KVO_OK;
 }
 
+// ---------------------------------------------------------------- canonical fragments
+int kvo_copy_plan(const int64_t *local_offset, const int64_t *local_stride,
+                  const int64_t *canonical_offset, const int64_t *canonical_stride,
+                  const int64_t *num_fragments, const int64_t *fragment_size, int64_t n_runs,
+                  int gpu_to_cpu, int64_t *frag_src, int64_t *frag_dst, int64_t *frag_sizes,
+                  int64_t capacity, int64_t *n_frags) {
+  clear_error();
+  const char *fn = "kvo_copy_plan";
+  if (!n_frags) return fail(KVO_ERR_ARG, "%s: n_frags is NULL", fn);
+  *n_frags = 0;
+  if (n_runs < 0 || capacity < 0) return fail(KVO_ERR_ARG, "%s: negative size", fn);
+  if (n_runs == 0) return KVO_OK;
+  if (!local_offset || !local_stride || !canonical_offset || !canonical_stride || !num_fragments ||
+      !fragment_size)
+    return fail(KVO_ERR_ARG, "%s: NULL run array", fn);
+  int64_t total = 0;
+  for (int64_t r = 0; r < n_runs; ++r) {
+    if (num_fragments[r] < 0 || fragment_size[r] < 0) return fail(KVO_ERR_ARG, "%s: negative run field", fn);
+    total += num_fragments[r];
+  }
+  if (total > capacity) return fail(KVO_ERR_ARG, "%s: %lld fragments exceed capacity %lld", fn,
+                                    (long long)total, (long long)capacity);
+  if (total > 0 && (!frag_src || !frag_dst || !frag_sizes)) return fail(KVO_ERR_ARG, "%s: NULL output", fn);
+  int64_t n = 0;
+  for (int64_t r = 0; r < n_runs; ++r) {
+    int64_t local = local_offset[r], canon = canonical_offset[r];
+    for (int64_t i = 0; i < num_fragments[r]; ++i, ++n) {
+      frag_src[n] = gpu_to_cpu ? local : canon;
+      frag_dst[n] = gpu_to_cpu ? canon : local;
+      frag_sizes[n] = fragment_size[r];
+      local += local_stride[r];
+      canon += canonical_stride[r];
+    }
+  }
+  *n_frags = n;
+  return KVO_OK;
+}
+
+int kvo_fragment_ptrs(const int64_t *src_bases, const int64_t *dst_bases, int64_t n_blocks,
+                      const int64_t *frag_src, const int64_t *frag_dst, const int64_t *frag_sizes,
+                      int64_t n_frags, int64_t *out_src, int64_t *out_dst, int64_t *out_sizes) {
+  clear_error();
+  const char *fn = "kvo_fragment_ptrs";
+  if (n_blocks < 0 || n_frags < 0) return fail(KVO_ERR_ARG, "%s: negative size", fn);
+  if (n_blocks == 0 || n_frags == 0) return KVO_OK;
+  if (!src_bases || !dst_bases || !frag_src || !frag_dst || !frag_sizes || !out_src || !out_dst || !out_sizes)
+    return fail(KVO_ERR_ARG, "%s: NULL array", fn);
+  for (int64_t b = 0; b < n_blocks; ++b) {
+    const uint64_t sb = (uint64_t)src_bases[b], db = (uint64_t)dst_bases[b];
+    int64_t *os = out_src + b * n_frags, *od = out_dst + b * n_frags, *oz = out_sizes + b * n_frags;
+    for (int64_t f = 0; f < n_frags; ++f) {
+      os[f] = (int64_t)(sb + (uint64_t)frag_src[f]);
+      od[f] = (int64_t)(db + (uint64_t)frag_dst[f]);
+      oz[f] = frag_sizes[f];
+    }
+  }
+  return KVO_OK;
+}
+
 // ---------------------------------------------------------------- a2
 int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst, const int64_t *sizes,
                           int64_t n, uint32_t flags, void *stream) {
@@ -179,14 +238,15 @@ int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst, const int64_t 
   } else if (flags & KVO_SWAP_FORCE_SM) {
     use_ce = false;
   } else {
-    // Measured crossover: the copy engine only pays off when each call moves
-    // enough bytes to hide its ~2.7 us issue cost.  The mean needs the sizes
-    // on the host, which pinned descriptor arrays allow.
+    // Measured crossover: SM copies reach the link peak from 2 KiB pages up,
+    // and a copy-engine call costs ~2.7 us to issue, so the copy engine only
+    // pays off (by leaving the SMs free) for a few large copies.  The rule
+    // reads at most KVO_SWAP_CE_MAX_DESCRIPTORS sizes, keeping the decision
+    // cheap on the host.
     use_ce = false;
-    if (kz == kMappedHost) {
-      long double total = 0;
-      for (int64_t i = 0; i < n; ++i) total += (long double)sizes[i];
-      use_ce = total / (long double)n >= (long double)KVO_SWAP_CE_MIN_MEAN_BYTES;
+    if (kz == kMappedHost && n <= KVO_SWAP_CE_MAX_DESCRIPTORS) {
+      use_ce = true;
+      for (int64_t i = 0; i < n && use_ce; ++i) use_ce = sizes[i] >= KVO_SWAP_CE_MIN_BYTES;
     }
   }
   if (use_ce) {
@@ -350,6 +410,62 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
     a.hi_device = 1;
   }
   return launch_decode(a, st);
+}
+
+// ---------------------------------------------------------------- write path
+int kvo_append_kv_tiered(const void *k_new, const void *v_new, int src_dtype, int64_t n_new,
+                         int64_t pos0, int64_t n_kv_heads, int64_t head_dim, void *k_vram,
+                         void *v_vram, void *k_host, void *v_host, int kv_dtype,
+                         int64_t n_vram_cells, int64_t capacity_cells, void *stream) {
+  clear_error();
+  const char *fn = "kvo_append_kv_tiered";
+  if (n_new < 0 || pos0 < 0 || n_kv_heads < 1 || head_dim < 1 || n_vram_cells < 0 || capacity_cells < 0)
+    return fail(KVO_ERR_ARG, "%s: bad size", fn);
+  if (n_new == 0) return KVO_OK;
+  if (pos0 + n_new > capacity_cells) return fail(KVO_ERR_ARG, "%s: cells past the capacity", fn);
+  if (src_dtype != KVO_F16 && src_dtype != KVO_BF16)
+    return fail(KVO_ERR_UNSUPPORTED, "%s: source dtype must be f16 or bf16", fn);
+  if (kv_dtype != KVO_Q8_0 && kv_dtype != src_dtype)
+    return fail(KVO_ERR_UNSUPPORTED, "%s: a f16/bf16 cache takes its own dtype only", fn);
+  if (kv_dtype == KVO_Q8_0 && head_dim % 32)
+    return fail(KVO_ERR_UNSUPPORTED, "%s: q8_0 needs head_dim %% 32 == 0", fn);
+  if (kv_dtype == KVO_Q8_0 && n_kv_heads * head_dim > 8 * 256)
+    return fail(KVO_ERR_UNSUPPORTED, "%s: q8_0 rows of more than 2048 values", fn);
+  const int64_t src_row = n_kv_heads * head_dim * 2;
+  const int64_t rb = kv_dtype == KVO_Q8_0 ? n_kv_heads * (head_dim / 32) * 34 : src_row;
+  if (src_row % 16 || (kv_dtype != KVO_Q8_0 && rb % 16))
+    return fail(KVO_ERR_ALIGN, "%s: row bytes %% 16 != 0", fn);
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(KVO_ERR_ALIGN, "%s: source alignment", fn);
+  if (!classify(k_new, (size_t)n_new * src_row) || !classify(v_new, (size_t)n_new * src_row))
+    return fail(KVO_ERR_NOT_MAPPED, "%s: k_new/v_new not device-accessible", fn);
+  const int64_t n_lo = n_vram_cells < capacity_cells ? n_vram_cells : capacity_cells;
+  const int64_t end = pos0 + n_new;
+  if (pos0 < n_lo) {                                   // touches the VRAM head
+    const size_t bytes = (size_t)(end < n_lo ? end : n_lo) * rb;
+    if (classify(k_vram, bytes) != kDeviceMem || classify(v_vram, bytes) != kDeviceMem)
+      return fail(KVO_ERR_NOT_MAPPED, "%s: k_vram/v_vram must be device memory", fn);
+    if (kv_dtype != KVO_Q8_0 && (!aligned16(k_vram) || !aligned16(v_vram)))
+      return fail(KVO_ERR_ALIGN, "%s: vram alignment", fn);
+    if (kv_dtype == KVO_Q8_0 && (((uintptr_t)k_vram | (uintptr_t)v_vram) & 1))
+      return fail(KVO_ERR_ALIGN, "%s: vram alignment", fn);
+  }
+  if (end > n_lo) {                                    // touches the host tail
+    const size_t bytes = (size_t)(end - n_lo) * rb;
+    if (!classify(k_host, bytes) || !classify(v_host, bytes))
+      return fail(KVO_ERR_NOT_MAPPED, "%s: k_host/v_host not device-accessible", fn);
+    if (kv_dtype != KVO_Q8_0 && (!aligned16(k_host) || !aligned16(v_host)))
+      return fail(KVO_ERR_ALIGN, "%s: host alignment", fn);
+    if (kv_dtype == KVO_Q8_0 && (((uintptr_t)k_host | (uintptr_t)v_host) & 1))
+      return fail(KVO_ERR_ALIGN, "%s: host alignment", fn);
+  }
+  AppendArgs a;
+  a.k_new = (const uint8_t *)k_new; a.v_new = (const uint8_t *)v_new;
+  a.src_dtype = src_dtype; a.kv_dtype = kv_dtype;
+  a.n_new = n_new; a.pos0 = pos0; a.n_kv_heads = n_kv_heads; a.head_dim = head_dim; a.row_bytes = rb;
+  a.k_lo = (uint8_t *)k_vram; a.v_lo = (uint8_t *)v_vram;
+  a.k_hi = (uint8_t *)k_host; a.v_hi = (uint8_t *)v_host;
+  a.n_vram = n_lo;
+  return launch_append(a, (cudaStream_t)stream);
 }
 
 // ---------------------------------------------------------------- a7-a8

@@ -81,4 +81,14 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t st);  // kvo_status (mma.s
 int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg, int64_t seg_rows,
                       cudaStream_t st);
 
+struct AppendArgs {
+  const uint8_t *k_new, *v_new;  // [n_new][n_kv_heads][head_dim] of src_dtype
+  int src_dtype, kv_dtype;
+  int64_t n_new, pos0, n_kv_heads, head_dim, row_bytes;   // row_bytes: cache row
+  uint8_t *k_lo, *v_lo;          // cells < n_vram: row j
+  uint8_t *k_hi, *v_hi;          // cells >= n_vram: row j - n_vram
+  int64_t n_vram;
+};
+int launch_append(const AppendArgs &a, cudaStream_t st);   // kvo_status
+
 }  // namespace kvo

@@ -207,7 +207,6 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t *v) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <int DT>
@@ -474,7 +473,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float x[32];
         tmem_ld32(s_addr + c * 32, x);
@@ -524,7 +523,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       float sm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         float x[32];
         tmem_ld32(s_addr + c * 32, x);

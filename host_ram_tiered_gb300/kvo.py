@@ -19,7 +19,8 @@ KVO_SWAP_D2H = 0x2
 KVO_SWAP_SRC_ORDER_ANY = 0x4
 KVO_SWAP_FORCE_SM = 0x8
 KVO_SWAP_FORCE_CE = 0x10
-KVO_SWAP_CE_MIN_MEAN_BYTES = 1 << 20
+KVO_SWAP_CE_MIN_BYTES = 1 << 20
+KVO_SWAP_CE_MAX_DESCRIPTORS = 64
 KVO_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 STATUS = {0: "KVO_OK", -1: "KVO_ERR_ARG", -2: "KVO_ERR_ALIGN", -3: "KVO_ERR_NOT_MAPPED",
@@ -34,6 +35,8 @@ SIGNATURES = {
     "kvo_last_error": (ctypes.c_char_p, []),
     "kvo_device_errors": (_int, [_vp, _int]),
     "kvo_sub_block_ptrs": (_int, [_vp, _i64, _i64, _i64, _u64, _i64, _i64, _vp, _i64]),
+    "kvo_copy_plan": (_int, [_vp] * 6 + [_i64, _int, _vp, _vp, _vp, _i64, _vp]),
+    "kvo_fragment_ptrs": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "kvo_swap_blocks_batch": (_int, [_vp, _vp, _vp, _i64, _u32, _vp]),
     "kvo_gather_blocks": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _i64, _vp, _i64, _vp,
                                  _vp, _vp]),
@@ -44,6 +47,8 @@ SIGNATURES = {
     "kvo_attn_decode_tiered_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp,
                                               _vp, _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp,
                                               _vp]),
+    "kvo_append_kv_tiered": (_int, [_vp, _vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
+                                    _int, _i64, _i64, _vp]),
     "kvo_attn_prefill_workspace_bytes": (_sz, [_i64, _i64]),
     "kvo_attn_prefill_tiered": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                        _int, _i64, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz,
@@ -81,11 +86,13 @@ def load():
 
 
 def _p(x) -> int | None:
-    """Address of a tensor / int / None."""
+    """Address of a tensor / numpy array / int / None."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
     return x.data_ptr()
 
 
@@ -121,6 +128,24 @@ def kvo_sub_block_ptrs(block_ids, n_ids, blocks_per_chunk, skip_count, base, row
     _check(load().kvo_sub_block_ptrs(_p(block_ids), n_ids, blocks_per_chunk, skip_count, base,
                                      row_stride_bytes, row_bytes, _p(out), n_out),
            "kvo_sub_block_ptrs")
+
+
+def kvo_copy_plan(local_offset, local_stride, canonical_offset, canonical_stride, num_fragments,
+                  fragment_size, n_runs, gpu_to_cpu, frag_src, frag_dst, frag_sizes, capacity) -> int:
+    """Returns the fragment count written to frag_src / frag_dst / frag_sizes."""
+    n = ctypes.c_int64(0)
+    _check(load().kvo_copy_plan(_p(local_offset), _p(local_stride), _p(canonical_offset),
+                                _p(canonical_stride), _p(num_fragments), _p(fragment_size), n_runs,
+                                int(gpu_to_cpu), _p(frag_src), _p(frag_dst), _p(frag_sizes), capacity,
+                                ctypes.addressof(n)), "kvo_copy_plan")
+    return n.value
+
+
+def kvo_fragment_ptrs(src_bases, dst_bases, n_blocks, frag_src, frag_dst, frag_sizes, n_frags,
+                      out_src, out_dst, out_sizes) -> None:
+    _check(load().kvo_fragment_ptrs(_p(src_bases), _p(dst_bases), n_blocks, _p(frag_src),
+                                    _p(frag_dst), _p(frag_sizes), n_frags, _p(out_src), _p(out_dst),
+                                    _p(out_sizes)), "kvo_fragment_ptrs")
 
 
 def kvo_swap_blocks_batch(src, dst, sizes, n, flags, stream=None) -> None:
@@ -161,6 +186,15 @@ def kvo_attn_decode_tiered_noalloc(q, q_dtype, batch, n_q_heads, n_kv_heads, hea
         vram_seq_stride_rows, _p(k_host), _p(v_host), host_seq_stride_rows, kv_dtype, _p(ctx_len),
         max_ctx, n_vram_cells, scale, _p(staging_k), _p(staging_v), _p(out), _s(stream)),
         "kvo_attn_decode_tiered_noalloc")
+
+
+def kvo_append_kv_tiered(k_new, v_new, src_dtype, n_new, pos0, n_kv_heads, head_dim, k_vram,
+                         v_vram, k_host, v_host, kv_dtype, n_vram_cells, capacity_cells,
+                         stream=None) -> None:
+    _check(load().kvo_append_kv_tiered(
+        _p(k_new), _p(v_new), src_dtype, n_new, pos0, n_kv_heads, head_dim, _p(k_vram), _p(v_vram),
+        _p(k_host), _p(v_host), kv_dtype, n_vram_cells, capacity_cells, _s(stream)),
+        "kvo_append_kv_tiered")
 
 
 def kvo_attn_prefill_workspace_bytes(rows, n_q_heads) -> int:

@@ -86,6 +86,45 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
                        int64_t row_bytes, int64_t *out, int64_t n_out);
 
 /* ------------------------------------------------------------------------
+ * kvo_copy_plan / kvo_fragment_ptrs -- host functions, synchronous, no CUDA:
+ * descriptors for a canonical host layout, fed to kvo_swap_blocks_batch.
+ *
+ * vLLM gpu_worker.py, _build_copy_plan: in a canonical layout one cache
+ * block is scattered as fragments that come from mapping runs.  Run r has
+ * num_fragments[r] fragments of fragment_size[r] bytes; fragment i sits at
+ * local_offset[r] + i * local_stride[r] in the worker's block and at
+ * canonical_offset[r] + i * canonical_stride[r] in the canonical block.
+ * kvo_copy_plan lists the fragments run by run into frag_src / frag_dst /
+ * frag_sizes (int64[capacity], host): source and destination offsets are
+ * (local, canonical) when gpu_to_cpu is non-zero, (canonical, local)
+ * otherwise; *n_frags receives the count.
+ *
+ * vLLM gpu_worker.py, _fill_canonical_ops (its step 3): kvo_fragment_ptrs
+ * expands per-block base addresses (e.g. from kvo_sub_block_ptrs) and the
+ * plan into one descriptor per (block, fragment), block-major:
+ *     out_src[b * n_frags + f] = src_bases[b] + frag_src[f]
+ *     out_dst[b * n_frags + f] = dst_bases[b] + frag_dst[f]
+ *     out_sizes[b * n_frags + f] = frag_sizes[f]
+ * All arrays are host int64.  (The pages' multi-rank writer rotation is not
+ * part of this.)
+ * Errors: KVO_ERR_ARG for negative counts or sizes, NULL arrays with a
+ * non-zero count, or more fragments than capacity.
+ * ---------------------------------------------------------------------- */
+int kvo_copy_plan(const int64_t *local_offset, const int64_t *local_stride,
+                  const int64_t *canonical_offset,
+                  const int64_t *canonical_stride,
+                  const int64_t *num_fragments, const int64_t *fragment_size,
+                  int64_t n_runs, int gpu_to_cpu, int64_t *frag_src,
+                  int64_t *frag_dst, int64_t *frag_sizes, int64_t capacity,
+                  int64_t *n_frags);
+
+int kvo_fragment_ptrs(const int64_t *src_bases, const int64_t *dst_bases,
+                      int64_t n_blocks, const int64_t *frag_src,
+                      const int64_t *frag_dst, const int64_t *frag_sizes,
+                      int64_t n_frags, int64_t *out_src, int64_t *out_dst,
+                      int64_t *out_sizes);
+
+/* ------------------------------------------------------------------------
  * kvo_swap_blocks_batch -- batched block copy between a paged device cache
  * and pinned host blocks.
  *
@@ -104,10 +143,14 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
  * flags: KVO_SWAP_H2D or KVO_SWAP_D2H (direction, used for the mode
  *   choice); KVO_SWAP_SRC_ORDER_ANY (the source is not written while the copy
  *   runs: the SM kernel may read it through the read-only path);
- *   KVO_SWAP_FORCE_SM / KVO_SWAP_FORCE_CE force a mode.  Default: SM mode
- *   unless the mean descriptor is at least KVO_SWAP_CE_MIN_MEAN_BYTES, a
- *   crossover measured on GB300 (copy-engine calls cost ~2.7 us each; SM
- *   copies reach the same link bandwidth as the copy engine).
+ *   KVO_SWAP_FORCE_SM / KVO_SWAP_FORCE_CE force a mode.  Default: the copy
+ *   engine when there are at most KVO_SWAP_CE_MAX_DESCRIPTORS descriptors
+ *   and each is at least KVO_SWAP_CE_MIN_BYTES, else SM mode -- a crossover
+ *   measured on GB300: SM copies reach the same link bandwidth as the copy
+ *   engine from 2 KiB pages up, while a copy-engine call costs ~2.7 us to
+ *   issue, so the copy engine is only worth it (it leaves the SMs free) for
+ *   a few large copies.  The rule reads no more than
+ *   KVO_SWAP_CE_MAX_DESCRIPTORS sizes on the host.
  * n == 0 is a no-op.
  * Errors: KVO_ERR_ARG (n < 0, NULL arrays, both FORCE flags),
  *   KVO_ERR_NOT_MAPPED (descriptor arrays not device-accessible in SM mode,
@@ -118,7 +161,8 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
 #define KVO_SWAP_SRC_ORDER_ANY 0x4u
 #define KVO_SWAP_FORCE_SM 0x8u
 #define KVO_SWAP_FORCE_CE 0x10u
-#define KVO_SWAP_CE_MIN_MEAN_BYTES (1 << 20)
+#define KVO_SWAP_CE_MIN_BYTES (1 << 20)
+#define KVO_SWAP_CE_MAX_DESCRIPTORS 64
 
 int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst,
                           const int64_t *sizes, int64_t n, uint32_t flags,
@@ -241,6 +285,39 @@ int kvo_attn_decode_tiered_noalloc(const void *q, int q_dtype, int64_t batch,
                                    int64_t n_vram_cells, float scale,
                                    void *staging_k, void *staging_v,
                                    float *out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_append_kv_tiered -- write path: new tokens into a tiered cache.
+ *
+ * ExLlamaV3 qsa-kv-offload patch (the paged cache update that writes new
+ * tokens' K/V into the host-resident planes) and llama.cpp PR "tiered KV
+ * cache": token t < n_new of k_new / v_new becomes cell pos0 + t of one
+ * sequence, stored in the tier that holds it -- VRAM head row j for j < N,
+ * pinned host tail row j - N for j >= N -- in the cache dtype.
+ *   kv_dtype == src_dtype (F16 or BF16): the rows are copied.
+ *   kv_dtype == Q8_0: each 32-value block of each head is quantised in
+ *     fp32: amax = max|x|, d = amax / 127, q = round-half-away-from-zero(
+ *     x * (1/d)) (0 when d == 0), stored as {fp16 d (round to nearest
+ *     even); int8 q[32]}.  The pages name the q8_0 format, not its rounding:
+ *     this rule is the library's stated reading.  q8_0 rows hold at most
+ *     2048 values (n_kv_heads * head_dim).
+ *
+ * k_new, v_new: device-accessible [n_new][n_kv_heads][head_dim] of src_dtype
+ *   (F16 or BF16), 16-byte aligned.
+ * k_vram, v_vram: the head, min(N, capacity_cells) rows; k_host, v_host:
+ *   the tail, capacity_cells - N rows (either may be NULL if never touched).
+ *   Rows of n_kv_heads * head_dim values or n_kv_heads * head_dim/32 q8_0
+ *   blocks; f16/bf16 tiers 16-byte aligned, q8_0 tiers 2-byte aligned.
+ * Errors: KVO_ERR_ARG (cells past capacity_cells, bad sizes),
+ *   KVO_ERR_UNSUPPORTED (dtype pair), KVO_ERR_ALIGN, KVO_ERR_NOT_MAPPED,
+ *   KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int kvo_append_kv_tiered(const void *k_new, const void *v_new, int src_dtype,
+                         int64_t n_new, int64_t pos0, int64_t n_kv_heads,
+                         int64_t head_dim, void *k_vram, void *v_vram,
+                         void *k_host, void *v_host, int kv_dtype,
+                         int64_t n_vram_cells, int64_t capacity_cells,
+                         void *stream);
 
 /* ------------------------------------------------------------------------
  * kvo_attn_prefill_tiered -- causal chunked-prefill GQA attention over a

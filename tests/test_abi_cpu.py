@@ -96,3 +96,36 @@ def test_swap_host_side_checks_need_no_gpu(kvo_lib):
 def test_workspace_sizes_are_deterministic(kvo_lib):
     assert kvo.kvo_attn_prefill_workspace_bytes(2048, 32) == 2048 * 32 * 2 * 4
     assert kvo.kvo_attn_prefill_workspace_bytes(-1, 32) == 0
+
+
+# ---------------------------------------------------------------- canonical fragments
+
+RUNS = [(0, 1024, 0, 256, 4, 256), (4096, 0, 1024, 0, 1, 512), (2048, 64, 3000, 96, 3, 32)]
+
+
+@pytest.mark.parametrize("gpu_to_cpu", [True, False])
+def test_copy_plan_matches_oracle(kvo_lib, gpu_to_cpu):
+    cols = [np.array([r[k] for r in RUNS], np.int64) for k in range(6)]
+    cap = 16
+    fs, fd, fz = (np.zeros(cap, np.int64) for _ in range(3))
+    n = kvo.kvo_copy_plan(*cols, len(RUNS), gpu_to_cpu, fs, fd, fz, cap)
+    es, ed, ez = oracle.copy_plan(RUNS, gpu_to_cpu)
+    assert n == len(es)
+    assert np.array_equal(fs[:n], es) and np.array_equal(fd[:n], ed) and np.array_equal(fz[:n], ez)
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_copy_plan(*cols, len(RUNS), gpu_to_cpu, fs, fd, fz, n - 1)
+    assert e.value.status == -1
+
+
+def test_fragment_ptrs_matches_oracle(kvo_lib):
+    g = synth.rng(35)
+    nb = 37
+    sb = g.integers(0, 1 << 40, size=nb).astype(np.int64)
+    db = g.integers(0, 1 << 40, size=nb).astype(np.int64)
+    es, ed, ez = oracle.copy_plan(RUNS, True)
+    nf = len(es)
+    os_, od, oz = (np.zeros(nb * nf, np.int64) for _ in range(3))
+    kvo.kvo_fragment_ptrs(sb, db, nb, es, ed, ez, nf, os_, od, oz)
+    rs, rd, rz = oracle.fragment_ptrs(sb.view(np.uint64), db.view(np.uint64), es, ed, ez)
+    assert np.array_equal(os_.view(np.uint64), rs) and np.array_equal(od.view(np.uint64), rd)
+    assert np.array_equal(oz, rz)

@@ -220,3 +220,42 @@ def test_c2_full_size_swap_sampled(page):
         assert np.array_equal(host[hs:hs + page], exp)
         got = dev[ds:ds + page].cpu().numpy()
         assert np.array_equal(got, exp)
+
+
+@pytest.mark.parametrize("gpu_to_cpu", [True, False])
+def test_canonical_fragment_swap(gpu_to_cpu):
+    # A 32 KiB device block (16 tokens x 8 heads x 128 fp16) stored canonically on the
+    # host head-major: fragment (token t, head h) of 256 B moves from t*2048 + h*256
+    # locally to h*4096 + t*256 canonically -- 8 runs of 16 fragments each.
+    t = torch()
+    g = synth.rng(36, int(gpu_to_cpu))
+    page, nb, pool = 32768, 24, 64
+    runs = [(h * 256, 2048, h * 4096, 256, 16, 256) for h in range(8)]
+    cols = [np.array([r[k] for r in runs], np.int64) for k in range(6)]
+    fs, fd, fz = (np.zeros(128, np.int64) for _ in range(3))
+    nf = kvo.kvo_copy_plan(*cols, len(runs), gpu_to_cpu, fs, fd, fz, 128)
+    dev = t.from_numpy(g.integers(0, 256, size=pool * page, dtype=np.uint8)).cuda()
+    host = pinned(pool * page)
+    host.numpy()[:] = g.integers(0, 256, size=pool * page, dtype=np.uint8)
+    dev_ids = g.permutation(pool)[:nb]
+    host_ids = g.permutation(pool)[:nb]
+    dev_b = (dev.data_ptr() + dev_ids * page).astype(np.int64)
+    host_b = (host.data_ptr() + host_ids * page).astype(np.int64)
+    sb, db = (dev_b, host_b) if gpu_to_cpu else (host_b, dev_b)
+    n = nb * nf
+    os_, od, oz = (np.zeros(n, np.int64) for _ in range(3))
+    kvo.kvo_fragment_ptrs(sb, db, nb, fs[:nf], fd[:nf], fz[:nf], nf, os_, od, oz)
+    dev_mirror = dev.cpu().numpy().copy()
+    host_mirror = host.numpy().copy()
+    kvo.kvo_swap_blocks_batch(_pinned_i64(os_), _pinned_i64(od), _pinned_i64(oz), n,
+                              kvo.KVO_SWAP_D2H if gpu_to_cpu else kvo.KVO_SWAP_H2D)
+    t.cuda.synchronize()
+    # oracle: the same plan and descriptors, built by the oracle, on host mirrors
+    es, ed, ez = oracle.copy_plan(runs, gpu_to_cpu)
+    mb_dev = (np.uint64(dev_mirror.ctypes.data) + (dev_ids * page).astype(np.uint64))
+    mb_host = (np.uint64(host_mirror.ctypes.data) + (host_ids * page).astype(np.uint64))
+    msb, mdb = (mb_dev, mb_host) if gpu_to_cpu else (mb_host, mb_dev)
+    rs, rd, rz = oracle.fragment_ptrs(msb, mdb, es, ed, ez)
+    oracle.swap_blocks(rs, rd, rz)
+    assert np.array_equal(host.numpy(), host_mirror)
+    assert np.array_equal(dev.cpu().numpy(), dev_mirror)
