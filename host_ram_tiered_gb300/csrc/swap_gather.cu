@@ -43,24 +43,26 @@ __device__ __forceinline__ void warp_copy(const char *s, char *d, int64_t bytes,
   }
 }
 
-// A warp takes 32 consecutive descriptors: lane i loads descriptor i (three
-// coalesced reads through the mapping instead of 32 dependent ones), then
-// the warp copies them one after another, broadcasting each by shuffle.
+// A warp takes `per_warp` (1..32) consecutive descriptors: lane i loads
+// descriptor i (coalesced reads through the mapping instead of dependent
+// ones), then the warp copies them one after another, broadcasting each by
+// shuffle.  per_warp is chosen so the grid fills the GPU even for short
+// batches.
 __global__ void __launch_bounds__(kSwapThreads)
 swap_kernel(const int64_t *__restrict__ src, const int64_t *__restrict__ dst,
-            const int64_t *__restrict__ sizes, int64_t n) {
+            const int64_t *__restrict__ sizes, int64_t n, int per_warp) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kSwapThreads + threadIdx.x) >> 5;
   const int64_t n_warps = ((int64_t)gridDim.x * kSwapThreads) >> 5;
-  for (int64_t base = warp * 32; base < n; base += n_warps * 32) {
+  for (int64_t base = warp * per_warp; base < n; base += n_warps * per_warp) {
     const int64_t i = base + lane;
     int64_t s = 0, d = 0, z = 0;
-    if (i < n) {
+    if (lane < per_warp && i < n) {
       s = src[i];
       d = dst[i];
       z = sizes[i];
     }
-    const int cnt = n - base < 32 ? (int)(n - base) : 32;
+    const int cnt = n - base < per_warp ? (int)(n - base) : per_warp;
     for (int k = 0; k < cnt; ++k) {
       const int64_t zk = __shfl_sync(0xffffffffu, z, k);
       const int64_t sk = __shfl_sync(0xffffffffu, s, k);
@@ -145,14 +147,17 @@ uint32_t *device_error_word() {
 
 cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes, int64_t n,
                            bool src_readonly, cudaStream_t st) {
-  const int64_t desc_per_cta = kSwapThreads;      // 8 warps x 32 descriptors
-  int64_t grid = (n + desc_per_cta - 1) / desc_per_cta;
-  const int64_t cap = (int64_t)num_sms() * 8;      // 8 CTAs of 8 warps per SM in flight
-  if (grid > cap) grid = cap;
   // Every copy here is stream-ordered, which already satisfies both source
   // access orders; the read-only hint needs no separate kernel.
   (void)src_readonly;
-  swap_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(src, dst, sizes, n);
+  const int64_t warps_per_cta = kSwapThreads / 32;
+  const int64_t max_warps = (int64_t)num_sms() * 8 * warps_per_cta;   // 8 CTAs of 8 warps per SM
+  int64_t per_warp = n / max_warps;
+  if (per_warp < 1) per_warp = 1;
+  if (per_warp > 32) per_warp = 32;
+  int64_t grid = (n + per_warp * warps_per_cta - 1) / (per_warp * warps_per_cta);
+  if (grid > max_warps / warps_per_cta) grid = max_warps / warps_per_cta;
+  swap_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(src, dst, sizes, n, (int)per_warp);
   return cudaGetLastError();
 }
 
