@@ -178,34 +178,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Issue a 32-column TMEM load without waiting; the registers are valid only
-// after tmem_wait_bind on the same array.
-__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t *r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-
-// Wait for all outstanding TMEM loads; the array passes through the asm so
-// no use of it can move above the wait.
-__device__ __forceinline__ void tmem_wait_bind(uint32_t *r) {
-  asm volatile(
-      "tcgen05.wait::ld.sync.aligned;"
-      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
-        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
-        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
-        "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
-        "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-      :
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -501,31 +473,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-      // two 32-column loads in flight: chunk c+1 is read from TMEM while
-      // chunk c is reduced
-      auto max_chunk = [&](const uint32_t *u, int c) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(u[i]);
-          if (need_mask) {
-            const int64_t cj = t0 + c * 32 + i;
-            if (!row_ok || cj >= c_end || cj > pos) v = -INFINITY;
-          }
-          mx[i & 7] = fmaxf(mx[i & 7], v);
-        }
-      };
-      {
-        uint32_t ua[32], ub[32];
-        tmem_ld32_async(s_addr, ua);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; c += 2) {
-          tmem_wait_bind(ua);
-          tmem_ld32_async(s_addr + (c + 1) * 32, ub);
-          max_chunk(ua, c);
-          tmem_wait_bind(ub);
-          if (c + 2 < BN / 32) tmem_ld32_async(s_addr + (c + 2) * 32, ua);
-          max_chunk(ub, c + 1);
+      for (int c = 0; c < BN / 32; ++c) {
+        float x[32];
+        tmem_ld32(s_addr + c * 32, x);
+        if (need_mask) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int64_t cj = t0 + c * 32 + i;
+            if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
+          }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
       }
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
@@ -563,16 +523,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       float sm[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sm[k] = 0.f;
-      auto exp_chunk = [&](uint32_t *u, int c) {
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
         float x[32];
+        tmem_ld32(s_addr + c * 32, x);
+        if (need_mask) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float v = __uint_as_float(u[i]);
-          if (need_mask) {
+          for (int i = 0; i < 32; ++i) {
             const int64_t cj = t0 + c * 32 + i;
-            if (!row_ok || cj >= c_end || cj > pos) v = -INFINITY;
+            const bool off = !row_ok || cj >= c_end || cj > pos;
+            x[i] = off ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
           }
-          x[i] = ex2(fmaf(v, a.scale_log2, nref));           // 2^-inf = 0
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = ex2(fmaf(x[i], a.scale_log2, nref));
         }
         uint32_t w[32];
 #pragma unroll
@@ -581,19 +545,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
           split2<DT>(x[2 * e], x[2 * e + 1], w[e], w[16 + e]);
         }
         tmem_st32u(s_addr + c * 32, w);
-      };
-      {
-        uint32_t ua[32], ub[32];
-        tmem_ld32_async(s_addr, ua);
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; c += 2) {
-          tmem_wait_bind(ua);
-          tmem_ld32_async(s_addr + (c + 1) * 32, ub);
-          exp_chunk(ua, c);
-          tmem_wait_bind(ub);
-          if (c + 2 < BN / 32) tmem_ld32_async(s_addr + (c + 2) * 32, ua);
-          exp_chunk(ub, c + 1);
-        }
       }
       l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       tmem_wait_st();
