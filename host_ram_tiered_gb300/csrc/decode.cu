@@ -5,20 +5,32 @@
 namespace kvo {
 namespace dec {
 template <int KVT> cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st);
-constexpr int kMinSplit = 64;
+constexpr int kMaxChunkTiles = 20;   // chunks of at most 640 cells
 }  // namespace dec
 
 void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *split_cells,
                      int *n_splits) {
   (void)head_dim;
-  // About four CTAs per SM over the whole batch; splits are multiples of 32
-  // cells (every tile size divides them) and at least kMinSplit cells.
-  const int64_t target = (int64_t)num_sms() * 4;
-  int64_t per = (max_ctx * (batch > 0 ? batch : 1) + target - 1) / target;
-  per = (per + 31) / 32 * 32;
-  if (per < dec::kMinSplit) per = dec::kMinSplit;
-  *split_cells = (int)per;
-  const int64_t ns = (max_ctx + per - 1) / per;
+  // Chunk length C (32..640 cells, whole 32-cell tiles) minimising the tiles
+  // of the busiest CTA when batch * ceil(max_ctx / C) chunks are dealt
+  // round-robin to one persistent CTA per SM; ties go to the longer chunk
+  // (fewer partials to combine).
+  const int64_t sms = num_sms();
+  const int64_t bt = batch > 0 ? batch : 1;
+  int64_t best_c = 32, best_cost = -1;
+  for (int64_t tiles = 1; tiles <= dec::kMaxChunkTiles; ++tiles) {
+    const int64_t c = tiles * 32;
+    const int64_t chunks = (max_ctx + c - 1) / c;
+    const int64_t waves = (bt * chunks + sms - 1) / sms;
+    const int64_t cost = (waves > 0 ? waves : 1) * tiles;
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      best_c = c;
+    }
+    if (chunks <= 1) break;                 // longer chunks change nothing
+  }
+  *split_cells = (int)best_c;
+  const int64_t ns = (max_ctx + best_c - 1) / best_c;
   *n_splits = (int)(ns > 0 ? ns : 1);
 }
 

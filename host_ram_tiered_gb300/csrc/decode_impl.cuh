@@ -4,19 +4,36 @@
 // the arithmetic does not depend on where a cell lives, so a tiered cache
 // gives output bit-identical to an all-VRAM one.
 //
-// One CTA = one fixed cell range (split) of one sequence, one warp per kv
-// head (n_kv_heads warps).  A tile of 32 cell rows (all kv heads, 16-byte
-// chunks, coalesced across the CTA) is copied into shared memory from
-// whichever tier holds each cell, rows padded so that lane-per-row reads hit
-// distinct banks.  Scores: lane c owns cell c of the tile and computes its
-// G dot products against the warp's query heads, which sit in shared memory
-// pre-scaled by scale*log2(e) (for q8_0 the block scale multiplies each
-// 32-value partial; d * q is exact in fp32).  Online softmax in the log2
-// domain with warp-wide max / sum (fixed butterflies).  P*V: lane l owns head
-// dims [l*D/32, (l+1)*D/32) and walks the tile's cells in order with the
-// weights broadcast from shared memory.  Each CTA writes an unnormalised
-// partial (m, l, acc); a second kernel folds the splits of a head in a fixed
-// order.  Instantiated per K/V dtype in decode_<dtype>.cu.
+// Work decomposition.  The cells of a sequence are cut into fixed chunks
+// (a multiple of 32 cells, a function of max_ctx, batch and the SM count
+// only).  Each chunk yields one unnormalised partial (m, l, acc) per query
+// head; a second kernel folds the chunks of a head in a fixed order.  Which
+// CTA computes a chunk never changes a bit of its partial, so the grid is
+// persistent (one CTA per SM, chunks dealt round-robin) and the tier split
+// only decides how a chunk's rows reach shared memory:
+//   * a chunk wholly in device memory streams through a 3-stage ring of
+//     32-cell tiles filled with cp.async (16-byte copies, L1 bypassed);
+//   * a chunk with host-resident rows is filled tile by tile with 16-byte
+//     loads through the host mapping, every thread keeping 8 in flight.
+//
+// Per tile, warp g (kv head g) computes the scores of the tile's 32 cells
+// for its G query heads, an online softmax in the log2 domain, and P*V:
+//   * QK: lane = (quarter or eighth of the head dims, cell).  The lane's
+//     query slice lives in registers as fp16/bf16 pairs for the whole chunk;
+//     each pass takes CPP cells, and the LPC partial dot products of a cell
+//     are added by a transposing butterfly, after which lane c holds the G
+//     scores of cell c.  Products are fp16 x fp16 (or bf16 x bf16) with an
+//     fp32 accumulator (exact products, fp32 sums).  A q8_0 value x enters as
+//     the exact fp16 number 1152 + x (its byte with the sign bit flipped under
+//     an 0x64 exponent byte); the 1152 * sum(q) term is removed once per
+//     block before the block scale d multiplies the sum.
+//   * softmax: per-head tile maxima by warp butterflies; the running maximum
+//     moves only when a tile exceeds it by more than 2^8 (all p stay <= 256);
+//     l is kept per lane and summed once per chunk.
+//   * PV: lane owns D/32 dims of every head; V is converted to fp32 (q8_0:
+//     exact d * x) and accumulated with packed f32x2 FMAs, weights (p, p)
+//     read from shared memory.
+// Instantiated per K/V dtype in decode_<dtype>.cu.
 #pragma once
 #include <cuda_fp16.h>
 #include <math.h>
@@ -26,6 +43,28 @@
 namespace kvo {
 namespace dec {
 
+constexpr int kTile = 32;                 // cells per tile
+constexpr int kMaxStages = 3;
+constexpr int kSmemLimit = 232448;        // dynamic shared memory per CTA (sm_103a opt-in)
+
+// Shared-memory pitch of a cell row: rows stay 16-byte aligned and an odd
+// number of 16-byte units apart, so 16-byte reads of consecutive rows by
+// 8 lanes hit distinct banks.
+__host__ __device__ constexpr int64_t row_pitch(int64_t rb) { return (rb % 32 == 0) ? rb + 16 : rb; }
+
+template <int KVT, int G, int D>
+struct Shape {
+  static constexpr int LPC = (G * D / 8 <= 96) ? 4 : 8;   // lanes per cell in QK
+  static constexpr int CPP = 32 / LPC;                    // cells per QK pass
+  static constexpr int NP = kTile / CPP;                  // QK passes per tile
+  static constexpr int DL = D / LPC;                      // head dims per lane in QK
+  static constexpr int QW = DL / 2;                       // query pair words per head
+  static constexpr int DV = D / 32;                       // head dims per lane in PV
+  static constexpr int NB = D / 32;                       // q8_0 blocks per head
+  static constexpr int HB = KVT == KVO_Q8_0 ? NB * 34 : 2 * D;   // bytes of one head in a row
+};
+
+// ---------------------------------------------------------------- helpers
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -39,106 +78,118 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// lo(a) * lo(b) + c and hi(a) * hi(b) + c for 16-bit float pairs (fp16, or
+// bf16 for a bf16 cache), fp32 accumulator.
+template <int KVT>
+__device__ __forceinline__ float mfma_lo(uint32_t a, uint32_t b, float c) {
+  float r;
+  if constexpr (KVT == KVO_BF16)
+    asm("{.reg .b16 a0,a1,b0,b1;\n mov.b32 {a0,a1}, %1;\n mov.b32 {b0,b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a0, b0, %3;}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 a0,a1,b0,b1;\n mov.b32 {a0,a1}, %1;\n mov.b32 {b0,b1}, %2;\n"
+        " fma.rn.f32.f16 %0, a0, b0, %3;}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  return r;
+}
+template <int KVT>
+__device__ __forceinline__ float mfma_hi(uint32_t a, uint32_t b, float c) {
+  float r;
+  if constexpr (KVT == KVO_BF16)
+    asm("{.reg .b16 a0,a1,b0,b1;\n mov.b32 {a0,a1}, %1;\n mov.b32 {b0,b1}, %2;\n"
+        " fma.rn.f32.bf16 %0, a1, b1, %3;}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{.reg .b16 a0,a1,b0,b1;\n mov.b32 {a0,a1}, %1;\n mov.b32 {b0,b1}, %2;\n"
+        " fma.rn.f32.f16 %0, a1, b1, %3;}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
+  return r;
+}
+
+// Packed fp32 pairs.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ float h2f(uint16_t b, int dt) {
   if (dt == KVO_BF16) return __uint_as_float((uint32_t)b << 16);
   return __half2float(__ushort_as_half(b));
-}
-
-// Four int8 values packed in a word -> four exact floats without the
-// conversion pipe: x ^ 0x80 is x + 128 as an unsigned byte; placed in the low
-// mantissa byte of 2^23 it reads as 2^23 + x + 128, and subtracting
-// 2^23 + 128 leaves x (all steps exact in fp32).
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float *f) {
-  const uint32_t u = w ^ 0x80808080u;
-  f[0] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)) - 8388736.f;
-  f[1] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)) - 8388736.f;
-  f[2] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)) - 8388736.f;
-  f[3] = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)) - 8388736.f;
-}
-
-// Four int8 values at a 2-byte aligned shared-memory address.
-__device__ __forceinline__ uint32_t ld_i8x4(const uint8_t *p) {
-  return __byte_perm(*(const uint16_t *)p, *(const uint16_t *)(p + 2), 0x5410);
-}
-
-// Read this lane's DPL dims of kv head g from a cell row held in shared memory.
-template <int KVT, int D>
-__device__ __forceinline__ void lane_dims(const uint8_t *row, int g, int lane, float *x) {
-  constexpr int DPL = D / 32;
-  if constexpr (KVT == KVO_Q8_0) {
-    constexpr int NB = D / 32;                       // blocks per head
-    constexpr int LPB = 32 / DPL;                    // lanes per block
-    const uint8_t *blk = row + (g * NB + lane / LPB) * 34;
-    const float d = __half2float(__ushort_as_half(*(const uint16_t *)blk));
-    const uint8_t *qs = blk + 2 + (lane % LPB) * DPL;  // 2-byte aligned
-    float f[4];
-    if constexpr (DPL == 4) i8x4_to_f32(ld_i8x4(qs), f);
-    else i8x4_to_f32(*(const uint16_t *)qs, f);
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) x[i] = d * f[i];
-  } else {
-    const uint16_t *h = (const uint16_t *)(row + g * D * 2) + lane * DPL;
-    if constexpr (DPL == 4) {
-      const uint2 u = *(const uint2 *)h;
-      x[0] = h2f(u.x & 0xffff, KVT); x[1] = h2f(u.x >> 16, KVT);
-      x[2] = h2f(u.y & 0xffff, KVT); x[3] = h2f(u.y >> 16, KVT);
-    } else {
-      const uint32_t u = *(const uint32_t *)h;
-      x[0] = h2f(u & 0xffff, KVT); x[1] = h2f(u >> 16, KVT);
-    }
-  }
-}
-
-constexpr int kTile = 32;                             // cells per tile (one per lane)
-
-// Shared-memory pitch of a cell row: 16 bytes of padding, so 16-byte rows
-// stay aligned and lane-per-row reads spread over the banks.
-template <int KVT>
-__host__ __device__ constexpr int64_t row_pitch(int64_t rb) {
-  return rb + 16;
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Tile of cell rows [c0, c0 + n) of sequence b (K and V) that lies wholly in
-// device memory: every 16-byte chunk is an asynchronous copy (cp.async,
-// bypassing L1), all in flight at once; V rows n..kTile-1 are zero-filled.
-template <int KVT>
-__device__ __forceinline__ void load_tile_async(const DecodeArgs &a, int b, int64_t c0, int n,
-                                                uint8_t *sk, uint8_t *sv) {
-  const int64_t rb = a.row_bytes;
-  const int64_t pitch = row_pitch<KVT>(rb);
-  const int cpr = (int)(rb >> 4);
-  const int total = kTile * cpr;
+// Four int8 values (one word) -> two packed fp32 pairs, exact: x ^ 0x80 is
+// x + 128 as an unsigned byte; in the low mantissa byte of 2^23 it reads as
+// 2^23 + x + 128, and subtracting 2^23 + 128 leaves x.
+__device__ __forceinline__ void i8x4_to_f32x2(uint32_t w, uint64_t &p01, uint64_t &p23) {
+  const uint32_t u = w ^ 0x80808080u;
+  const uint64_t bias = 0x4B0000804B000080ull;            // (2^23 + 128, 2^23 + 128)
+  p01 = fsub2(pk2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))), bias);
+  p23 = fsub2(pk2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))), bias);
+}
+
+// ---------------------------------------------------------------- tile fill
+
+// floor(n / d) for a divisor d >= 2 fixed per launch: m = ceil(2^32 / d)
+// gives the exact quotient for every n < 2^32 / d.
+struct FastDiv {
+  uint32_t d, m;
+};
+__host__ __device__ inline FastDiv make_fastdiv(uint32_t d) {
+  return FastDiv{d, (uint32_t)((0x100000000ull + d - 1) / d)};
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f) { return __umulhi(n, f.m); }
+
+// Source of 16-byte chunk ch of K or V row j of sequence b.
+__device__ __forceinline__ const int4 *row_src(const DecodeArgs &a, int b, int64_t j, bool is_v) {
+  const uint8_t *p;
+  if (j < a.n_vram) p = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * a.row_bytes;
+  else p = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * a.row_bytes;
+  return (const int4 *)p;
+}
+
+// Cell rows [c0, c0 + n) of sequence b, K and V, into one stage: asynchronous
+// 16-byte copies, all in flight at once (device-resident rows only).
+__device__ __forceinline__ void fill_async(const DecodeArgs &a, int b, int64_t c0, int n,
+                                           uint8_t *sk, uint8_t *sv, int64_t pitch, FastDiv cpr) {
+  const int total = n * (int)cpr.d;
   for (int i = threadIdx.x; i < 2 * total; i += blockDim.x) {
     const bool is_v = i >= total;
     const int k = is_v ? i - total : i;
-    const int r = k / cpr, ch = k - r * cpr;
-    const int64_t j = c0 + (r < n ? r : 0);
-    const uint8_t *src;
-    if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
-    else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
+    const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
     const uint32_t dst = smem_addr((is_v ? sv : sk) + r * pitch + ch * 16);
-    const uint32_t bytes = r < n ? 16u : 0u;            // 0: zero-fill, nothing read
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
-                 "l"((const int4 *)src + ch), "r"(bytes)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(row_src(a, b, c0 + r, is_v) + ch)
                  : "memory");
   }
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
-// Copy cell rows [c0, c0 + n) of sequence b (K and V) into shared memory;
-// V rows n..kTile-1 are zeroed (their weights are 0 and must meet finite
-// values).
-template <int KVT>
-__device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0, int n,
-                                          uint8_t *sk, uint8_t *sv) {
-  const int64_t rb = a.row_bytes;
-  const int64_t pitch = row_pitch<KVT>(rb);
-  const int cpr = (int)(rb >> 4);                    // 16-byte chunks per row
-  const int total = kTile * cpr;                     // per tensor, full tile
+// The same rows with plain 16-byte loads (any device-accessible memory),
+// eight per thread in flight.
+__device__ __forceinline__ void fill_sync(const DecodeArgs &a, int b, int64_t c0, int n,
+                                          uint8_t *sk, uint8_t *sv, int64_t pitch, FastDiv cpr) {
+  const int total = n * (int)cpr.d;
   const int nthr = blockDim.x;
   constexpr int kBatch = 8;
   for (int base = 0; base < 2 * total; base += kBatch * nthr) {
@@ -146,18 +197,11 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = base + u * nthr + (int)threadIdx.x;
-      v[u] = make_int4(0, 0, 0, 0);
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
-        const int r = k / cpr, ch = k - r * cpr;
-        if (r < n) {
-          const int64_t j = c0 + r;
-          const uint8_t *src;
-          if (j < a.n_vram) src = (is_v ? a.v_lo : a.k_lo) + (b * a.lo_seq_stride_rows + j) * rb;
-          else src = (is_v ? a.v_hi : a.k_hi) + (b * a.hi_seq_stride_rows + (j - a.n_vram)) * rb;
-          v[u] = *((const int4 *)src + ch);
-        }
+        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
+        v[u] = row_src(a, b, c0 + r, is_v)[ch];
       }
     }
 #pragma unroll
@@ -166,161 +210,311 @@ __device__ __forceinline__ void load_tile(const DecodeArgs &a, int b, int64_t c0
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
-        const int r = k / cpr, ch = k - r * cpr;
+        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
         *(int4 *)((is_v ? sv : sk) + r * pitch + ch * 16) = v[u];
       }
     }
   }
 }
 
-// Dot products of one cell's kv head g (row in shared memory) with the G
-// query heads (qs: [G][D] fp32, pre-scaled), into s[G].
+// ---------------------------------------------------------------- per-warp state
+
 template <int KVT, int G, int D>
-__device__ __forceinline__ void cell_scores(const uint8_t *row, int g, const float *qs, float *s) {
+struct WarpState {
+  using S = Shape<KVT, G, D>;
+  uint32_t q[G][S::QW];      // this lane's query slice, 16-bit pairs
+  float qb[G];               // q8_0: -1152 * sum of the slice (the offset term)
+  uint64_t acc[G][S::DV / 2];// PV accumulators, fp32 pairs
+  float m[G], l[G];          // running max (log2 units) and this lane's share of l
+};
+
+// ---------------------------------------------------------------- QK
+
+// Partial dot products of this lane's dims for cell row `row` (kv head g).
+template <int KVT, int G, int D>
+__device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const uint8_t *row, int g,
+                                        int qq, float scale_log2, float *part) {
+  using S = Shape<KVT, G, D>;
+  float sb[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) s[h] = 0.f;
+  for (int h = 0; h < G; ++h) sb[h] = 0.f;
   if constexpr (KVT == KVO_Q8_0) {
-    constexpr int NB = D / 32;
+    constexpr int DL = S::DL;                            // 16 or 32 values, one block
+    const int blk = (qq * DL) / 32, wo = (qq * DL) % 32;
+    const int o = (g * S::NB + blk) * 34;                // block start in the row
+    const float d = __half2float(__ushort_as_half(*(const uint16_t *)(row + o)));
+    const int vb = o + 2 + wo;                           // first value byte (even)
+    const uint32_t *wp = (const uint32_t *)(row + (vb & ~3));
+    const uint32_t sh = (uint32_t)(vb & 3) * 8;          // 0 or 16
+    uint32_t w[DL / 4 + 1];
 #pragma unroll
-    for (int bk = 0; bk < NB; ++bk) {
-      const uint8_t *blk = row + (g * NB + bk) * 34;
-      const float d = __half2float(__ushort_as_half(*(const uint16_t *)blk));
-      float sb[G];
+    for (int i = 0; i <= DL / 4; ++i) w[i] = wp[i];
+    float sc[G];                                         // second chain per head
 #pragma unroll
-      for (int h = 0; h < G; ++h) sb[h] = 0.f;
+    for (int h = 0; h < G; ++h) sc[h] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float kf[4];
-        i8x4_to_f32(ld_i8x4(blk + 2 + i), kf);
-        const float k0 = kf[0], k1 = kf[1], k2 = kf[2], k3 = kf[3];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float4 q = *(const float4 *)(qs + h * D + bk * 32 + i);
-          sb[h] = fmaf(q.x, k0, sb[h]);
-          sb[h] = fmaf(q.y, k1, sb[h]);
-          sb[h] = fmaf(q.z, k2, sb[h]);
-          sb[h] = fmaf(q.w, k3, sb[h]);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) s[h] = fmaf(d, sb[h], s[h]);
-    }
-  } else {
-    const uint8_t *hrow = row + g * D * 2;
-#pragma unroll 4
-    for (int dc = 0; dc < D / 8; ++dc) {
-      const uint4 u = *(const uint4 *)(hrow + dc * 16);
-      float k[8];
-      k[0] = h2f(u.x & 0xffff, KVT); k[1] = h2f(u.x >> 16, KVT);
-      k[2] = h2f(u.y & 0xffff, KVT); k[3] = h2f(u.y >> 16, KVT);
-      k[4] = h2f(u.z & 0xffff, KVT); k[5] = h2f(u.z >> 16, KVT);
-      k[6] = h2f(u.w & 0xffff, KVT); k[7] = h2f(u.w >> 16, KVT);
+    for (int i = 0; i < DL / 4; ++i) {
+      const uint32_t x = __funnelshift_r(w[i], w[i + 1], sh) ^ 0x80808080u;
+      const uint32_t k0 = __byte_perm(x, 0x64646464u, 0x4140);   // (1152 + x0, 1152 + x1)
+      const uint32_t k1 = __byte_perm(x, 0x64646464u, 0x4342);   // (1152 + x2, 1152 + x3)
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float4 q0 = *(const float4 *)(qs + h * D + dc * 8);
-        const float4 q1 = *(const float4 *)(qs + h * D + dc * 8 + 4);
-        float t = s[h];
-        t = fmaf(q0.x, k[0], t); t = fmaf(q0.y, k[1], t);
-        t = fmaf(q0.z, k[2], t); t = fmaf(q0.w, k[3], t);
-        t = fmaf(q1.x, k[4], t); t = fmaf(q1.y, k[5], t);
-        t = fmaf(q1.z, k[6], t); t = fmaf(q1.w, k[7], t);
-        s[h] = t;
+        sb[h] = mfma_lo<KVT>(ws.q[h][2 * i], k0, sb[h]);
+        sc[h] = mfma_hi<KVT>(ws.q[h][2 * i], k0, sc[h]);
+        sb[h] = mfma_lo<KVT>(ws.q[h][2 * i + 1], k1, sb[h]);
+        sc[h] = mfma_hi<KVT>(ws.q[h][2 * i + 1], k1, sc[h]);
       }
     }
-  }
-}
-
-template <int KVT, int QT, int G, int D>
-__global__ void __launch_bounds__(256)
-decode_split_kernel(const DecodeArgs a) {
-  constexpr int DPL = D / 32;
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int split = blockIdx.x, b = blockIdx.y;
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
-  const int64_t cs = (int64_t)split * a.split_cells;
-  const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
-  if (cs >= ce) return;                               // split beyond the context: never combined
-  const int64_t pitch = row_pitch<KVT>(a.row_bytes);
-  float *qs_all = (float *)smem;                                    // [Hq][D]
-  float *ps_all = qs_all + (size_t)a.n_q_heads * D;                 // [Hkv][G][kTile]
-  uint8_t *sk = (uint8_t *)(ps_all + (size_t)a.n_kv_heads * G * kTile);
-  uint8_t *sv = sk + (size_t)kTile * pitch;
-  float *qs = qs_all + (size_t)g * G * D;
-  float *ps = ps_all + (size_t)g * G * kTile;
-  // Cells wholly in device memory are fetched with asynchronous copies;
-  // host-mapped cells with plain 16-byte loads.  Same bytes either way.
-  const bool dev_split = ce <= a.n_vram || a.hi_device;
-
-  // query heads of this sequence, pre-scaled, into shared memory
-  for (int i = threadIdx.x; i < a.n_q_heads * D; i += blockDim.x)
-    qs_all[i] = h2f(((const uint16_t *)a.q)[(size_t)b * a.n_q_heads * D + i], QT) * a.scale_log2;
-
-  float acc[G][DPL], m[G], l[G];
+    const float ds = d * scale_log2;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
+    for (int h = 0; h < G; ++h) part[h] = ds * ((sb[h] + sc[h]) + ws.qb[h]);
+  } else {
+    const uint4 *kp = (const uint4 *)(row + g * S::HB + qq * S::DL * 2);
+    float sc[G];                                         // second chain per head
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[h][i] = 0.f;
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-  }
-
-  for (int64_t t0 = cs; t0 < ce; t0 += kTile) {
-    const int n = ce - t0 < kTile ? (int)(ce - t0) : kTile;
-    __syncthreads();                                  // previous tile fully consumed
-    if (dev_split) load_tile_async<KVT>(a, b, t0, n, sk, sv);
-    else load_tile<KVT>(a, b, t0, n, sk, sv);
-    __syncthreads();
-    float sc[G];
-    cell_scores<KVT, G, D>(sk + (size_t)lane * pitch, g, qs, sc);
+    for (int h = 0; h < G; ++h) sc[h] = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float sv_h = lane < n ? sc[h] : -INFINITY;
-      const float m_new = fmaxf(m[h], warp_max(sv_h));
-      const float alpha = exp2f(m[h] - m_new);
-      const float p = lane < n ? exp2f(sv_h - m_new) : 0.f;
-      l[h] = l[h] * alpha + warp_sum(p);
+    for (int i = 0; i < S::DL / 8; ++i) {
+      const uint4 k = kp[i];
+      const uint32_t kw[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) acc[h][i] *= alpha;
-      m[h] = m_new;
-      ps[h * kTile + lane] = p;
-    }
-    __syncwarp();
-    for (int c = 0; c < kTile; c += 4) {
-      if (c >= n) break;
-      float4 p4[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) p4[h] = *(const float4 *)(ps + h * kTile + c);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float vd[DPL];
-        lane_dims<KVT, D>(sv + (size_t)(c + cc) * pitch, g, lane, vd);
+      for (int e = 0; e < 4; ++e)
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float pc = cc == 0 ? p4[h].x : cc == 1 ? p4[h].y : cc == 2 ? p4[h].z : p4[h].w;
-#pragma unroll
-          for (int i = 0; i < DPL; ++i) acc[h][i] = fmaf(pc, vd[i], acc[h][i]);
+          sb[h] = mfma_lo<KVT>(ws.q[h][4 * i + e], kw[e], sb[h]);
+          sc[h] = mfma_hi<KVT>(ws.q[h][4 * i + e], kw[e], sc[h]);
         }
-      }
     }
+#pragma unroll
+    for (int h = 0; h < G; ++h) part[h] = (sb[h] + sc[h]) * scale_log2;
   }
+}
 
+// Scores of the tile's 32 cells: lane c ends with the G scores of cell c.
+template <int KVT, int G, int D>
+__device__ __forceinline__ void qk_tile(const WarpState<KVT, G, D> &ws, const uint8_t *sk,
+                                        int64_t pitch, int g, int lane, float scale_log2,
+                                        float *s) {
+  using S = Shape<KVT, G, D>;
+  const int qq = lane / S::CPP, cl = lane % S::CPP;
+  float v[S::NP][G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const int qh = g * G + h;
-    const size_t pi = ((size_t)b * a.n_splits + split) * a.n_q_heads + qh;
-    float *pa = a.part_acc + pi * D + lane * DPL;
+  for (int ps = 0; ps < S::NP; ++ps)
+    qk_cell<KVT, G, D>(ws, sk + (int64_t)(cl + S::CPP * ps) * pitch, g, qq, scale_log2, v[ps]);
+  // Transposing butterfly: stage k pairs passes that differ in bit k and
+  // keeps the one whose bit k equals bit k of qq, adding the partner lane's
+  // (lane ^ (CPP << k)) other half.  After log2(LPC) stages the remaining
+  // pass is qq, i.e. cell cl + CPP * qq = lane.
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) pa[i] = acc[h][i];
-    if (lane == 0) {
-      a.part_ml[pi * 2] = m[h];
-      a.part_ml[pi * 2 + 1] = l[h];
+  for (int k = 0, n = S::NP; n > 1; ++k, n >>= 1) {
+    const bool hi = (qq >> k) & 1;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i)
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mine = hi ? v[2 * i + 1][h] : v[2 * i][h];
+        const float other = hi ? v[2 * i][h] : v[2 * i + 1][h];
+        v[i][h] = mine + __shfl_xor_sync(0xffffffffu, other, S::CPP << k);
+      }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) s[h] = v[0][h];
+}
+
+// ---------------------------------------------------------------- PV
+
+// This lane's D/32 dims of V for cell row `row` (kv head g), as fp32 pairs.
+template <int KVT, int G, int D>
+__device__ __forceinline__ void v_cell(const uint8_t *row, int g, int lane, uint64_t *vp) {
+  using S = Shape<KVT, G, D>;
+  constexpr int DV = S::DV;
+  if constexpr (KVT == KVO_Q8_0) {
+    const int blk = (DV * lane) / 32, wo = (DV * lane) % 32;
+    const int o = (g * S::NB + blk) * 34;
+    const float d = __half2float(__ushort_as_half(*(const uint16_t *)(row + o)));
+    const uint64_t dd = pk2(d, d);
+    const int vb = o + 2 + wo;                           // even
+    if constexpr (DV == 4) {
+      const uint32_t *wp = (const uint32_t *)(row + (vb & ~3));
+      const uint32_t x = __funnelshift_r(wp[0], wp[1], (uint32_t)(vb & 3) * 8);
+      uint64_t p01, p23;
+      i8x4_to_f32x2(x, p01, p23);
+      vp[0] = fmul2(p01, dd);
+      vp[1] = fmul2(p23, dd);
+    } else {
+      const uint32_t x = *(const uint16_t *)(row + vb);
+      uint64_t p01, p23;
+      i8x4_to_f32x2(x, p01, p23);
+      vp[0] = fmul2(p01, dd);
+    }
+  } else {
+    const uint8_t *hp = row + g * S::HB + lane * DV * 2;
+    if constexpr (DV == 4) {
+      const uint2 u = *(const uint2 *)hp;
+      vp[0] = pk2(h2f(u.x & 0xffff, KVT), h2f(u.x >> 16, KVT));
+      vp[1] = pk2(h2f(u.y & 0xffff, KVT), h2f(u.y >> 16, KVT));
+    } else {
+      const uint32_t u = *(const uint32_t *)hp;
+      vp[0] = pk2(h2f(u & 0xffff, KVT), h2f(u >> 16, KVT));
     }
   }
 }
 
-// Fold the splits of one (sequence, q head): weights 2^(m_s - M) with M the
-// maximum over splits, out = acc / max(l, 1e-30).  Warp w sums the splits
+// ---------------------------------------------------------------- kernel
+
+template <int KVT, int QT, int G, int D>
+__global__ void __launch_bounds__(256, 1)
+decode_split_kernel(const DecodeArgs a, int n_stages) {
+  using S = Shape<KVT, G, D>;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t pitch = row_pitch(a.row_bytes);
+  const int64_t stage_bytes = 2 * kTile * pitch;
+  uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)g * kTile * G;  // [cell][G]
+  const int qq = lane / S::CPP;
+  const int64_t n_items = (int64_t)a.batch * a.n_splits;
+  const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
+
+  for (int64_t w = blockIdx.x; w < n_items; w += gridDim.x) {
+    const int chunk = (int)(w / a.batch), b = (int)(w % a.batch);
+    const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+    const int64_t cs = (int64_t)chunk * a.split_cells;
+    const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
+    if (cs >= ce) continue;                  // chunk beyond the context: never combined
+    const int ntiles = (int)((ce - cs + kTile - 1) / kTile);
+
+    WarpState<KVT, G, D> ws;
+    {
+      // query slice of each of the warp's heads: dims [qq*DL, qq*DL + DL)
+      const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + (size_t)g * G) * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < S::DL / 8; ++i) {
+          const uint4 u = qp[i];
+          ws.q[h][4 * i] = u.x; ws.q[h][4 * i + 1] = u.y;
+          ws.q[h][4 * i + 2] = u.z; ws.q[h][4 * i + 3] = u.w;
+          if constexpr (KVT == KVO_Q8_0) {
+            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sum += h2f(uw[e] & 0xffff, QT) + h2f(uw[e] >> 16, QT);
+          }
+        }
+        ws.qb[h] = -1152.f * sum;
+        ws.m[h] = -INFINITY;
+        ws.l[h] = 0.f;
+#pragma unroll
+        for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = 0ull;
+      }
+    }
+
+    // Device-resident chunk: the ring.  Anything else: tile by tile.
+    const bool ring = n_stages >= 2 && (ce <= a.n_vram || a.hi_device);
+    __syncthreads();                         // smem of the previous chunk fully consumed
+    if (ring) {
+      for (int t = 0; t < n_stages - 1; ++t) {
+        if (t < ntiles) {
+          const int64_t t0 = cs + (int64_t)t * kTile;
+          uint8_t *st = smem + t * stage_bytes;
+          fill_async(a, b, t0, (int)(ce - t0 < kTile ? ce - t0 : kTile), st, st + kTile * pitch, pitch, cpr);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const int64_t t0 = cs + (int64_t)t * kTile;
+      const int n = (int)(ce - t0 < kTile ? ce - t0 : kTile);
+      uint8_t *st;
+      if (ring) {
+        if (n_stages == 3) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();                     // tile t landed; tile t-1 fully consumed
+        const int tn = t + n_stages - 1;
+        if (tn < ntiles) {
+          const int64_t tn0 = cs + (int64_t)tn * kTile;
+          uint8_t *sn = smem + (tn % n_stages) * stage_bytes;
+          fill_async(a, b, tn0, (int)(ce - tn0 < kTile ? ce - tn0 : kTile), sn, sn + kTile * pitch, pitch, cpr);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        st = smem + (t % n_stages) * stage_bytes;
+      } else {
+        if (t > 0) __syncthreads();          // previous tile fully consumed
+        st = smem;
+        fill_sync(a, b, t0, n, st, st + kTile * pitch, pitch, cpr);
+        __syncthreads();
+      }
+      const uint8_t *sk = st, *sv = st + kTile * pitch;
+
+      // scores of cell `lane`, then the online softmax
+      float s[G];
+      qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, s);
+      const bool valid = lane < n;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float sv_h = valid ? s[h] : -INFINITY;
+        const float tmax = warp_max(sv_h);
+        if (tmax > ws.m[h] + 8.f) {          // warp-uniform: move the reference
+          const float alpha = exp2f(ws.m[h] - tmax);
+          const uint64_t aa = pk2(alpha, alpha);
+          ws.l[h] *= alpha;
+#pragma unroll
+          for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = fmul2(ws.acc[h][i], aa);
+          ws.m[h] = tmax;
+        }
+        const float p = valid ? exp2f(sv_h - ws.m[h]) : 0.f;
+        ws.l[h] += p;
+        pbuf[lane * G + h] = pk2(p, p);
+      }
+      __syncwarp();
+      for (int c = 0; c < n; ++c) {
+        uint64_t vp[S::DV / 2];
+        v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
+        const uint64_t *pc = pbuf + c * G;
+        uint64_t pp[G];
+#pragma unroll
+        for (int h = 0; h + 1 < G; h += 2) {
+          const ulonglong2 u = *(const ulonglong2 *)(pc + h);   // G even: 16-byte aligned
+          pp[h] = u.x; pp[h + 1] = u.y;
+        }
+        if constexpr (G & 1) pp[G - 1] = pc[G - 1];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = ffma2(pp[h], vp[i], ws.acc[h][i]);
+      }
+      __syncwarp();                          // pbuf reads done before the next tile's writes
+    }
+    if (ring) asm volatile("cp.async.wait_group 0;" ::: "memory");
+
+    // partial of this chunk: acc (this lane's dims), m, l
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float lsum = warp_sum(ws.l[h]);
+      const int qh = g * G + h;
+      const size_t pi = ((size_t)b * a.n_splits + chunk) * a.n_q_heads + qh;
+      float *pa = a.part_acc + pi * D + lane * S::DV;
+      if constexpr (S::DV == 4) {
+        float x0, x1, x2, x3;
+        upk2(ws.acc[h][0], x0, x1);
+        upk2(ws.acc[h][1], x2, x3);
+        *(float4 *)pa = make_float4(x0, x1, x2, x3);
+      } else {
+        float x0, x1;
+        upk2(ws.acc[h][0], x0, x1);
+        *(float2 *)pa = make_float2(x0, x1);
+      }
+      if (lane == 0) {
+        a.part_ml[pi * 2] = ws.m[h];
+        a.part_ml[pi * 2 + 1] = lsum;
+      }
+    }
+  }
+}
+
+// Fold the chunks of one (sequence, q head): weights 2^(m_s - M) with M the
+// maximum over chunks, out = acc / max(l, 1e-30).  Warp w sums the chunks
 // s = w, w + 8, w + 16, ... in ascending order and the 8 warp sums are added
 // in warp order: a fixed reduction tree, so the result depends on the
 // partials only (never on timing, the tier split or staging).
@@ -374,15 +568,24 @@ decode_combine_kernel(const DecodeArgs a) {
   }
 }
 
+// Shared memory of the split kernel for n_stages ring stages.
+inline size_t split_smem_bytes(const DecodeArgs &a, int n_stages) {
+  return (size_t)n_stages * 2 * kTile * row_pitch(a.row_bytes) +
+         (size_t)a.n_kv_heads * kTile * a.group * sizeof(uint64_t);
+}
+
 template <int KVT, int QT, int G, int D>
 cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
-  const size_t smem = (size_t)a.n_q_heads * D * 4 + (size_t)a.n_kv_heads * G * kTile * 4 +
-                      (size_t)2 * kTile * row_pitch<KVT>(a.row_bytes);
+  int n_stages = kMaxStages;
+  while (n_stages > 1 && split_smem_bytes(a, n_stages) > (size_t)kSmemLimit) --n_stages;
+  const size_t smem = split_smem_bytes(a, n_stages);
+  if (smem > (size_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   auto k = decode_split_kernel<KVT, QT, G, D>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_splits, a.batch);
-  k<<<grid, 32 * a.n_kv_heads, smem, st>>>(a);
+  const int64_t items = (int64_t)a.batch * a.n_splits;
+  const int64_t grid = items < num_sms() ? items : num_sms();
+  k<<<(unsigned)grid, 32 * a.n_kv_heads, smem, st>>>(a, n_stages);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
@@ -395,8 +598,11 @@ cudaError_t launch_g(const DecodeArgs &a, cudaStream_t st) {
   return launch_d<KVT, QT, G, 64>(a, st);
 }
 
-template <int KVT, int QT>
-cudaError_t launch_q(const DecodeArgs &a, cudaStream_t st) {
+// The query type is the cache's 16-bit type (fp16 for a q8_0 cache); the
+// entry points reject other pairs.
+template <int KVT>
+cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
+  constexpr int QT = KVT == KVO_BF16 ? KVO_BF16 : KVO_F16;
   switch (a.group) {
     case 1: return launch_g<KVT, QT, 1>(a, st);
     case 2: return launch_g<KVT, QT, 2>(a, st);
@@ -407,12 +613,6 @@ cudaError_t launch_q(const DecodeArgs &a, cudaStream_t st) {
     case 7: return launch_g<KVT, QT, 7>(a, st);
     default: return launch_g<KVT, QT, 8>(a, st);
   }
-}
-
-template <int KVT>
-cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
-  if (a.q_dtype == KVO_BF16) return launch_q<KVT, KVO_BF16>(a, st);
-  return launch_q<KVT, KVO_F16>(a, st);
 }
 
 }  // namespace dec

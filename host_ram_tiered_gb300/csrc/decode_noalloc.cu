@@ -65,6 +65,8 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
                 (long long)group, (long long)n_kv_heads, (long long)head_dim);
   const int64_t rb = row_bytes_of(kv_dtype, n_kv_heads, head_dim);
   if (rb < 0) return fail(KVO_ERR_UNSUPPORTED, "%s: kv dtype", fn);
+  if (q_dtype != (kv_dtype == KVO_BF16 ? KVO_BF16 : KVO_F16))
+    return fail(KVO_ERR_UNSUPPORTED, "%s: q dtype must be the cache's 16-bit type (f16 for q8_0)", fn);
   if (rb % 16) return fail(KVO_ERR_ALIGN, "%s: cell row bytes %% 16 != 0", fn);
   if (!out || !q || !ctx_len) return fail(KVO_ERR_ARG, "%s: NULL q/out/ctx_len", fn);
   if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "%s: q/out alignment", fn);

@@ -343,6 +343,8 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
                 (long long)group, (long long)n_kv_heads, (long long)head_dim);
   const int64_t rb = kv_row_bytes(kv_dtype, n_kv_heads, head_dim);
   if (rb < 0) return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_decode_tiered: kv dtype");
+  if (q_dtype != (kv_dtype == KVO_BF16 ? KVO_BF16 : KVO_F16))
+    return fail(KVO_ERR_UNSUPPORTED, "kvo_attn_decode_tiered: q dtype must be the cache's 16-bit type (f16 for q8_0)");
   if (rb % 16) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: cell row bytes %% 16 != 0");
   if (!out || !q || !ctx_len) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: NULL q/out/ctx_len");
   if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: q/out alignment");

@@ -207,16 +207,19 @@ int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
  * (kv head g = h / (n_q_heads / n_kv_heads)):
  *     out[b][h] = sum_j softmax_j(scale * q[b][h] . k[b][j][g]) v[b][j][g]
  * over cells j < ctx_len[b], computed as split-K flash-decoding: fixed
- * cell ranges (a function of max_ctx and batch only) give partial
- * (m, l, acc) in fp32, combined in ascending split order.  An empty context
- * gives 0.
+ * cell ranges (a function of max_ctx, batch and the device's SM count only)
+ * give partial (m, l, acc) in fp32, combined in a fixed order.  Products
+ * q * k are exact (16-bit x 16-bit, or 16-bit x int8) and summed in fp32;
+ * P * V runs in fp32.  An empty context gives 0.
  *
  * Cell row j of sequence b (n_kv_heads * head_dim values, or n_kv_heads *
  * head_dim/32 q8_0 blocks):
  *     j <  N: k_vram + (b * vram_seq_stride_rows + j)     * row_bytes
  *     j >= N: k_host + (b * host_seq_stride_rows + j - N) * row_bytes
  * (the same for V).  k_vram/v_vram may be NULL when N == 0.
- * q: device [batch][n_q_heads][head_dim] of q_dtype (F16 or BF16).
+ * q: device [batch][n_q_heads][head_dim] of q_dtype: the cache's 16-bit
+ *   type for an F16 or BF16 cache, F16 for a Q8_0 cache (other pairs return
+ *   KVO_ERR_UNSUPPORTED).
  * kv_dtype: F16, BF16 or Q8_0.  head_dim: 64 or 128.  Group size
  *   n_q_heads / n_kv_heads: 1..8.  n_kv_heads <= 8.  row_bytes and every
  *   base pointer 16-byte aligned.

@@ -94,11 +94,13 @@ def test_group_sizes_and_head_dims(hq, hkv, d, kvdt):
     g = synth.rng(8, hq * 1000 + d)
     L = 517
     k, v = cells(L, hkv, d, kvdt, g)
-    q, qd = _q(1, hq, d, "f16", g)
+    # q is the cache's 16-bit type (fp16 for a q8_0 cache)
+    bf = kvdt == oracle.BF16
+    q, qd = _q(1, hq, d, "bf16" if bf else "f16", g)
     s = scale_for(d)
     tc = Tiered(k, v, 200)
-    out = run_decode(tc, qd, kvo.F16, hq, hkv, d, kvdt, _ctx([L]), s, staging=True)
-    ref = _oracle(tc, q, oracle.F16, hq, hkv, d, kvdt, [L], s)
+    out = run_decode(tc, qd, kvo.BF16 if bf else kvo.F16, hq, hkv, d, kvdt, _ctx([L]), s, staging=True)
+    ref = _oracle(tc, q, oracle.BF16 if bf else oracle.F16, hq, hkv, d, kvdt, [L], s)
     assert normwise_rel_err(out, ref) <= REL_TOL
 
 
@@ -120,6 +122,8 @@ def test_argument_errors():
         (dict(n_q_heads=18), -4),                     # group 9
         (dict(head_dim=96), -4),
         (dict(q_dtype=kvo.Q8_0), -4),
+        (dict(q_dtype=kvo.BF16), -4),                 # q must be the cache's 16-bit type
+        (dict(kv_dtype=kvo.BF16), -4),
     ]
     base = dict(q=qd, q_dtype=kvo.F16, batch=1, n_q_heads=hq, n_kv_heads=hkv, head_dim=d,
                 k_vram=tc.k_head, v_vram=tc.v_head, vram_seq_stride_rows=32, k_host=tc.k_tail,
