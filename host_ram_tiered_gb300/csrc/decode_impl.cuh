@@ -16,8 +16,10 @@
 //   * a chunk with host-resident rows is filled tile by tile with 16-byte
 //     loads through the host mapping, every thread keeping 8 in flight.
 //
-// Per tile, warp g (kv head g) computes the scores of the tile's 32 cells
-// for its G query heads, an online softmax in the log2 domain, and P*V:
+// Per tile, each warp computes, for one kv head and G of its query heads
+// (all of them, or an equal share when fewer than 8 kv heads leave room for
+// more warps), the scores of the tile's 32 cells, an online softmax in the
+// log2 domain, and P*V:
 //   * QK: lane = (quarter or eighth of the head dims, cell).  The lane's
 //     query slice lives in registers as fp16/bf16 pairs for the whole chunk;
 //     each pass takes CPP cells, and the LPC partial dot products of a cell
@@ -362,15 +364,24 @@ __device__ __forceinline__ void v_cell(const uint8_t *row, int g, int lane, uint
 
 // ---------------------------------------------------------------- kernel
 
+// Up to 16 warps when a warp holds at most two query heads (few registers),
+// else up to 8.
+template <int G>
+constexpr int max_decode_threads() { return G <= 2 ? 512 : 256; }
+
 template <int KVT, int QT, int G, int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(max_decode_threads<G>(), 1)
 decode_split_kernel(const DecodeArgs a, int n_stages) {
   using S = Shape<KVT, G, D>;
   extern __shared__ __align__(16) uint8_t smem[];
-  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Warp w serves kv head g = w / wph and its query heads h0 .. h0 + G - 1
+  // (G = heads per warp; wph warps share a kv head when the group allows).
+  const int w_id = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wph = a.group / G;
+  const int g = w_id / wph, h0 = g * a.group + (w_id % wph) * G;
   const int64_t pitch = row_pitch(a.row_bytes);
   const int64_t stage_bytes = 2 * kTile * pitch;
-  uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)g * kTile * G;  // [cell][G]
+  uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)w_id * kTile * G;  // [cell][G]
   const int qq = lane / S::CPP;
   const int64_t n_items = (int64_t)a.batch * a.n_splits;
   const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
@@ -386,7 +397,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     WarpState<KVT, G, D> ws;
     {
       // query slice of each of the warp's heads: dims [qq*DL, qq*DL + DL)
-      const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + (size_t)g * G) * D;
+      const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + (size_t)h0) * D;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
@@ -492,7 +503,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float lsum = warp_sum(ws.l[h]);
-      const int qh = g * G + h;
+      const int qh = h0 + h;
       const size_t pi = ((size_t)b * a.n_splits + chunk) * a.n_q_heads + qh;
       float *pa = a.part_acc + pi * D + lane * S::DV;
       if constexpr (S::DV == 4) {
@@ -585,7 +596,7 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.batch * a.n_splits;
   const int64_t grid = items < num_sms() ? items : num_sms();
-  k<<<(unsigned)grid, 32 * a.n_kv_heads, smem, st>>>(a, n_stages);
+  k<<<(unsigned)grid, 32 * a.n_kv_heads * (a.group / G), smem, st>>>(a, n_stages);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
@@ -598,12 +609,25 @@ cudaError_t launch_g(const DecodeArgs &a, cudaStream_t st) {
   return launch_d<KVT, QT, G, 64>(a, st);
 }
 
+// Warps per kv head: the largest power of two w dividing the group with
+// n_kv_heads * w <= 8 warps, or <= 16 warps when each warp is then left with
+// at most two query heads; each warp takes group / w query heads.
+inline int warps_per_kv_head(const DecodeArgs &a) {
+  int w = 1;
+  while (a.group % (w * 2) == 0) {
+    const int warps = a.n_kv_heads * w * 2, heads = a.group / (w * 2);
+    if (warps > (heads <= 2 ? 16 : 8)) break;
+    w *= 2;
+  }
+  return w;
+}
+
 // The query type is the cache's 16-bit type (fp16 for a q8_0 cache); the
 // entry points reject other pairs.
 template <int KVT>
 cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
   constexpr int QT = KVT == KVO_BF16 ? KVO_BF16 : KVO_F16;
-  switch (a.group) {
+  switch (a.group / warps_per_kv_head(a)) {
     case 1: return launch_g<KVT, QT, 1>(a, st);
     case 2: return launch_g<KVT, QT, 2>(a, st);
     case 3: return launch_g<KVT, QT, 3>(a, st);
