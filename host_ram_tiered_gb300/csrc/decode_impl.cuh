@@ -381,7 +381,10 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   const int g = w_id / wph, h0 = g * a.group + (w_id % wph) * G;
   const int64_t pitch = row_pitch(a.row_bytes);
   const int64_t stage_bytes = 2 * kTile * pitch;
-  uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)w_id * kTile * G;  // [cell][G]
+  // weights (p, p) of the tile: [cell][GP], GP = G rounded up to even so
+  // that every cell's entries start on a 16-byte boundary
+  constexpr int GP = (G + 1) & ~1;
+  uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)w_id * kTile * GP;
   const int qq = lane / S::CPP;
   const int64_t n_items = (int64_t)a.batch * a.n_splits;
   const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
@@ -476,17 +479,17 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         }
         const float p = valid ? exp2f(sv_h - ws.m[h]) : 0.f;
         ws.l[h] += p;
-        pbuf[lane * G + h] = pk2(p, p);
+        pbuf[lane * GP + h] = pk2(p, p);
       }
       __syncwarp();
       for (int c = 0; c < n; ++c) {
         uint64_t vp[S::DV / 2];
         v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
-        const uint64_t *pc = pbuf + c * G;
+        const uint64_t *pc = pbuf + c * GP;
         uint64_t pp[G];
 #pragma unroll
         for (int h = 0; h + 1 < G; h += 2) {
-          const ulonglong2 u = *(const ulonglong2 *)(pc + h);   // G even: 16-byte aligned
+          const ulonglong2 u = *(const ulonglong2 *)(pc + h);   // h and GP even: 16-byte aligned
           pp[h] = u.x; pp[h + 1] = u.y;
         }
         if constexpr (G & 1) pp[G - 1] = pc[G - 1];
@@ -580,16 +583,17 @@ decode_combine_kernel(const DecodeArgs a) {
 }
 
 // Shared memory of the split kernel for n_stages ring stages.
-inline size_t split_smem_bytes(const DecodeArgs &a, int n_stages) {
-  return (size_t)n_stages * 2 * kTile * row_pitch(a.row_bytes) +
-         (size_t)a.n_kv_heads * kTile * a.group * sizeof(uint64_t);
+inline size_t split_smem_bytes(const DecodeArgs &a, int g_per_warp, int n_stages) {
+  const int warps = a.n_kv_heads * (a.group / g_per_warp);
+  const int gp = (g_per_warp + 1) & ~1;
+  return (size_t)n_stages * 2 * kTile * row_pitch(a.row_bytes) + (size_t)warps * kTile * gp * sizeof(uint64_t);
 }
 
 template <int KVT, int QT, int G, int D>
 cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   int n_stages = kMaxStages;
-  while (n_stages > 1 && split_smem_bytes(a, n_stages) > (size_t)kSmemLimit) --n_stages;
-  const size_t smem = split_smem_bytes(a, n_stages);
+  while (n_stages > 1 && split_smem_bytes(a, G, n_stages) > (size_t)kSmemLimit) --n_stages;
+  const size_t smem = split_smem_bytes(a, G, n_stages);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   auto k = decode_split_kernel<KVT, QT, G, D>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
