@@ -548,8 +548,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append) "
-                         "(default all)")
+                    help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append), "
+                         "c3vram (the 184,320-cell all-VRAM decode alone; not in 'all') (default all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -632,6 +632,16 @@ def main(argv=None):
                 results[f"c3_q8_0_decode_L{L}_all_vram"] = {
                     "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
                     "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
+        del st3
+    if "c3vram" in rows and "c3" not in rows:
+        st3 = c3_setup()
+        L = max(C3_LS)
+        tot, _ = timer.run(lambda: c3_run(st3, L, 0, all_vram=True), K, W)
+        us_r = max_over_ranks(tot, world) / K * 1e3
+        db_r = L * 2 * C3_HKV * (C3_D // 32) * 34
+        results[f"c3_q8_0_decode_L{L}_all_vram"] = {
+            "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
+            "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
         del st3
     # ---- C1 tiny (latency-bound: microseconds, fractions not meaningful)
     if "c1" in rows:
@@ -742,17 +752,31 @@ def main(argv=None):
     return 0
 
 
+def decode_source_sha256():
+    """sha256 of the decode kernel source (the kernels the headline times)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode_impl.cuh", "decode.cu"):
+        with open(os.path.join(ROOT, "host_ram_tiered_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def profiled_traffic():
     """DRAM bytes per launch of the headline decode kernel, as recorded by the
-    committed ncu summary (None if the summary is missing)."""
+    committed ncu summary; None if the summary is missing or was taken on a
+    different decode kernel source than the one built now."""
     path = os.path.join(ROOT, "profiles", "decode_split_kernel_c3_headline.md")
+    traffic = sha = None
     try:
         for line in open(path):
             if line.startswith("traffic_bytes_per_launch:"):
-                return int(line.split(":")[1])
+                traffic = int(line.split(":")[1])
+            elif line.startswith("decode_source_sha256:"):
+                sha = line.split(":")[1].strip()
     except OSError:
-        pass
-    return None
+        return None
+    return traffic if sha == decode_source_sha256() else None
 
 
 def gpu_launch_count(K, rows):
@@ -762,6 +786,8 @@ def gpu_launch_count(K, rows):
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
     if "c3" in rows:
         n += 2 * K * (3 * 2 * 2 - 1 + 3)           # 11 tiered variants + 3 all-VRAM, 2 kernels each
+    elif "c3vram" in rows:
+        n += 2 * K                                 # the 184,320-cell all-VRAM decode
     if "c1" in rows:
         n += K * 2 + K * 2 * 2                     # swap both ways; decode direct + staged (2 kernels)
     if "c2" in rows:
