@@ -77,6 +77,10 @@ def lib():
         L.orc_copy_plan.argtypes = [vp] * 6 + [i64, ctypes.c_int, vp, vp, vp, i64]
         L.orc_copy_plan.restype = i64
         L.orc_fragment_ptrs.argtypes = [vp, vp, i64, vp, vp, vp, i64, vp, vp, vp]
+        L.orc_staging_worthwhile.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+        L.orc_staging_worthwhile.restype = ctypes.c_int
+        L.orc_attn_sparse_rows.argtypes = [vp, vp, ctypes.c_int, i64, i64, i64, vp, i64, vp, i64, i64,
+                                           vp, ctypes.c_int, i64, dbl, vp]
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
         _lib = L
@@ -229,6 +233,28 @@ def attn_decode(cache: Cache, q: np.ndarray, q_dtype, batch, n_q_heads, ctx_len,
     out = np.empty((batch, n_q_heads, cache.head_dim), np.float64)
     lib().orc_attn_decode(ctypes.byref(cache), _ptr(q), q_dtype, batch, n_q_heads, _ptr(ctx),
                           scale, _ptr(out))
+    return out
+
+
+def staging_worthwhile(rows, k_pad, num_pages_used, page_size, enabled=True) -> bool:
+    return bool(lib().orc_staging_worthwhile(rows, k_pad, num_pages_used, page_size, int(enabled)))
+
+
+def attn_sparse_rows(k_pages: np.ndarray, v_pages: np.ndarray, dtype, page_size, n_kv_heads, head_dim,
+                     block_table, num_pages_used, indices, q: np.ndarray, q_dtype, n_q_heads, scale):
+    """k_pages / v_pages: raw bytes [pages][page_size][n_kv_heads][head_dim];
+    indices: int32 [rows][k_pad] (negative = padding); q: uint16 [rows][n_q_heads][head_dim].
+    Returns float64 [rows][n_q_heads][head_dim]."""
+    kp = np.ascontiguousarray(k_pages).view(np.uint8)
+    vp_ = np.ascontiguousarray(v_pages).view(np.uint8)
+    bt = np.ascontiguousarray(block_table, np.int32)
+    idx = np.ascontiguousarray(indices, np.int32)
+    rows, k_pad = idx.shape
+    q = np.ascontiguousarray(q, np.uint16)
+    out = np.empty((rows, n_q_heads, head_dim), np.float64)
+    lib().orc_attn_sparse_rows(_ptr(kp), _ptr(vp_), dtype, page_size, n_kv_heads, head_dim, _ptr(bt),
+                               num_pages_used, _ptr(idx), rows, k_pad, _ptr(q), q_dtype, n_q_heads,
+                               scale, _ptr(out))
     return out
 
 

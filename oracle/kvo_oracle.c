@@ -273,6 +273,69 @@ void orc_attn_prefill(const orc_cache *c, const uint16_t *q, int q_dtype,
   }
 }
 
+int orc_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
+                           int64_t page_size, int enabled) {
+  return enabled && rows * k_pad > 2 * num_pages_used * page_size;
+}
+
+/* Row of position p in the paged planes, or NULL when p is padding. */
+static const uint8_t *paged_row(const uint8_t *pages, int64_t p, int64_t page_size,
+                                const int32_t *block_table, int64_t num_pages_used,
+                                int64_t row_bytes) {
+  if (p < 0 || p >= num_pages_used * page_size) return NULL;
+  return pages + ((int64_t)block_table[p / page_size] * page_size + p % page_size) * row_bytes;
+}
+
+void orc_attn_sparse_rows(const uint8_t *k_pages, const uint8_t *v_pages,
+                          int dtype, int64_t page_size, int64_t n_kv_heads,
+                          int64_t head_dim, const int32_t *block_table,
+                          int64_t num_pages_used, const int32_t *indices,
+                          int64_t rows, int64_t k_pad, const uint16_t *q,
+                          int q_dtype, int64_t n_q_heads, double scale,
+                          double *out) {
+  int64_t D = head_dim, group = n_q_heads / n_kv_heads;
+  int64_t rb = orc_row_bytes(dtype, n_kv_heads, head_dim);
+  int64_t task;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (task = 0; task < rows * n_q_heads; ++task) {
+    int64_t r = task / n_q_heads, h = task % n_q_heads, g = h / group, k, d;
+    const int32_t *sel = indices + r * k_pad;
+    double qd[ORC_MAX_D], kd[ORC_MAX_D], vd[ORC_MAX_D];
+    double mx = -INFINITY, sum = 0.0;
+    double *o = out + task * D;
+    load_q(q + task * D, q_dtype, D, qd);
+    for (d = 0; d < D; ++d) o[d] = 0.0;
+    /* pass 1: the maximum logit over the selected positions */
+    for (k = 0; k < k_pad; ++k) {
+      const uint8_t *kr = paged_row(k_pages, sel[k], page_size, block_table, num_pages_used, rb);
+      double s = 0.0;
+      if (!kr) continue;
+      orc_load_head(kr, dtype, D, g, kd);
+      for (d = 0; d < D; ++d) s += qd[d] * kd[d];
+      s *= scale;
+      if (s > mx) mx = s;
+    }
+    /* pass 2: exp-weights and the weighted sum of V */
+    for (k = 0; k < k_pad; ++k) {
+      const uint8_t *kr = paged_row(k_pages, sel[k], page_size, block_table, num_pages_used, rb);
+      const uint8_t *vr = paged_row(v_pages, sel[k], page_size, block_table, num_pages_used, rb);
+      double s = 0.0, p;
+      if (!kr) continue;
+      orc_load_head(kr, dtype, D, g, kd);
+      orc_load_head(vr, dtype, D, g, vd);
+      for (d = 0; d < D; ++d) s += qd[d] * kd[d];
+      s *= scale;
+      p = exp(s - mx);
+      sum += p;
+      for (d = 0; d < D; ++d) o[d] += p * vd[d];
+    }
+    if (sum < 1e-30) sum = 1e-30;
+    for (d = 0; d < D; ++d) o[d] /= sum;
+  }
+}
+
 uint16_t orc_float_to_half_bits(float x) {
   /* decompose |x| = m * 2^e exactly in binary64, then round m to the
    * binary16 grid at that exponent */

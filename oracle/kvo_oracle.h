@@ -28,7 +28,10 @@
  * numpy matmuls, and against closed forms (one cell gives v, q = 0 gives the
  * mean of v, a constant-per-head V gives the kv-head index, the causal
  * boundary gives pos/2 for V = position); the fold against the one-shot
- * softmax over the union of buckets.
+ * softmax over the union of buckets; the sparse-row attention against a
+ * numpy/scipy gather-and-softmax (padding, order, duplicates, one selection
+ * gives v, every earlier position gives the causal prefill row); the staging
+ * rule against the page's own worked example.
  */
 #ifndef KVO_ORACLE_H
 #define KVO_ORACLE_H
@@ -150,6 +153,32 @@ void orc_attn_decode(const orc_cache *c, const uint16_t *q, int q_dtype,
 void orc_attn_prefill(const orc_cache *c, const uint16_t *q, int q_dtype,
                       int64_t rows, int64_t q_pos0, int64_t n_q_heads,
                       int64_t ctx_len, double scale, double *out);
+
+/* ExLlamaV3 qsa-kv-offload patch, qsa_staging_worthwhile: staging the page
+ * range through the VRAM arena pays when the direct gather would read more
+ * cache positions (rows * k_pad, every row its own selection) than twice the
+ * positions staging reads once (num_pages_used * page_size).  Returns 1 or 0
+ * (0 as well when staging is disabled). */
+int orc_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
+                           int64_t page_size, int enabled);
+
+/* ExLlamaV3 qsa-kv-offload patch, qsa_sparse_attend_rows(_staged): query
+ * row r (n_q_heads heads of head_dim, fp16 or bf16) attends to the cache
+ * positions indices[r][0 .. k_pad) that are >= 0 and below
+ * num_pages_used * page_size; the others are padding.  Position p is slot
+ * p % page_size of page block_table[p / page_size] of the paged planes
+ * k_pages / v_pages ([pages][page_size][n_kv_heads][head_dim], fp16 or bf16),
+ * and q head h reads kv head h / (n_q_heads / n_kv_heads):
+ *     out[r][h] = sum_p softmax_p(scale * q[r][h] . k_p) v_p
+ * over the selected positions (a position listed twice counts twice).  A row
+ * with no selection gives 0 (acc / max(l, 1e-30)). */
+void orc_attn_sparse_rows(const uint8_t *k_pages, const uint8_t *v_pages,
+                          int dtype, int64_t page_size, int64_t n_kv_heads,
+                          int64_t head_dim, const int32_t *block_table,
+                          int64_t num_pages_used, const int32_t *indices,
+                          int64_t rows, int64_t k_pad, const uint16_t *q,
+                          int q_dtype, int64_t n_q_heads, double scale,
+                          double *out);
 
 /* IEEE binary32 -> binary16 bits, round to nearest, ties to even (with
  * subnormals, overflow to infinity, NaN kept quiet). */

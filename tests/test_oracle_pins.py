@@ -473,3 +473,108 @@ def test_fragment_ptrs_broadcast_block_major():
             i = b * 3 + f
             assert os_[i] == sb[b] + np.uint64(fs[f]) and od[i] == db[b] + np.uint64(fd[f])
             assert oz[i] == fz[f]
+
+
+# ---------------------------------------------------------------- sparse rows (QSA staged prefill)
+
+def test_staging_policy_golden_cases():
+    path = __file__.replace("test_oracle_pins.py", "golden/staging_policy.txt")
+    cases = [list(map(int, ln.split())) for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    assert cases
+    for rows, k_pad, npu, ps, want in cases:
+        assert oracle.staging_worthwhile(rows, k_pad, npu, ps) == bool(want)
+        assert not oracle.staging_worthwhile(rows, k_pad, npu, ps, enabled=False)
+    # the boundary is strict: rows * k_pad == 2 * pages * page_size stays direct
+    assert not oracle.staging_worthwhile(2, 64, 1, 64)
+    assert oracle.staging_worthwhile(2, 65, 1, 64)
+
+
+def _paged(pages, ps, H, D, dtype, g):
+    raw_k, raw_v = _cells(pages * ps, H, D, dtype, g)
+    return raw_k.reshape(pages, ps, -1), raw_v.reshape(pages, ps, -1)
+
+
+def _sparse_ref(kp, vp, dtype, ps, H, D, bt, npu, idx, Q, Hq, scale):
+    """numpy/scipy brute force: gather each row's selected positions by page
+    table, softmax over them, weight V."""
+    K = _decode_values(kp.reshape(-1, kp.shape[-1]), dtype, H, D).reshape(kp.shape[0], ps, H, D)
+    V = _decode_values(vp.reshape(-1, vp.shape[-1]), dtype, H, D).reshape(kp.shape[0], ps, H, D)
+    G = Hq // H
+    out = np.zeros((idx.shape[0], Hq, D))
+    for r in range(idx.shape[0]):
+        pos = [int(p) for p in idx[r] if 0 <= p < npu * ps]
+        if not pos:
+            continue
+        pg = np.array([bt[p // ps] for p in pos])
+        sl = np.array([p % ps for p in pos])
+        for h in range(Hq):
+            kk = K[pg, sl, h // G, :]
+            vv = V[pg, sl, h // G, :]
+            p = scipy.special.softmax(scale * (kk @ Q[r, h]))
+            out[r, h] = p @ vv
+    return out
+
+
+@pytest.mark.parametrize("dtype", [oracle.F16, oracle.BF16])
+def test_sparse_rows_match_scipy_bruteforce(dtype):
+    g = synth.rng(61, dtype)
+    pages, ps, H, D, Hq, rows, k_pad, npu = 7, 4, 2, 32, 6, 5, 12, 6
+    kp, vp = _paged(pages, ps, H, D, dtype, g)
+    bt = g.permutation(pages).astype(np.int32)
+    idx = g.integers(-1, npu * ps + 3, size=(rows, k_pad)).astype(np.int32)   # -1 pads, some past the pages
+    idx[0, :] = -1                                                          # a row with no selection
+    idx[1, 1:] = -1                                                         # a row with one
+    qname = "bf16" if dtype == oracle.BF16 else "f16"
+    q = synth.normal_bits((rows, Hq, D), qname, g)
+    scale = 1 / math.sqrt(D)
+    got = oracle.attn_sparse_rows(kp, vp, dtype, ps, H, D, bt, npu, idx, q, dtype, Hq, scale)
+    Q = _decode_values(q.reshape(rows, -1).view(np.uint8), dtype, Hq, D)
+    ref = _sparse_ref(kp, vp, dtype, ps, H, D, bt, npu, idx, Q, Hq, scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    assert np.all(got[0] == 0.0)
+    j = int(idx[1, 0])
+    if 0 <= j < npu * ps:                                                   # one selection: o = v exactly
+        V = _decode_values(vp.reshape(-1, vp.shape[-1]), dtype, H, D).reshape(pages, ps, H, D)
+        for h in range(Hq):
+            assert np.array_equal(got[1, h], V[bt[j // ps], j % ps, h // (Hq // H)])
+
+
+def test_sparse_rows_padding_order_and_duplicates():
+    g = synth.rng(62)
+    pages, ps, H, D, Hq, k_pad, npu = 6, 8, 2, 64, 4, 20, 6
+    kp, vp = _paged(pages, ps, H, D, oracle.F16, g)
+    bt = g.permutation(pages).astype(np.int32)
+    base = g.choice(npu * ps, size=k_pad, replace=False).astype(np.int32)
+    q = synth.normal_bits((1, Hq, D), "f16", g)
+    scale = 0.125
+    a = oracle.attn_sparse_rows(kp, vp, oracle.F16, ps, H, D, bt, npu, base[None], q, oracle.F16, Hq, scale)
+    padded = np.concatenate([g.permutation(base), np.full(12, -1, np.int32)])[None]
+    b = oracle.attn_sparse_rows(kp, vp, oracle.F16, ps, H, D, bt, npu, padded, q, oracle.F16, Hq, scale)
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-14)
+    # a position listed twice weighs twice: equal to duplicating it in the brute force
+    dup = np.concatenate([base, base[:1]])[None]
+    c = oracle.attn_sparse_rows(kp, vp, oracle.F16, ps, H, D, bt, npu, dup, q, oracle.F16, Hq, scale)
+    Q = _decode_values(q.reshape(1, -1).view(np.uint8), oracle.F16, Hq, D)
+    ref = _sparse_ref(kp, vp, oracle.F16, ps, H, D, bt, npu, dup, Q, Hq, scale)
+    np.testing.assert_allclose(c, ref, rtol=1e-12, atol=1e-13)
+    assert np.abs(c - a).max() > 1e-6
+
+
+def test_sparse_rows_over_all_earlier_positions_is_causal_prefill():
+    # identity page table, row i selects every position <= its own: the causal prefill row
+    g = synth.rng(63)
+    pages, ps, H, D, Hq, rows = 5, 8, 2, 32, 4, 6
+    L = pages * ps
+    kp, vp = _paged(pages, ps, H, D, oracle.F16, g)
+    pos0 = L - rows
+    idx = np.full((rows, L), -1, np.int32)
+    for i in range(rows):
+        idx[i, : pos0 + i + 1] = np.arange(pos0 + i + 1)
+    q = synth.normal_bits((rows, Hq, D), "f16", g)
+    got = oracle.attn_sparse_rows(kp, vp, oracle.F16, ps, H, D, np.arange(pages, dtype=np.int32), pages,
+                                  idx, q, oracle.F16, Hq, 0.2)
+    k = np.ascontiguousarray(kp.reshape(L, -1))
+    v = np.ascontiguousarray(vp.reshape(L, -1))
+    c, keep = _tiered(k, v, L, oracle.F16, H, D)
+    ref = oracle.attn_prefill(c, q, oracle.F16, rows, pos0, Hq, L, 0.2)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-14)
