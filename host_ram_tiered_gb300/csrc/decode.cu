@@ -4,7 +4,7 @@
 
 namespace kvo {
 namespace dec {
-template <int KVT> cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st);
+template <int KVT, bool SP> cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st);
 constexpr int kMaxChunkTiles = 20;   // chunks of at most 640 cells
 }  // namespace dec
 
@@ -43,9 +43,9 @@ size_t decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t head_dim
 
 int launch_decode(const DecodeArgs &a, cudaStream_t st) {
   cudaError_t e;
-  if (a.kv_dtype == KVO_Q8_0) e = dec::launch_kv<KVO_Q8_0>(a, st);
-  else if (a.kv_dtype == KVO_BF16) e = dec::launch_kv<KVO_BF16>(a, st);
-  else e = dec::launch_kv<KVO_F16>(a, st);
+  if (a.kv_dtype == KVO_Q8_0) e = dec::launch_kv<KVO_Q8_0, false>(a, st);
+  else if (a.kv_dtype == KVO_BF16) e = dec::launch_kv<KVO_BF16, false>(a, st);
+  else e = dec::launch_kv<KVO_F16, false>(a, st);
   return cuda_status(e, "decode kernel launch");
 }
 

@@ -219,6 +219,50 @@ __device__ __forceinline__ void fill_sync(const DecodeArgs &a, int b, int64_t c0
   }
 }
 
+// ---------------------------------------------------------------- sparse rows (selection mode)
+
+// Row of cache position j in selection mode, or null when j is padding
+// (outside [win_lo, win_hi)) or its page-table entry is out of range.
+__device__ __forceinline__ const uint8_t *sparse_row(const DecodeArgs &a, int64_t j, bool is_v) {
+  if (j < a.win_lo || j >= a.win_hi) return nullptr;
+  if (a.sparse_staged) return (is_v ? a.v_lo : a.k_lo) + (j - a.win_lo) * a.row_bytes;
+  const int64_t page = a.block_table[j / a.page_size];
+  if (page < 0 || page >= a.n_pages_total) return nullptr;
+  return (is_v ? a.v_hi : a.k_hi) + (page * a.page_size + j % a.page_size) * a.row_bytes;
+}
+
+// Slots [s0, s0 + n) of work row b's selection list, K and V, into one stage.
+// Warp w takes slots w, w + warps, ...; a padding slot gets a zero V row (its
+// weight is 0 and must meet finite values).  Async: 16-byte cp.async copies
+// (device-resident arena); else 16-byte loads through the mapping.
+template <bool ASYNC>
+__device__ __forceinline__ void fill_sparse(const DecodeArgs &a, int b, int64_t s0, int n,
+                                            uint8_t *sk, uint8_t *sv, int64_t pitch) {
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cpr = (int)(a.row_bytes >> 4);
+  for (int r = warp; r < n; r += warps) {
+    const int64_t j = a.indices[(int64_t)b * a.max_ctx + s0 + r];
+    const int4 *ks = (const int4 *)sparse_row(a, j, false);
+    const int4 *vs = (const int4 *)sparse_row(a, j, true);
+    if (!ks && lane == 0 && j >= a.win_lo && j < a.win_hi) atomicOr(a.err, kErrPageTable);
+    uint8_t *kd = sk + r * pitch, *vd = sv + r * pitch;
+    for (int ch = lane; ch < cpr; ch += 32) {
+      if (!ks) {
+        *(int4 *)(vd + ch * 16) = make_int4(0, 0, 0, 0);
+      } else if constexpr (ASYNC) {
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(kd + ch * 16)), "l"(ks + ch)
+                     : "memory");
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(vd + ch * 16)), "l"(vs + ch)
+                     : "memory");
+      } else {
+        const int4 kx = ks[ch], vx = vs[ch];
+        *(int4 *)(kd + ch * 16) = kx;
+        *(int4 *)(vd + ch * 16) = vx;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- per-warp state
 
 template <int KVT, int G, int D>
@@ -369,7 +413,9 @@ __device__ __forceinline__ void v_cell(const uint8_t *row, int g, int lane, uint
 template <int G>
 constexpr int max_decode_threads() { return G <= 2 ? 512 : 256; }
 
-template <int KVT, int QT, int G, int D>
+// SP: selection mode (QSA sparse rows): cell k of work row b is cache
+// position a.indices[b * a.max_ctx + k], padding masked out.
+template <int KVT, int QT, int G, int D, bool SP>
 __global__ void __launch_bounds__(max_decode_threads<G>(), 1)
 decode_split_kernel(const DecodeArgs a, int n_stages) {
   using S = Shape<KVT, G, D>;
@@ -391,7 +437,17 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
 
   for (int64_t w = blockIdx.x; w < n_items; w += gridDim.x) {
     const int chunk = (int)(w / a.batch), b = (int)(w % a.batch);
-    const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+    int64_t ctx, sel0 = 0;                   // selection mode: row b's slots sel0 .. sel0 + ctx
+    if constexpr (SP) {
+      ctx = a.max_ctx;
+      if (a.offs) {
+        const int32_t *ob = a.offs + (int64_t)b * a.offs_stride + a.bucket;
+        sel0 = ob[0];
+        ctx = ob[1] - ob[0];
+      }
+    } else {
+      ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+    }
     const int64_t cs = (int64_t)chunk * a.split_cells;
     const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
     if (cs >= ce) continue;                  // chunk beyond the context: never combined
@@ -425,14 +481,16 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     }
 
     // Device-resident chunk: the ring.  Anything else: tile by tile.
-    const bool ring = n_stages >= 2 && (ce <= a.n_vram || a.hi_device);
+    const bool ring = n_stages >= 2 && (SP ? a.sparse_staged != 0 : (ce <= a.n_vram || a.hi_device));
     __syncthreads();                         // smem of the previous chunk fully consumed
     if (ring) {
       for (int t = 0; t < n_stages - 1; ++t) {
         if (t < ntiles) {
           const int64_t t0 = cs + (int64_t)t * kTile;
           uint8_t *st = smem + t * stage_bytes;
-          fill_async(a, b, t0, (int)(ce - t0 < kTile ? ce - t0 : kTile), st, st + kTile * pitch, pitch, cpr);
+          const int nt = (int)(ce - t0 < kTile ? ce - t0 : kTile);
+          if constexpr (SP) fill_sparse<true>(a, b, sel0 + t0, nt, st, st + kTile * pitch, pitch);
+          else fill_async(a, b, t0, nt, st, st + kTile * pitch, pitch, cpr);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
       }
@@ -449,14 +507,17 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         if (tn < ntiles) {
           const int64_t tn0 = cs + (int64_t)tn * kTile;
           uint8_t *sn = smem + (tn % n_stages) * stage_bytes;
-          fill_async(a, b, tn0, (int)(ce - tn0 < kTile ? ce - tn0 : kTile), sn, sn + kTile * pitch, pitch, cpr);
+          const int nn = (int)(ce - tn0 < kTile ? ce - tn0 : kTile);
+          if constexpr (SP) fill_sparse<true>(a, b, sel0 + tn0, nn, sn, sn + kTile * pitch, pitch);
+          else fill_async(a, b, tn0, nn, sn, sn + kTile * pitch, pitch, cpr);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
         st = smem + (t % n_stages) * stage_bytes;
       } else {
         if (t > 0) __syncthreads();          // previous tile fully consumed
         st = smem;
-        fill_sync(a, b, t0, n, st, st + kTile * pitch, pitch, cpr);
+        if constexpr (SP) fill_sparse<false>(a, b, sel0 + t0, n, st, st + kTile * pitch, pitch);
+        else fill_sync(a, b, t0, n, st, st + kTile * pitch, pitch, cpr);
         __syncthreads();
       }
       const uint8_t *sk = st, *sv = st + kTile * pitch;
@@ -464,7 +525,8 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       // scores of cell `lane`, then the online softmax
       float s[G];
       qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, s);
-      const bool valid = lane < n;
+      bool valid = lane < n;
+      if constexpr (SP) valid = valid && sparse_row(a, a.indices[(int64_t)b * a.max_ctx + sel0 + t0 + lane], false);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float sv_h = valid ? s[h] : -INFINITY;
@@ -543,7 +605,13 @@ decode_combine_kernel(const DecodeArgs a) {
   __shared__ float red_m[kCombineWarps];
   const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+  int64_t ctx;
+  if (a.offs) {                              // selection mode, staged: this bucket's picks
+    const int32_t *ob = a.offs + (int64_t)b * a.offs_stride + a.bucket;
+    ctx = ob[1] - ob[0];
+  } else {
+    ctx = !a.ctx_len ? a.max_ctx : (a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx);
+  }
   const int ns = ctx > 0 ? (int)((ctx + a.split_cells - 1) / a.split_cells) : 0;
   const size_t base = (size_t)b * a.n_splits * a.n_q_heads + h;
   float M = -INFINITY;
@@ -561,7 +629,8 @@ decode_combine_kernel(const DecodeArgs a) {
 #pragma unroll 4
   for (int s = warp; s < ns; s += kCombineWarps) {
     const size_t pi = base + (size_t)s * a.n_q_heads;
-    const float w = exp2f(a.part_ml[pi * 2] - M);
+    const float ms = a.part_ml[pi * 2];
+    const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);     // a chunk with nothing selected
     l = fmaf(w, a.part_ml[pi * 2 + 1], l);
     const float *pa = a.part_acc + pi * D + lane * DPL;
 #pragma unroll
@@ -571,14 +640,47 @@ decode_combine_kernel(const DecodeArgs a) {
   for (int i = 0; i < DPL; ++i) red[warp][lane * DPL + i] = acc[i];
   if (lane == 0) red_l[warp] = l;
   __syncthreads();
-  for (int d = threadIdx.x; d < D; d += kCombineWarps * 32) {
-    float sl = 0.f, sa = 0.f;
+  const size_t oi = (size_t)b * a.n_q_heads + h;
+  if (!a.run_acc) {
+    for (int d = threadIdx.x; d < D; d += kCombineWarps * 32) {
+      float sl = 0.f, sa = 0.f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-      sl += red_l[w];
-      sa += red[w][d];
+      for (int w = 0; w < kCombineWarps; ++w) {
+        sl += red_l[w];
+        sa += red[w][d];
+      }
+      a.out[oi * D + d] = sa / fmaxf(sl, 1e-30f);
     }
-    a.out[((size_t)b * a.n_q_heads + h) * D + d] = sa / fmaxf(sl, 1e-30f);
+    return;
+  }
+  // Fold this launch's (M, l, acc) into the running state (ExLlamaV3
+  // qsa-kv-offload patch, the per-bucket fold), in log2 units:
+  //   m' = max(m, M); alpha = 2^(m - m') (0 if m = -inf); beta = 2^(M - m') (0 if M = -inf)
+  //   acc = alpha acc + beta acc_b; l = alpha l + beta l_b
+  float sl = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) sl += red_l[w];
+  float m_run = -INFINITY, l_run = 0.f;
+  if (!a.init) {
+    m_run = a.run_ml[oi * 2];
+    l_run = a.run_ml[oi * 2 + 1];
+  }
+  const float m_new = fmaxf(m_run, M);
+  const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+  const float beta = M == -INFINITY ? 0.f : exp2f(M - m_new);
+  const float l_new = alpha * l_run + beta * sl;
+  for (int d = threadIdx.x; d < D; d += kCombineWarps * 32) {
+    float sa = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) sa += red[w][d];
+    const float acc_run = a.init ? 0.f : a.run_acc[oi * D + d];
+    const float acc_new = alpha * acc_run + beta * sa;
+    if (a.finalize) a.out[oi * D + d] = acc_new / fmaxf(l_new, 1e-30f);
+    else a.run_acc[oi * D + d] = acc_new;
+  }
+  if (!a.finalize && threadIdx.x == 0) {
+    a.run_ml[oi * 2] = m_new;
+    a.run_ml[oi * 2 + 1] = l_new;
   }
 }
 
@@ -589,13 +691,13 @@ inline size_t split_smem_bytes(const DecodeArgs &a, int g_per_warp, int n_stages
   return (size_t)n_stages * 2 * kTile * row_pitch(a.row_bytes) + (size_t)warps * kTile * gp * sizeof(uint64_t);
 }
 
-template <int KVT, int QT, int G, int D>
+template <int KVT, int QT, int G, int D, bool SP>
 cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   int n_stages = kMaxStages;
   while (n_stages > 1 && split_smem_bytes(a, G, n_stages) > (size_t)kSmemLimit) --n_stages;
   const size_t smem = split_smem_bytes(a, G, n_stages);
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidConfiguration;
-  auto k = decode_split_kernel<KVT, QT, G, D>;
+  auto k = decode_split_kernel<KVT, QT, G, D, SP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = (int64_t)a.batch * a.n_splits;
@@ -607,10 +709,10 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int KVT, int QT, int G>
+template <int KVT, int QT, int G, bool SP>
 cudaError_t launch_g(const DecodeArgs &a, cudaStream_t st) {
-  if (a.head_dim == 128) return launch_d<KVT, QT, G, 128>(a, st);
-  return launch_d<KVT, QT, G, 64>(a, st);
+  if (a.head_dim == 128) return launch_d<KVT, QT, G, 128, SP>(a, st);
+  return launch_d<KVT, QT, G, 64, SP>(a, st);
 }
 
 // Warps per kv head: the largest power of two w dividing the group with
@@ -628,18 +730,18 @@ inline int warps_per_kv_head(const DecodeArgs &a) {
 
 // The query type is the cache's 16-bit type (fp16 for a q8_0 cache); the
 // entry points reject other pairs.
-template <int KVT>
+template <int KVT, bool SP = false>
 cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
   constexpr int QT = KVT == KVO_BF16 ? KVO_BF16 : KVO_F16;
   switch (a.group / warps_per_kv_head(a)) {
-    case 1: return launch_g<KVT, QT, 1>(a, st);
-    case 2: return launch_g<KVT, QT, 2>(a, st);
-    case 3: return launch_g<KVT, QT, 3>(a, st);
-    case 4: return launch_g<KVT, QT, 4>(a, st);
-    case 5: return launch_g<KVT, QT, 5>(a, st);
-    case 6: return launch_g<KVT, QT, 6>(a, st);
-    case 7: return launch_g<KVT, QT, 7>(a, st);
-    default: return launch_g<KVT, QT, 8>(a, st);
+    case 1: return launch_g<KVT, QT, 1, SP>(a, st);
+    case 2: return launch_g<KVT, QT, 2, SP>(a, st);
+    case 3: return launch_g<KVT, QT, 3, SP>(a, st);
+    case 4: return launch_g<KVT, QT, 4, SP>(a, st);
+    case 5: return launch_g<KVT, QT, 5, SP>(a, st);
+    case 6: return launch_g<KVT, QT, 6, SP>(a, st);
+    case 7: return launch_g<KVT, QT, 7, SP>(a, st);
+    default: return launch_g<KVT, QT, 8, SP>(a, st);
   }
 }
 

@@ -3,6 +3,6 @@
 
 namespace kvo {
 namespace dec {
-template cudaError_t launch_kv<KVO_Q8_0>(const DecodeArgs &a, cudaStream_t st);
+template cudaError_t launch_kv<KVO_Q8_0, false>(const DecodeArgs &a, cudaStream_t st);
 }  // namespace dec
 }  // namespace kvo

@@ -26,7 +26,7 @@ int num_sms();                       // SMs of the current device (cached)
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Device-side error bits set by kernels that skipped an out-of-range item.
-enum DeviceErrorBits : uint32_t { kErrGatherSel = 1u };
+enum DeviceErrorBits : uint32_t { kErrGatherSel = 1u, kErrPageTable = 2u };
 uint32_t *device_error_word();       // address of the per-device word (nullptr on failure)
 
 // Launchers implemented in the kernel translation units.  They assume the
@@ -51,6 +51,25 @@ struct DecodeArgs {
   float *out;
   float *part_acc, *part_ml;   // workspace: [B][splits][Hq][D], [B][splits][Hq][2]
   int split_cells, n_splits;
+  // Running softmax state folded by the combine kernel (null: plain decode,
+  // out = the normalised result).  init: this launch starts the state;
+  // finalize: this launch writes out = acc / max(l, 1e-30).
+  float *run_acc = nullptr, *run_ml = nullptr;   // [B][Hq][D], [B][Hq][2]
+  int init = 1, finalize = 1;
+  // Sparse rows (QSA): cell k of work row b is cache position
+  // indices[b * max_ctx + k]; positions outside [win_lo, win_hi) are padding.
+  // staged: position j is row j - win_lo of k_lo / v_lo (the arena); else row
+  // block_table[j / page_size] * page_size + j % page_size of k_hi / v_hi.
+  const int32_t *indices = nullptr;              // null for the decode
+  // Staged mode: row b's picks of this bucket are indices[b * max_ctx +
+  // offs[b * offs_stride + bucket] ...] up to offs[... + bucket + 1].
+  const int32_t *offs = nullptr;
+  int64_t offs_stride = 0, bucket = 0;
+  int64_t win_lo = 0, win_hi = 0;
+  const int32_t *block_table = nullptr;
+  int64_t page_size = 1, n_pages_total = 0;
+  int sparse_staged = 0;
+  uint32_t *err = nullptr;     // device error word (sparse: bad page-table entries)
 };
 // Split geometry for a decode: fixed cell ranges that depend on max_ctx and
 // batch only (never on N or on staging), so tiered and all-VRAM runs match.
@@ -59,6 +78,16 @@ void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *spli
 size_t decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t head_dim,
                               int64_t max_ctx);
 int launch_decode(const DecodeArgs &a, cudaStream_t st);   // kvo_status
+// Sparse rows: the split kernel in selection mode (fp16 / bf16 caches), then
+// the combine (with the running-state fold when a.run_acc is set).
+int launch_sparse_rows(const DecodeArgs &a, cudaStream_t st);   // kvo_status
+// Copy pages block_table[p0 .. p0 + n) of the K and V planes (page_bytes each)
+// to arena slots 0 .. n-1; entries outside [0, n_pages_total) are skipped and
+// set kErrPageTable.
+cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t page_bytes,
+                               const int32_t *block_table, int64_t p0, int64_t n,
+                               int64_t n_pages_total, void *k_arena, void *v_arena, uint32_t *err,
+                               cudaStream_t st);
 
 struct PrefillArgs {
   const uint16_t *q;           // [rows][Hq][D] (rows of this launch start at q)

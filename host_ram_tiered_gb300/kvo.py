@@ -49,6 +49,11 @@ SIGNATURES = {
                                               _vp]),
     "kvo_append_kv_tiered": (_int, [_vp, _vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                     _int, _i64, _i64, _vp]),
+    "kvo_staging_worthwhile": (_int, [_i64, _i64, _i64, _i64]),
+    "kvo_attn_sparse_rows_workspace_bytes": (_sz, [_i64] * 8 + [_sz]),
+    "kvo_attn_sparse_rows": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _int, _i64, _i64,
+                                    _vp, _i64, _vp, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz, _vp]),
+    "kvo_copy_pages_host": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _vp]),
     "kvo_attn_prefill_workspace_bytes": (_sz, [_i64, _i64]),
     "kvo_attn_prefill_tiered": (_int, [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                        _int, _i64, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz,
@@ -210,3 +215,31 @@ def kvo_attn_prefill_tiered(q, rows, q_pos0, n_q_heads, n_kv_heads, head_dim, k_
         _p(v_host), kv_dtype, ctx_len, n_vram_cells, scale, _p(arena), arena_bytes,
         rows_per_launch, _p(out), _p(workspace), workspace_bytes, _s(stream)),
         "kvo_attn_prefill_tiered")
+
+
+def kvo_staging_worthwhile(rows, k_pad, num_pages_used, page_size) -> bool:
+    return bool(load().kvo_staging_worthwhile(rows, k_pad, num_pages_used, page_size))
+
+
+def kvo_attn_sparse_rows_workspace_bytes(rows, n_q_heads, n_kv_heads, head_dim, k_pad, rows_per_launch,
+                                         page_size, num_pages_used, arena_bytes) -> int:
+    return load().kvo_attn_sparse_rows_workspace_bytes(rows, n_q_heads, n_kv_heads, head_dim, k_pad,
+                                                       rows_per_launch, page_size, num_pages_used,
+                                                       arena_bytes)
+
+
+def kvo_attn_sparse_rows(q, q_dtype, rows, n_q_heads, n_kv_heads, head_dim, k_pages, v_pages, dtype,
+                         page_size, n_pages, block_table, num_pages_used, indices, k_pad, scale, arena,
+                         arena_bytes, rows_per_launch, out, workspace, workspace_bytes, stream=None) -> None:
+    _check(load().kvo_attn_sparse_rows(
+        _p(q), q_dtype, rows, n_q_heads, n_kv_heads, head_dim, _p(k_pages), _p(v_pages), dtype,
+        page_size, n_pages, _p(block_table), num_pages_used, _p(indices), k_pad, scale, _p(arena),
+        arena_bytes, rows_per_launch, _p(out), _p(workspace), workspace_bytes, _s(stream)),
+        "kvo_attn_sparse_rows")
+
+
+def kvo_copy_pages_host(src_k, src_v, dst_k, dst_v, page_tokens, token_bytes, from_page, to_page,
+                        num_tokens, stream=None) -> None:
+    _check(load().kvo_copy_pages_host(_p(src_k), _p(src_v), _p(dst_k), _p(dst_v), page_tokens,
+                                      token_bytes, from_page, to_page, num_tokens, _s(stream)),
+           "kvo_copy_pages_host")

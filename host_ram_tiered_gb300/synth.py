@@ -101,3 +101,23 @@ def topk_selection(n_seq: int, n_kv_heads: int, n_blocks: int, k: int,
             sel[s, h, :k - 1] = np.sort(pick)
             sel[s, h, k - 1] = n_blocks - 1
     return sel
+
+
+def row_selections(rows: int, k_pad: int, first_pos: int, n_pick: int,
+                   gen: np.random.Generator, pad_frac: float = 0.0) -> np.ndarray:
+    """Per query row i (at position first_pos + i): n_pick distinct cache
+    positions drawn uniformly from [0, first_pos + i], in random order, then
+    -1 padding up to k_pad; with pad_frac > 0 about that fraction of the picks
+    is replaced by -1 as well.  int32 [rows][k_pad]."""
+    out = np.full((rows, k_pad), -1, np.int32)
+    for i in range(rows):
+        hi = first_pos + i + 1
+        n = min(n_pick, hi)
+        pick = np.unique(gen.integers(0, hi, size=n + n // 4 + 8))
+        while pick.size < n:
+            pick = np.unique(np.concatenate([pick, gen.integers(0, hi, size=n)]))
+        pick = gen.permutation(gen.permutation(pick)[:n])
+        out[i, :n] = pick
+    if pad_frac > 0:
+        out[gen.random(out.shape) < pad_frac] = -1
+    return out

@@ -290,6 +290,96 @@ int kvo_attn_decode_tiered_noalloc(const void *q, int q_dtype, int64_t batch,
                                    float *out, void *stream);
 
 /* ------------------------------------------------------------------------
+ * kvo_staging_worthwhile -- the staged/direct rule of the sparse rows.
+ *
+ * ExLlamaV3 patch "QSA KV cache host-RAM offload", qsa_staging_worthwhile:
+ * the direct gather reads rows * k_pad cache positions (every row its own
+ * selection, re-reading shared pages), staging reads num_pages_used *
+ * page_size positions once.  Returns 1 when rows * k_pad > 2 *
+ * num_pages_used * page_size, else 0 (also for a negative size).  Pure host
+ * function.
+ * ---------------------------------------------------------------------- */
+int kvo_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
+                           int64_t page_size);
+
+/* ------------------------------------------------------------------------
+ * kvo_attn_sparse_rows -- QSA sparse attention of query rows over a paged,
+ * host-resident K/V cache, direct or staged through a VRAM arena.
+ *
+ * ExLlamaV3 patch "QSA KV cache host-RAM offload": qsa_sparse_attend_rows
+ * (direct) and qsa_sparse_attend_rows_staged.  Row r (q [rows][n_q_heads]
+ * [head_dim] of q_dtype == dtype) attends to the cache positions
+ * indices[r][0 .. k_pad) that are >= 0 and < num_pages_used * page_size
+ * (anything else is padding).  Position p is slot p % page_size of page
+ * block_table[p / page_size] of the planes k_pages / v_pages
+ * ([n_pages][page_size][n_kv_heads][head_dim], F16 or BF16); q head h reads
+ * kv head h / (n_q_heads / n_kv_heads):
+ *     out[r][h] = sum_p softmax_p(scale * q[r][h] . k_p) v_p
+ * (a position listed twice counts twice; a row with no selection gives 0).
+ *   arena == NULL (or num_pages_used == 0): direct -- every row reads its
+ *     picks through the host mapping, rows_per_launch rows per launch.
+ *   arena != NULL: staged -- the pages in use are walked in buckets of
+ *     arena_pages = min(arena_bytes / (2 * page_bytes), num_pages_used)
+ *     pages (page_bytes = page_size * n_kv_heads * head_dim * 2; at least 2
+ *     pages must fit, KVO_ERR_ARG otherwise).  Each bucket is gathered into
+ *     the arena (K in the first half, V after it), every row block is scored
+ *     against it, and its partial (m, l, acc) is folded into a running
+ *     state; after the last bucket out = acc / max(l, 1e-30).
+ *   Staged and direct agree within the attention tolerance, not bit for bit.
+ * q, out (fp32 [rows][n_q_heads][head_dim]), workspace, arena: device
+ *   memory, 16-byte aligned.  indices (int32 [rows][k_pad]) and block_table
+ *   (int32 [num_pages_used]): device-accessible.  k_pages / v_pages: pinned
+ *   mapped host (or device) memory, 16-byte aligned.
+ * head_dim 64 or 128; group 1..8; n_kv_heads <= 8.
+ * A block_table entry outside [0, n_pages) is skipped (its picks count as
+ *   padding) and sets bit 1 of kvo_device_errors().
+ * Staged mode first groups every row's picks by bucket (order kept within a
+ *   bucket, padding dropped) so that each bucket scores only its own picks;
+ *   at most 51,199 buckets.
+ * workspace: at least kvo_attn_sparse_rows_workspace_bytes(rows, n_q_heads,
+ *   n_kv_heads, head_dim, k_pad, rows_per_launch, page_size, num_pages_used,
+ *   arena_bytes) bytes (the same arguments as the call).
+ * Errors: KVO_ERR_ARG, KVO_ERR_ALIGN, KVO_ERR_NOT_MAPPED,
+ *   KVO_ERR_UNSUPPORTED, KVO_ERR_WORKSPACE, KVO_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+size_t kvo_attn_sparse_rows_workspace_bytes(int64_t rows, int64_t n_q_heads,
+                                            int64_t n_kv_heads, int64_t head_dim,
+                                            int64_t k_pad,
+                                            int64_t rows_per_launch,
+                                            int64_t page_size,
+                                            int64_t num_pages_used,
+                                            size_t arena_bytes);
+
+int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows,
+                         int64_t n_q_heads, int64_t n_kv_heads,
+                         int64_t head_dim, const void *k_pages,
+                         const void *v_pages, int dtype, int64_t page_size,
+                         int64_t n_pages, const int32_t *block_table,
+                         int64_t num_pages_used, const int32_t *indices,
+                         int64_t k_pad, float scale, void *arena,
+                         size_t arena_bytes, int64_t rows_per_launch,
+                         float *out, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_copy_pages_host -- copy one page's first tokens between host planes.
+ *
+ * ExLlamaV3 patch "QSA KV cache host-RAM offload", copy_page: host-resident
+ * pages are copied by the CPU, not by a device kernel reading and writing
+ * across the host link.  The call first drains `stream` (queued GPU work may
+ * still read or write the pages), then copies num_tokens * token_bytes bytes
+ * from page from_page to page to_page (pages of page_tokens * token_bytes
+ * bytes) for K (src_k -> dst_k) and V (src_v -> dst_v); overlapping ranges
+ * are allowed.  Synchronous; the planes must be host memory (pinned or not).
+ * Errors: KVO_ERR_ARG (num_tokens > page_tokens, negative sizes, NULL),
+ *   KVO_ERR_NOT_MAPPED (a device pointer), KVO_ERR_CUDA (the drain).
+ * ---------------------------------------------------------------------- */
+int kvo_copy_pages_host(const void *src_k, const void *src_v, void *dst_k,
+                        void *dst_v, int64_t page_tokens, int64_t token_bytes,
+                        int64_t from_page, int64_t to_page, int64_t num_tokens,
+                        void *stream);
+
+/* ------------------------------------------------------------------------
  * kvo_append_kv_tiered -- write path: new tokens into a tiered cache.
  *
  * ExLlamaV3 qsa-kv-offload patch (the paged cache update that writes new

@@ -129,3 +129,26 @@ def test_fragment_ptrs_matches_oracle(kvo_lib):
     rs, rd, rz = oracle.fragment_ptrs(sb.view(np.uint64), db.view(np.uint64), es, ed, ez)
     assert np.array_equal(os_.view(np.uint64), rs) and np.array_equal(od.view(np.uint64), rd)
     assert np.array_equal(oz, rz)
+
+
+def test_staging_rule_matches_the_oracle_and_golden(kvo_lib):
+    # pure host function: callable without a GPU
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "staging_policy.txt")
+    cases = [list(map(int, ln.split())) for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    for rows, k_pad, npu, ps, want in cases:
+        assert kvo.kvo_staging_worthwhile(rows, k_pad, npu, ps) == bool(want)
+    g = np.random.default_rng(5)
+    for _ in range(200):
+        r, k, n, p = (int(x) for x in g.integers(0, 3000, 4))
+        assert kvo.kvo_staging_worthwhile(r, k, n, p) == oracle.staging_worthwhile(r, k, n, p)
+    assert not kvo.kvo_staging_worthwhile(-1, 5, 1, 1)
+
+
+def test_sparse_rows_workspace_grows_with_buckets(kvo_lib):
+    direct = kvo.kvo_attn_sparse_rows_workspace_bytes(64, 8, 2, 128, 96, 64, 16, 40, 0)
+    staged = kvo.kvo_attn_sparse_rows_workspace_bytes(64, 8, 2, 128, 96, 64, 16, 40, 2 * 5 * 16 * 2 * 128 * 2)
+    assert direct > 0 and staged > direct
+    # grouped picks (64 x 96 int32) and offsets (64 x 9 int32) on top
+    assert staged - direct >= 64 * 96 * 4 + 64 * 9 * 4
+    assert kvo.kvo_attn_sparse_rows_workspace_bytes(0, 8, 2, 128, 96, 64, 16, 40, 0) == 0
