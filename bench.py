@@ -382,6 +382,8 @@ def c4_decode(st):
 
 C5_R, C5_POS0, C5_L, C5_HQ, C5_HKV, C5_D, C5_N = 2048, 260096, 262144, 32, 8, 128, 65536
 C5_ARENA, C5_RPL = 32 << 20, 1024
+# FP32 multiply-adds per second on CUDA cores: 152 SMs x 128 lanes x 2.07 GHz
+FP32_FMA_PEAK = 152 * 128 * 2.07e9
 
 
 def c5_setup(seed=SEED0 + 4):
@@ -424,6 +426,48 @@ def c5_flops():
     # causal: row i sees pos0 + i + 1 cells; QK^T and PV are 2 flops per MAC each
     cells = sum(C5_POS0 + i + 1 for i in range(C5_R))
     return 4.0 * C5_HQ * C5_D * cells
+
+
+# ----------------------------------------------------------------- QSA sparse rows (next row)
+
+# ExLlamaV3 QSA offload prefill: 2048 query rows, each picking 2080 cache
+# positions, over a paged fp16 host cache of 262,144 positions (1,024 pages
+# of 256 tokens, 32 q / 8 kv heads x 128), staged through a 32 MiB arena.
+C7_R, C7_POS0, C7_L, C7_PS, C7_KPAD = 2048, 260096, 262144, 256, 2080
+C7_HQ, C7_HKV, C7_D, C7_ARENA, C7_RPL = 32, 8, 128, 32 << 20, 1024
+
+
+def c7_setup(seed=SEED0 + 6):
+    t = torch()
+    n_pages = C7_L // C7_PS
+    page_bytes = C7_PS * C7_HKV * C7_D * 2
+    k_pages = pinned(n_pages * page_bytes)
+    v_pages = pinned(n_pages * page_bytes)
+    synth.fill_normal_bits_large(k_pages.numpy().view(np.uint16), "f16", seed, 1)
+    synth.fill_normal_bits_large(v_pages.numpy().view(np.uint16), "f16", seed, 2)
+    g = synth.rng(seed, 3)
+    bt = g.permutation(n_pages).astype(np.int32)
+    idx = synth.row_selections(C7_R, C7_KPAD, C7_POS0, C7_KPAD, synth.rng(seed, 4))
+    q = synth.normal_bits((C7_R, C7_HQ, C7_D), "f16", synth.rng(seed, 5))
+    st = {"n_pages": n_pages, "page_bytes": page_bytes, "k_pages": k_pages, "v_pages": v_pages,
+          "bt_np": bt, "idx_np": idx, "q_np": q, "bt": t.from_numpy(bt).cuda(),
+          "idx": t.from_numpy(idx.reshape(-1).copy()).cuda(),
+          "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(), "arena": dev(C7_ARENA),
+          "out": t.empty(C7_R * C7_HQ * C7_D, dtype=t.float32, device="cuda")}
+    k = kvo()
+    st["ws_bytes"] = max(k.kvo_attn_sparse_rows_workspace_bytes(C7_R, C7_HQ, C7_HKV, C7_D, C7_KPAD, C7_RPL,
+                                                                C7_PS, n_pages, a)
+                         for a in (0, C7_ARENA))
+    st["ws"] = dev(st["ws_bytes"])
+    return st
+
+
+def c7_run(st, staged=True):
+    k = kvo()
+    k.kvo_attn_sparse_rows(st["q"], k.F16, C7_R, C7_HQ, C7_HKV, C7_D, st["k_pages"], st["v_pages"], k.F16,
+                           C7_PS, st["n_pages"], st["bt"], st["n_pages"], st["idx"], C7_KPAD,
+                           1.0 / math.sqrt(C7_D), st["arena"] if staged else None, C7_ARENA if staged else 0,
+                           C7_RPL, st["out"], st["ws"], st["ws_bytes"])
 
 
 # ----------------------------------------------------------------- write path (append)
@@ -549,7 +593,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
                     help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append), "
-                         "c3vram (the 184,320-cell all-VRAM decode alone; not in 'all') (default all)")
+                         "c7 (QSA sparse rows), c3vram (the 184,320-cell all-VRAM decode alone; not in "
+                         "'all') (default all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -569,7 +614,7 @@ def main(argv=None):
     build.build()
     k = kvo()
     k.load()
-    rows = set(args.rows.split(",")) if args.rows != "all" else {"head", "c1", "c2", "c3", "c4", "c5", "c6"}
+    rows = set(args.rows.split(",")) if args.rows != "all" else {"head", "c1", "c2", "c3", "c4", "c5", "c6", "c7"}
     timer = Timer()
     peaks = measure_link_peak(timer)
     hbm = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6789.0) \
@@ -695,6 +740,23 @@ def main(argv=None):
                 "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["d2h"],
                 "host_bytes": host_b}
         del st6
+    # ---- QSA sparse rows (staged through the arena vs direct)
+    if "c7" in rows:
+        st7 = c7_setup()
+        host_staged = 2 * st7["n_pages"] * st7["page_bytes"]
+        host_direct = 2 * C7_R * C7_KPAD * C7_HKV * C7_D * 2
+        fma = 2.0 * C7_R * C7_KPAD * C7_HQ * C7_D
+        for staged in (True, False):
+            steps = K if staged else max(1, min(K, 2))
+            tot, _ = timer.run(lambda: c7_run(st7, staged), steps, min(W, 3))
+            us_r = max_over_ranks(tot, world) / steps * 1e3
+            hb = host_staged if staged else host_direct
+            gbs = hb / (us_r * 1e-6) / 1e9
+            t_star = max(hb / (peaks["h2d"] * 1e9), fma / FP32_FMA_PEAK)
+            results[f"c7_qsa_sparse_rows_{'staged' if staged else 'direct'}"] = {
+                "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": t_star / (us_r * 1e-6),
+                "rows_per_s": C7_R / (us_r * 1e-6)}
+        del st7
     # ---- C5 prefill
     if "c5" in rows:
         st5 = c5_setup()
@@ -800,6 +862,10 @@ def gpu_launch_count(K, rows):
         # staged: VRAM head (2 row blocks) + 48 arena buckets of 4096 cells x 2 row blocks;
         # direct: head + host tail, 2 row blocks each
         n += K * (2 + 48 * 2) + min(K, 3) * 4
+    if "c7" in rows:
+        # staged: partition + 32 buckets x (page gather + 2 row blocks x (split + combine));
+        # direct: 2 row blocks x (split + combine)
+        n += K * (1 + 32 * (1 + 2 * 2)) + max(1, min(K, 2)) * 4
     return n
 
 

@@ -684,6 +684,72 @@ decode_combine_kernel(const DecodeArgs a) {
   }
 }
 
+// The same fold for launches with few chunks (<= kSmallCombineChunks): one
+// warp per (row, q head), chunks folded in ascending order, lane l owning
+// dims [l * D/32, (l + 1) * D/32).  Many small (row, head) items (the sparse
+// rows) then cost one warp each instead of one CTA.
+constexpr int kSmallCombineChunks = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+decode_combine_small_kernel(const DecodeArgs a) {
+  constexpr int DPL = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kCombineWarps + warp;
+  if (item >= (int64_t)a.batch * a.n_q_heads) return;
+  const int b = (int)(item / a.n_q_heads), h = (int)(item % a.n_q_heads);
+  int64_t ctx;
+  if (a.offs) {
+    const int32_t *ob = a.offs + (int64_t)b * a.offs_stride + a.bucket;
+    ctx = ob[1] - ob[0];
+  } else {
+    ctx = !a.ctx_len ? a.max_ctx : (a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx);
+  }
+  const int ns = ctx > 0 ? (int)((ctx + a.split_cells - 1) / a.split_cells) : 0;
+  const size_t base = (size_t)b * a.n_splits * a.n_q_heads + h;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_ml[(base + (size_t)s * a.n_q_heads) * 2]);
+  float l = 0.f, acc[DPL];
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const size_t pi = base + (size_t)s * a.n_q_heads;
+    const float ms = a.part_ml[pi * 2];
+    const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+    l = fmaf(w, a.part_ml[pi * 2 + 1], l);
+    const float *pa = a.part_acc + pi * D + lane * DPL;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = fmaf(w, pa[i], acc[i]);
+  }
+  const size_t oi = (size_t)b * a.n_q_heads + h;
+  float *o = a.out + oi * D + lane * DPL;
+  if (!a.run_acc) {
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = acc[i] / fmaxf(l, 1e-30f);
+    return;
+  }
+  float m_run = -INFINITY, l_run = 0.f;
+  if (!a.init) {
+    m_run = a.run_ml[oi * 2];
+    l_run = a.run_ml[oi * 2 + 1];
+  }
+  const float m_new = fmaxf(m_run, M);
+  const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+  const float beta = M == -INFINITY ? 0.f : exp2f(M - m_new);
+  const float l_new = alpha * l_run + beta * l;
+  float *ra = a.run_acc + oi * D + lane * DPL;
+#pragma unroll
+  for (int i = 0; i < DPL; ++i) {
+    const float acc_new = alpha * (a.init ? 0.f : ra[i]) + beta * acc[i];
+    if (a.finalize) o[i] = acc_new / fmaxf(l_new, 1e-30f);
+    else ra[i] = acc_new;
+  }
+  if (!a.finalize && lane == 0) {
+    a.run_ml[oi * 2] = m_new;
+    a.run_ml[oi * 2 + 1] = l_new;
+  }
+}
+
 // Shared memory of the split kernel for n_stages ring stages.
 inline size_t split_smem_bytes(const DecodeArgs &a, int g_per_warp, int n_stages) {
   const int warps = a.n_kv_heads * (a.group / g_per_warp);
@@ -705,7 +771,13 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   k<<<(unsigned)grid, 32 * a.n_kv_heads * (a.group / G), smem, st>>>(a, n_stages);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
+  if (a.n_splits <= kSmallCombineChunks) {
+    const int64_t items = (int64_t)a.batch * a.n_q_heads;
+    decode_combine_small_kernel<D><<<(unsigned)((items + kCombineWarps - 1) / kCombineWarps),
+                                     kCombineWarps * 32, 0, st>>>(a);
+  } else {
+    decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

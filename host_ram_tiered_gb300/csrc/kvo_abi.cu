@@ -47,22 +47,11 @@ int classify(const void *p, size_t bytes) {
   return k2 == k ? k : 0;
 }
 
-// Streams of the prefill: a side stream that fills one arena slot while the
-// caller's stream scores the other, and a second launch stream so that two
-// row blocks run concurrently (their CTAs fill each other's partial last
-// wave).  Created once per device; every use forks from and joins back into
-// the caller's stream.
-struct Ring {
-  cudaStream_t side = nullptr, comp2 = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
-  cudaEvent_t ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr}, done2[2] = {nullptr, nullptr};
-};
-
-Ring *ring() {
-  static Ring rings[64];
+Ring *ring(int which) {
+  static Ring rings[2][64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  Ring &r = rings[dev];
+  if (which < 0 || which > 1 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  Ring &r = rings[which][dev];
   if (!r.side) {
     cudaStream_t s = nullptr, s2 = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
@@ -563,7 +552,7 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
   std::unique_lock<std::mutex> lock(ring_mu, std::defer_lock);
   if (staged || two) {
     lock.lock();
-    rg = ring();
+    rg = ring(0);
     if (!rg) return fail(KVO_ERR_CUDA, "kvo_attn_prefill_tiered: library streams unavailable");
     int e = cuda_status(cudaEventRecord(rg->fork, st), "cudaEventRecord");
     if (!e && staged) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");

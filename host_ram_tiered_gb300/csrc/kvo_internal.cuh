@@ -23,6 +23,18 @@ enum Access { kDeviceMem = 1, kMappedHost = 2 };
 int classify(const void *p, size_t bytes);
 
 int num_sms();                       // SMs of the current device (cached)
+
+// Library streams for staged work: a side stream that fills one arena slot
+// while the caller's stream scores the other, and a second launch stream so
+// that two row blocks run concurrently.  One set per user (0: prefill,
+// 1: sparse rows) and device, created on first use; every use forks from and
+// joins back into the caller's stream, under the user's own mutex.
+struct Ring {
+  cudaStream_t side = nullptr, comp2 = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
+  cudaEvent_t ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr}, done2[2] = {nullptr, nullptr};
+};
+Ring *ring(int which);               // nullptr when the streams cannot be created
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Device-side error bits set by kernels that skipped an out-of-range item.

@@ -10,6 +10,7 @@
 // padding), and the combine kernel folds the bucket's (m, l, acc) into a
 // running state, writing out = acc / max(l, 1e-30) after the last bucket.
 #include <cstring>
+#include <mutex>
 
 #include "decode_impl.cuh"
 
@@ -129,11 +130,21 @@ int64_t row_block(int64_t rows, int64_t rows_per_launch) {
 
 size_t up16(size_t x) { return (x + 15) / 16 * 16; }
 
-// Arena pages per bucket (0: direct), per the page's arena sizing: half the
-// arena each for K and V pages, at most the pages in use.
-int64_t arena_pages_of(size_t arena_bytes, int64_t page_bytes, int64_t num_pages_used) {
+// Arena pages per bucket (0: direct).  The page sizes one bucket as half the
+// arena each for K and V pages (at most the pages in use); here the arena
+// holds two such slots when it can, so that the next bucket's pages arrive
+// while the current one is scored: slot pages = arena / (4 page_bytes), or
+// arena / (2 page_bytes) with a single slot when two do not fit.
+int64_t arena_pages_of(size_t arena_bytes, int64_t page_bytes, int64_t num_pages_used, int *slots) {
+  *slots = 0;
   if (arena_bytes == 0 || num_pages_used <= 0 || page_bytes <= 0) return 0;
-  int64_t n = (int64_t)(arena_bytes / (2 * (size_t)page_bytes));
+  int64_t n = (int64_t)(arena_bytes / (4 * (size_t)page_bytes));
+  *slots = 2;
+  if (n < 1) {
+    n = (int64_t)(arena_bytes / (2 * (size_t)page_bytes));
+    *slots = 1;
+  }
+  if (n < 1) *slots = 0;
   return n < num_pages_used ? n : num_pages_used;
 }
 
@@ -194,7 +205,8 @@ extern "C" size_t kvo_attn_sparse_rows_workspace_bytes(int64_t rows, int64_t n_q
   if (rows <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || head_dim <= 0 || k_pad < 0 || rows_per_launch <= 0 ||
       page_size <= 0 || num_pages_used < 0)
     return 0;
-  const int64_t ap = arena_pages_of(arena_bytes, page_size * n_kv_heads * head_dim * 2, num_pages_used);
+  int slots = 0;
+  const int64_t ap = arena_pages_of(arena_bytes, page_size * n_kv_heads * head_dim * 2, num_pages_used, &slots);
   const int64_t n_b = ap > 0 ? (num_pages_used + ap - 1) / ap : 0;
   return sparse_workspace(rows, n_q_heads, head_dim, k_pad, rows_per_launch, n_b).total;
 }
@@ -241,8 +253,9 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
   }
   const bool staged = arena != nullptr && arena_bytes > 0 && num_pages_used > 0;
   int64_t arena_pages = 0, n_b = 0;
+  int slots = 0;
   if (staged) {
-    arena_pages = arena_pages_of(arena_bytes, page_bytes, num_pages_used);
+    arena_pages = arena_pages_of(arena_bytes, page_bytes, num_pages_used, &slots);
     if (arena_pages < 1) return fail(KVO_ERR_ARG, "%s: arena smaller than 2 pages", fn);
     if (!aligned16(arena)) return fail(KVO_ERR_ALIGN, "%s: arena alignment", fn);
     if (classify(arena, arena_bytes) != kDeviceMem)
@@ -281,8 +294,6 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
   base.k_lo = base.v_lo = nullptr;
 
   if (staged) {
-    base.k_lo = (const uint8_t *)arena;
-    base.v_lo = (const uint8_t *)arena + (size_t)arena_pages * page_bytes;
     // group every row's picks by bucket once
     if (k_pad > 0) {
       int warps = (int)(kPartitionSmem / ((n_b + 1) * 4));
@@ -300,14 +311,41 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
     }
   }
 
+  // Two slots: slot bk % 2 is gathered on the library's side stream once the
+  // caller's stream has finished scoring the bucket that used it before.
+  static std::mutex ring_mu;
+  std::unique_lock<std::mutex> lock(ring_mu, std::defer_lock);
+  Ring *rg = nullptr;
+  if (staged && slots == 2) {
+    lock.lock();
+    rg = ring(1);
+    if (!rg) return fail(KVO_ERR_CUDA, "%s: library streams unavailable", fn);
+    int e = cuda_status(cudaEventRecord(rg->fork, st), "cudaEventRecord");
+    if (!e) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");
+    if (e) return e;
+  }
+  const size_t slot_bytes = 2 * (size_t)arena_pages * page_bytes;
   const int64_t n_buckets = staged ? n_b : 1;
   for (int64_t bk = 0; bk < n_buckets; ++bk) {
     const int64_t p0 = bk * arena_pages;
     const int64_t np = staged ? (num_pages_used - p0 < arena_pages ? num_pages_used - p0 : arena_pages) : 0;
+    const int slot = rg ? (int)(bk & 1) : 0;
     if (staged) {
+      base.k_lo = (const uint8_t *)arena + slot * slot_bytes;
+      base.v_lo = base.k_lo + (size_t)arena_pages * page_bytes;
+      cudaStream_t gs = rg ? rg->side : st;
+      if (rg && bk >= 2) {
+        const int e = cuda_status(cudaStreamWaitEvent(gs, rg->freed[slot], 0), "cudaStreamWaitEvent");
+        if (e) return e;
+      }
       const cudaError_t e = launch_page_gather(k_pages, v_pages, page_bytes, block_table, p0, np, n_pages,
-                                               (void *)base.k_lo, (void *)base.v_lo, err, st);
+                                               (void *)base.k_lo, (void *)base.v_lo, err, gs);
       if (e != cudaSuccess) return cuda_status(e, "page gather launch");
+      if (rg) {
+        int e2 = cuda_status(cudaEventRecord(rg->ready[slot], gs), "cudaEventRecord");
+        if (!e2) e2 = cuda_status(cudaStreamWaitEvent(st, rg->ready[slot], 0), "cudaStreamWaitEvent");
+        if (e2) return e2;
+      }
     }
     for (int64_t r0 = 0; r0 < rows; r0 += rbk) {
       const int64_t nr = rows - r0 < rbk ? rows - r0 : rbk;
@@ -338,6 +376,10 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
         a.win_hi = num_pages_used * page_size;
       }
       const int e = launch_sparse_rows(a, st);
+      if (e) return e;
+    }
+    if (rg) {
+      const int e = cuda_status(cudaEventRecord(rg->freed[slot], st), "cudaEventRecord");
       if (e) return e;
     }
   }

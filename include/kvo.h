@@ -318,13 +318,17 @@ int kvo_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
  * (a position listed twice counts twice; a row with no selection gives 0).
  *   arena == NULL (or num_pages_used == 0): direct -- every row reads its
  *     picks through the host mapping, rows_per_launch rows per launch.
- *   arena != NULL: staged -- the pages in use are walked in buckets of
- *     arena_pages = min(arena_bytes / (2 * page_bytes), num_pages_used)
- *     pages (page_bytes = page_size * n_kv_heads * head_dim * 2; at least 2
- *     pages must fit, KVO_ERR_ARG otherwise).  Each bucket is gathered into
- *     the arena (K in the first half, V after it), every row block is scored
- *     against it, and its partial (m, l, acc) is folded into a running
- *     state; after the last bucket out = acc / max(l, 1e-30).
+ *   arena != NULL: staged -- the pages in use are walked in buckets; each
+ *     bucket is gathered into an arena slot (its K pages, then its V pages),
+ *     every row block is scored against it, and its partial (m, l, acc) is
+ *     folded into a running state; after the last bucket
+ *     out = acc / max(l, 1e-30).  With page_bytes = page_size * n_kv_heads *
+ *     head_dim * 2, the arena holds two slots of arena_bytes / (4 *
+ *     page_bytes) pages when that is >= 1 (the next bucket is gathered on a
+ *     library stream while the current one is scored), else one slot of
+ *     arena_bytes / (2 * page_bytes) pages; a bucket never exceeds
+ *     num_pages_used pages.  At least 2 pages must fit (KVO_ERR_ARG
+ *     otherwise).
  *   Staged and direct agree within the attention tolerance, not bit for bit.
  * q, out (fp32 [rows][n_q_heads][head_dim]), workspace, arena: device
  *   memory, 16-byte aligned.  indices (int32 [rows][k_pad]) and block_table

@@ -59,10 +59,13 @@ def test_sparse_rows_direct_and_staged_match_oracle(dt, hq, hkv, d, rows):
     idx_dev = t.from_numpy(idx.reshape(-1).copy()).cuda()
     runs = {"direct": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev, k_pad,
                            scale),
-            "staged_1": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev, k_pad,
-                             scale, arena_pages=npu),
-            "staged_9": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev, k_pad,
-                             scale, arena_pages=5, rows_per_launch=64)}
+            # arena of 2 * arena_pages pages: two slots of arena_pages / 2 pages each when that is >= 1
+            "one_bucket": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev, k_pad,
+                               scale, arena_pages=2 * npu),
+            "two_slots_20_buckets": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev,
+                                         k_pad, scale, arena_pages=5, rows_per_launch=64),
+            "one_slot_40_buckets": _run(q_dev, dt, rows, hq, hkv, d, kp, vp, ps, n_pages, bt_dev, npu, idx_dev,
+                                        k_pad, scale, arena_pages=1)}
     for name_, out in runs.items():
         assert np.all(out[0] == 0.0), name_
         assert normwise_rel_err(out[1:], ref[1:]) <= REL_TOL, name_
@@ -157,3 +160,25 @@ def test_copy_pages_host_sees_queued_gpu_writes():
     with pytest.raises(kvo.KvoError) as e:
         kvo.kvo_copy_pages_host(dev, hv, hk, hv, ps, tok, 0, 1, 4, s)
     assert e.value.status == -3
+
+
+def test_full_size_qsa_prefill_sampled_rows():
+    # 2048 rows x 2080 picks over 262,144 fp16 positions in 1,024 host pages of 256,
+    # 32 q / 8 kv heads x 128, staged through a 32 MiB arena (32 buckets) and direct;
+    # 24 sampled rows against the oracle.
+    from bench import C7_D, C7_HKV, C7_HQ, C7_KPAD, C7_PS, c7_run, c7_setup
+    t = torch()
+    st = c7_setup()
+    kp = st["k_pages"].numpy()
+    vp = st["v_pages"].numpy()
+    rows = np.linspace(0, 2047, 24).astype(int)
+    ref = oracle.attn_sparse_rows(kp, vp, oracle.F16, C7_PS, C7_HKV, C7_D, st["bt_np"], st["n_pages"],
+                                  st["idx_np"][rows], st["q_np"][rows], oracle.F16, C7_HQ,
+                                  1.0 / math.sqrt(C7_D))
+    for staged in (True, False):
+        st["out"].fill_(float("nan"))
+        c7_run(st, staged)
+        t.cuda.synchronize()
+        out = st["out"].cpu().numpy().reshape(-1, C7_HQ, C7_D)
+        assert np.all(np.isfinite(out)), staged
+        assert normwise_rel_err(out[rows], ref) <= REL_TOL, staged
