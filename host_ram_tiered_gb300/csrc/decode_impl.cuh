@@ -311,9 +311,11 @@ __device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const ui
         sc[h] = mfma_hi<KVT>(ws.q[h][2 * i + 1], k1, sc[h]);
       }
     }
-    const float ds = d * scale_log2;
+    // explicit roundings (never contracted into FMAs): the same bits whatever
+    // code the compiler generates around them
+    const float ds = __fmul_rn(d, scale_log2);
 #pragma unroll
-    for (int h = 0; h < G; ++h) part[h] = ds * ((sb[h] + sc[h]) + ws.qb[h]);
+    for (int h = 0; h < G; ++h) part[h] = __fmul_rn(ds, __fadd_rn(__fadd_rn(sb[h], sc[h]), ws.qb[h]));
   } else {
     const uint4 *kp = (const uint4 *)(row + g * S::HB + qq * S::DL * 2);
     float sc[G];                                         // second chain per head
@@ -332,7 +334,7 @@ __device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const ui
         }
     }
 #pragma unroll
-    for (int h = 0; h < G; ++h) part[h] = (sb[h] + sc[h]) * scale_log2;
+    for (int h = 0; h < G; ++h) part[h] = __fmul_rn(__fadd_rn(sb[h], sc[h]), scale_log2);
   }
 }
 
@@ -360,7 +362,7 @@ __device__ __forceinline__ void qk_tile(const WarpState<KVT, G, D> &ws, const ui
       for (int h = 0; h < G; ++h) {
         const float mine = hi ? v[2 * i + 1][h] : v[2 * i][h];
         const float other = hi ? v[2 * i][h] : v[2 * i + 1][h];
-        v[i][h] = mine + __shfl_xor_sync(0xffffffffu, other, S::CPP << k);
+        v[i][h] = __fadd_rn(mine, __shfl_xor_sync(0xffffffffu, other, S::CPP << k));
       }
   }
 #pragma unroll
@@ -472,7 +474,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
             for (int e = 0; e < 4; ++e) sum += h2f(uw[e] & 0xffff, QT) + h2f(uw[e] >> 16, QT);
           }
         }
-        ws.qb[h] = -1152.f * sum;
+        ws.qb[h] = __fmul_rn(-1152.f, sum);
         ws.m[h] = -INFINITY;
         ws.l[h] = 0.f;
 #pragma unroll
@@ -526,21 +528,22 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       float s[G];
       qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, s);
       bool valid = lane < n;
-      if constexpr (SP) valid = valid && sparse_row(a, a.indices[(int64_t)b * a.max_ctx + sel0 + t0 + lane], false);
+      if constexpr (SP)                      // staged picks are grouped inside the window already
+        if (!a.offs) valid = valid && sparse_row(a, a.indices[(int64_t)b * a.max_ctx + sel0 + t0 + lane], false);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float sv_h = valid ? s[h] : -INFINITY;
         const float tmax = warp_max(sv_h);
         if (tmax > ws.m[h] + 8.f) {          // warp-uniform: move the reference
-          const float alpha = exp2f(ws.m[h] - tmax);
+          const float alpha = exp2f(__fsub_rn(ws.m[h], tmax));
           const uint64_t aa = pk2(alpha, alpha);
-          ws.l[h] *= alpha;
+          ws.l[h] = __fmul_rn(ws.l[h], alpha);
 #pragma unroll
           for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = fmul2(ws.acc[h][i], aa);
           ws.m[h] = tmax;
         }
-        const float p = valid ? exp2f(sv_h - ws.m[h]) : 0.f;
-        ws.l[h] += p;
+        const float p = valid ? exp2f(__fsub_rn(sv_h, ws.m[h])) : 0.f;
+        ws.l[h] = __fadd_rn(ws.l[h], p);
         pbuf[lane * GP + h] = pk2(p, p);
       }
       __syncwarp();
