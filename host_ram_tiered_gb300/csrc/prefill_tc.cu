@@ -178,6 +178,62 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// All 128 fp32 columns of this thread's TMEM lane in one load and one wait
+// (one round trip for the whole S row).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float *v) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,"
+      "%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+      "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),
+        "=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),
+        "=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),
+        "=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63]),
+        "=r"(r[64]),"=r"(r[65]),"=r"(r[66]),"=r"(r[67]),"=r"(r[68]),"=r"(r[69]),"=r"(r[70]),"=r"(r[71]),"=r"(r[72]),"=r"(r[73]),"=r"(r[74]),"=r"(r[75]),"=r"(r[76]),"=r"(r[77]),"=r"(r[78]),"=r"(r[79]),
+        "=r"(r[80]),"=r"(r[81]),"=r"(r[82]),"=r"(r[83]),"=r"(r[84]),"=r"(r[85]),"=r"(r[86]),"=r"(r[87]),"=r"(r[88]),"=r"(r[89]),"=r"(r[90]),"=r"(r[91]),"=r"(r[92]),"=r"(r[93]),"=r"(r[94]),"=r"(r[95]),
+        "=r"(r[96]),"=r"(r[97]),"=r"(r[98]),"=r"(r[99]),"=r"(r[100]),"=r"(r[101]),"=r"(r[102]),"=r"(r[103]),"=r"(r[104]),"=r"(r[105]),"=r"(r[106]),"=r"(r[107]),"=r"(r[108]),"=r"(r[109]),"=r"(r[110]),"=r"(r[111]),
+        "=r"(r[112]),"=r"(r[113]),"=r"(r[114]),"=r"(r[115]),"=r"(r[116]),"=r"(r[117]),"=r"(r[118]),"=r"(r[119]),"=r"(r[120]),"=r"(r[121]),"=r"(r[122]),"=r"(r[123]),"=r"(r[124]),"=r"(r[125]),"=r"(r[126]),"=r"(r[127])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed fp32 pairs (low word = first element).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -468,86 +524,94 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       tc_fence_after();
       const int64_t t0 = a.c0 + (int64_t)j * BN;
       const bool need_mask = (t0 + BN > c_end) || (t0 + BN - 1 > first_pos) || !row_ok;
-      // pass 1: row max of the raw scores (scale > 0), 8 independent chains,
-      // 32 columns at a time
+      // The whole S row of this thread in registers: one TMEM round trip.
+      // Row max of the raw scores (scale > 0), 8 chains of 3-input maxima.
+      float x[BN];
+      tmem_ld128(s_addr, x);
+      if (need_mask) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          const int64_t cj = t0 + i;
+          if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
+        }
+      }
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        float x[32];
-        tmem_ld32(s_addr + c * 32, x);
-        if (need_mask) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int64_t cj = t0 + c * 32 + i;
-            if (!row_ok || cj >= c_end || cj > pos) x[i] = -INFINITY;
-          }
-        }
+      for (int i = 0; i < BN; i += 16)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
-      }
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * a.scale_log2;
+        for (int k = 0; k < 8; ++k) mx[k] = max3(mx[k], x[i + 2 * k], x[i + 2 * k + 1]);
+      const float mt = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+                       a.scale_log2;
       // Lazy rescale (warp-uniform: tcgen05.ld/st are warp-collective): a row
       // whose tile max exceeds its reference by more than 2^8 moves its
       // reference to the tile max and rescales l and O by 2^(old - new).
       const bool mine = mt > m_used + kLazy;
       float alpha = 1.f;
       if (mine) alpha = m_used == -INFINITY ? 0.f : exp2f(m_used - mt);
-      if (__any_sync(0xffffffffu, mine)) {
-        l *= alpha;
-        if (o_valid) {
-          if (j > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[q], (j - 1) & 1, P.err));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          float v[32];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(o_addr + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(o_addr + c * 32, v);
-          }
-          tmem_wait_st();
-        }
-      }
+      const bool rescale = __any_sync(0xffffffffu, mine);
+      if (rescale) l *= alpha;
       if (mine) m_used = mt;
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
-      // pass 2: P = 2^(s*scale - ref), written back over the S columns it
-      // came from: chunk c (cells 32c..32c+31) -> hi pairs in columns
-      // 32c..32c+15, lo pairs in 32c+16..32c+31.  The PV of the previous tile
-      // read these columns before this tile's S was written into them.
-      float sm[8];
+      // P = 2^(s*scale - ref) from the registers (a masked score is -inf and
+      // gives +0), written back over the S columns it came from: chunk c
+      // (cells 32c..32c+31) -> hi pairs in columns 32c..32c+15, lo pairs in
+      // 32c+16..32c+31.  The PV of the previous tile read these columns before
+      // this tile's S was written into them.  Arguments, sums and residuals
+      // run as packed fp32 pairs.
+      const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nr2 = pk2(nref, nref);
+      uint64_t sm2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sm[k] = 0.f;
-#pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
-        float x[32];
-        tmem_ld32(s_addr + c * 32, x);
-        if (need_mask) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int64_t cj = t0 + c * 32 + i;
-            const bool off = !row_ok || cj >= c_end || cj > pos;
-            x[i] = off ? 0.f : ex2(fmaf(x[i], a.scale_log2, nref));
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = ex2(fmaf(x[i], a.scale_log2, nref));
-        }
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          sm[e & 7] += x[2 * e] + x[2 * e + 1];
-          split2<DT>(x[2 * e], x[2 * e + 1], w[e], w[16 + e]);
+          float a0, a1;
+          upk2(ffma2(pk2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nr2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          const uint64_t pp = pk2(p0, p1);
+          sm2[e & 3] = fadd2(sm2[e & 3], pp);
+          if constexpr (DT == KVO_BF16) {
+            // hi: the upper halves (truncation, exact in fp32); lo: the rounded residual
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(w[e]) : "r"(b0), "r"(b1));
+            float r0, r1;
+            upk2(fsub2(pp, pk2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u))), r0, r1);
+            w[16 + e] = pack2<DT>(r0, r1);
+          } else {
+            split2<DT>(p0, p1, w[e], w[16 + e]);
+          }
         }
         tmem_st32u(s_addr + c * 32, w);
       }
-      l += ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+      {
+        float u0, u1, u2, u3, u4, u5, u6, u7;
+        upk2(sm2[0], u0, u1);
+        upk2(sm2[1], u2, u3);
+        upk2(sm2[2], u4, u5);
+        upk2(sm2[3], u6, u7);
+        l += ((u0 + u2) + (u4 + u6)) + ((u1 + u3) + (u5 + u7));
+      }
       tmem_wait_st();
+      // O follows a moved reference (after P, so that S no longer occupies
+      // registers): wait until the previous tile's PV has finished with it.
+      if (rescale && o_valid) {
+        if (j > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&o_done[q], (j - 1) & 1, P.err));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(o_addr + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(o_addr + c * 32, v);
+        }
+        tmem_wait_st();
+      }
       tc_fence_before();
       mbar_arrive(&p_full[q]);
       o_valid = true;
