@@ -863,9 +863,13 @@ def gpu_launch_count(K, rows):
         # direct: head + host tail, 2 row blocks each
         n += K * (2 + 48 * 2) + min(K, 3) * 4
     if "c7" in rows:
-        # staged: partition + 32 buckets x (page gather + 2 row blocks x (split + combine));
-        # direct: 2 row blocks x (split + combine)
-        n += K * (1 + 32 * (1 + 2 * 2)) + max(1, min(K, 2)) * 4
+        # staged: partition + buckets x (page gather + 2 row blocks x (split + combine)), the
+        # arena holding two slots of arena / (4 page_bytes) pages; direct: 2 row blocks x
+        # (split + combine)
+        page_bytes = C7_PS * C7_HKV * C7_D * 2
+        slot = C7_ARENA // (4 * page_bytes)
+        buckets = -(-(C7_L // C7_PS) // slot)
+        n += K * (1 + buckets * (1 + 2 * 2)) + max(1, min(K, 2)) * 4
     return n
 
 
