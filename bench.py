@@ -888,9 +888,79 @@ def cpu_baseline():
         step()
         n += 1
     dt = (time.perf_counter() - t0) / n
-    return {"value": dt * 1e6 * (C3_HQ / heads), "unit": "us/step", "cores": threads, "kind": "oracle",
-            "sample": f"{heads} of {C3_HQ} query heads per step over the full 184,320 cells, "
-                      f"{n} steps, scaled x{C3_HQ // heads}"}
+    out = {"value": dt * 1e6 * (C3_HQ / heads), "unit": "us/step", "cores": threads, "kind": "oracle",
+           "sample": f"{heads} of {C3_HQ} query heads per step over the full 184,320 cells, "
+                     f"{n} steps, scaled x{C3_HQ // heads}"}
+    out["rows"] = cpu_rows(threads)
+    return out
+
+
+def _timed(fn, budget_s=3.0, max_n=20, warm=True):
+    if warm:
+        fn()
+    t0 = time.perf_counter()
+    n = 0
+    while n < 1 or (time.perf_counter() - t0 < budget_s and n < max_n):
+        fn()
+        n += 1
+    return (time.perf_counter() - t0) / n
+
+
+def cpu_rows(threads):
+    """The oracle on bounded samples of the other rows, scaled to one step of
+    each workload (the swap and gather oracles are single-threaded memcpy
+    loops; the attention oracles run on `threads` cores)."""
+    import oracle
+    res = {}
+    # swap, 32 KiB pages: 4,096 of the 131,072 descriptors, host to host
+    page, nd = 32768, 4096
+    src = np.zeros(nd * page, np.uint8)
+    dst = np.zeros(nd * page, np.uint8)
+    perm = synth.rng(SEED0 + 1, 9).permutation(nd)
+    s_ptr = (src.ctypes.data + perm.astype(np.uint64) * page).astype(np.uint64)
+    d_ptr = (dst.ctypes.data + np.arange(nd, dtype=np.uint64) * page).astype(np.uint64)
+    sizes = np.full(nd, page, np.int64)
+    dt = _timed(lambda: oracle.swap_blocks(s_ptr, d_ptr, sizes))
+    res["c2_swap_32KiB"] = {"value": dt * 1e6 * (131072 / nd), "unit": "us/step",
+                            "sample": f"{nd} of 131,072 descriptors, scaled x{131072 // nd}", "cores": 1}
+    del src, dst
+    # gather: 64 blocks of 64 tokens per (sequence, kv head), 8 x 4 x 128 bf16 planes of 65,536 tokens
+    # (the same 64 MiB copied as the full 2^20-token planes)
+    T = 65536
+    plane = np.zeros((C4_S, T, C4_HKV, C4_D), np.uint16)
+    sel = synth.topk_selection(C4_S, C4_HKV, T // 64, 64, synth.rng(SEED0 + 3, 9))
+    dt = _timed(lambda: oracle.gather_blocks(plane, C4_S, T, C4_HKV, C4_D, 2, 64, sel))
+    res["c4_gather"] = {"value": dt * 1e6 * 2, "unit": "us/step",
+                        "sample": "K plane only (x2 for K and V), 65,536-token planes, full selection",
+                        "cores": 1}
+    del plane
+    # sparse decode over the 4,096 gathered cells: full size
+    g = synth.rng(SEED0 + 3, 10)
+    cells = C4_S * 4096
+    kb = synth.normal_bits((cells, C4_HKV * C4_D), "bf16", g).view(np.uint8)
+    vb = synth.normal_bits((cells, C4_HKV * C4_D), "bf16", g).view(np.uint8)
+    qb = synth.normal_bits((C4_S, C4_HQ, C4_D), "bf16", g)
+    cache = oracle.make_cache(kb, vb, None, None, 4096, 0, 4096, oracle.BF16, C4_HKV, C4_D)
+    dt = _timed(lambda: oracle.attn_decode(cache, qb, oracle.BF16, C4_S, C4_HQ, [4096] * C4_S,
+                                           1.0 / math.sqrt(C4_D)))
+    res["c4_sparse_decode"] = {"value": dt * 1e6, "unit": "us/step", "sample": "full step", "cores": threads}
+    del kb, vb
+    # prefill: 2 of the 2,048 rows (all 32 heads) over the full 262,144 cells
+    rb = C5_HKV * C5_D * 2
+    kc = np.empty(C5_L * rb // 2, np.uint16)
+    vc = np.empty(C5_L * rb // 2, np.uint16)
+    synth.fill_normal_bits_large(kc, "bf16", SEED0 + 4, 11)
+    synth.fill_normal_bits_large(vc, "bf16", SEED0 + 4, 12)
+    q5 = synth.normal_bits((2, C5_HQ, C5_D), "bf16", synth.rng(SEED0 + 4, 13))
+    cache = oracle.make_cache(kc.view(np.uint8), vc.view(np.uint8), None, None, C5_L, 0, C5_L, oracle.BF16,
+                              C5_HKV, C5_D)
+    dt = _timed(lambda: oracle.attn_prefill(cache, q5, oracle.BF16, 2, C5_POS0 + C5_R - 2, C5_HQ, C5_L,
+                                            1.0 / math.sqrt(C5_D)), budget_s=0.0, max_n=1, warm=False)
+    res["c5_prefill"] = {"value": dt * 1e6 * (C5_R / 2), "unit": "us/step",
+                         "sample": "2 of 2,048 rows (the last positions, 64 tasks), one run, scaled x1024",
+                         "cores": threads}
+    del kc, vc
+    return res
 
 
 if __name__ == "__main__":
