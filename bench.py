@@ -594,7 +594,7 @@ def main(argv=None):
     ap.add_argument("--rows", default="all",
                     help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append), "
                          "c7 (QSA sparse rows), c3vram (the 184,320-cell all-VRAM decode alone; not in "
-                         "'all') (default all)")
+                         "'all') (default: all rows at one GPU, the headline alone under torchrun)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -614,7 +614,15 @@ def main(argv=None):
     build.build()
     k = kvo()
     k.load()
-    rows = set(args.rows.split(",")) if args.rows != "all" else {"head", "c1", "c2", "c3", "c4", "c5", "c6", "c7"}
+    # Every row at one GPU.  Under torchrun each rank replicates the workload,
+    # so the default there is the headline alone (the full set would pin about
+    # 30 GB of host memory per rank).
+    if args.rows == "all" and world > 1:
+        rows = {"head"}
+    elif args.rows == "all":
+        rows = {"head", "c1", "c2", "c3", "c4", "c5", "c6", "c7"}
+    else:
+        rows = set(args.rows.split(","))
     timer = Timer()
     peaks = measure_link_peak(timer)
     hbm = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs", 6789.0) \
@@ -777,7 +785,7 @@ def main(argv=None):
     clk = clocks.stop()
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
     if rank == 0 and head is None:
         # a subset of rows without the headline (profiling runs)
