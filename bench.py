@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 from host_ram_tiered_gb300 import synth  # noqa: E402
 
 METRIC = "tiered-KV decode µs/step & host-link GB/s (% of measured pinned-copy peak)"
-HEADLINE = "c3_q8_0_decode_L184320_N8192_direct"
+HEADLINE = "q8_0_decode_L184320_N8192_direct"
 SEED0 = 1234
 
 
@@ -162,9 +162,9 @@ class Clocks:
                 "samples": len(sm)}
 
 
-# ----------------------------------------------------------------- C1 tiny
+# ----------------------------------------------------------------- tiny paged cache (swap + decode)
 
-def c1_setup(seed=SEED0):
+def tiny_setup(seed=SEED0):
     """Tiny case: 2 layers x K,V paged fp16 (16 tokens x 8 heads x 128 = 32 KiB
     pages), 64 seeded blocks swapped between 128-block pools; decode for one
     sequence, 32 q / 8 kv heads, 1024 cells with 512 in VRAM."""
@@ -207,7 +207,7 @@ def c1_setup(seed=SEED0):
     return st
 
 
-def c1_decode(st, staging):
+def tiny_decode(st, staging):
     k = kvo()
     L, N = st["L"], st["N"]
     k.kvo_attn_decode_tiered(st["q"], k.F16, 1, st["hq"], st["hkv"], 128, st["k_head"], st["v_head"], N,
@@ -216,38 +216,38 @@ def c1_decode(st, staging):
                              st["stage_v"] if staging else None, st["out"], st["ws"], st["ws_bytes"])
 
 
-# ----------------------------------------------------------------- C2 swap
+# ----------------------------------------------------------------- 32-layer offload swap
 
-C2_TENSORS, C2_GPU_BLOCKS, C2_HOST_CHUNKS, C2_BLOCKS, C2_BPC, C2_SKIP = 64, 4096, 640, 2048, 4, 1
+SWAP_TENSORS, SWAP_GPU_BLOCKS, SWAP_HOST_CHUNKS, SWAP_BLOCKS, SWAP_BPC, SWAP_SKIP = 64, 4096, 640, 2048, 4, 1
 
 
-def c2_setup(page, seed=SEED0 + 1):
+def swap_setup(page, seed=SEED0 + 1):
     """vLLM-style CPU offload swap: 64 paged tensors (32 layers x K,V), 2048
     seeded GPU block ids per direction, host chunks of 4 pages with a row
     stride of 1.5 x the chunk, skip 1 on the first chunk."""
     k = kvo()
-    row = C2_BPC * page
+    row = SWAP_BPC * page
     stride = row * 3 // 2
-    gpu_bytes = C2_GPU_BLOCKS * page
-    host_bytes = C2_HOST_CHUNKS * stride
-    d = dev(C2_TENSORS * gpu_bytes)
-    h = pinned(C2_TENSORS * host_bytes)
-    init = np.empty(C2_TENSORS * gpu_bytes, np.uint8)
+    gpu_bytes = SWAP_GPU_BLOCKS * page
+    host_bytes = SWAP_HOST_CHUNKS * stride
+    d = dev(SWAP_TENSORS * gpu_bytes)
+    h = pinned(SWAP_TENSORS * host_bytes)
+    init = np.empty(SWAP_TENSORS * gpu_bytes, np.uint8)
     synth.fill_bytes_large(init, seed, 2)
     d.copy_(torch().from_numpy(init))
     synth.fill_bytes_large(h.numpy(), seed, 3)
     g = synth.rng(seed, 4)
-    gpu_ids = g.permutation(C2_GPU_BLOCKS)[:C2_BLOCKS].astype(np.int64)
-    need = -(-(C2_BLOCKS + C2_SKIP) // C2_BPC)
-    host_ids = g.permutation(C2_HOST_CHUNKS)[:need].astype(np.int64)
-    n_desc = C2_TENSORS * C2_BLOCKS
+    gpu_ids = g.permutation(SWAP_GPU_BLOCKS)[:SWAP_BLOCKS].astype(np.int64)
+    need = -(-(SWAP_BLOCKS + SWAP_SKIP) // SWAP_BPC)
+    host_ids = g.permutation(SWAP_HOST_CHUNKS)[:need].astype(np.int64)
+    n_desc = SWAP_TENSORS * SWAP_BLOCKS
     hp = np.empty(n_desc, np.int64)
     gp = np.empty(n_desc, np.int64)
-    for i in range(C2_TENSORS):
-        k.kvo_sub_block_ptrs(host_ids.ctypes.data, need, C2_BPC, C2_SKIP, h.data_ptr() + i * host_bytes,
-                             stride, row, hp[i * C2_BLOCKS:].ctypes.data, C2_BLOCKS)
-        k.kvo_sub_block_ptrs(gpu_ids.ctypes.data, C2_BLOCKS, 1, 0, d.data_ptr() + i * gpu_bytes,
-                             page, page, gp[i * C2_BLOCKS:].ctypes.data, C2_BLOCKS)
+    for i in range(SWAP_TENSORS):
+        k.kvo_sub_block_ptrs(host_ids.ctypes.data, need, SWAP_BPC, SWAP_SKIP, h.data_ptr() + i * host_bytes,
+                             stride, row, hp[i * SWAP_BLOCKS:].ctypes.data, SWAP_BLOCKS)
+        k.kvo_sub_block_ptrs(gpu_ids.ctypes.data, SWAP_BLOCKS, 1, 0, d.data_ptr() + i * gpu_bytes,
+                             page, page, gp[i * SWAP_BLOCKS:].ctypes.data, SWAP_BLOCKS)
     sizes = pinned_i64(np.full(n_desc, page, np.int64))
     st = {"page": page, "dev": d, "host": h, "n_desc": n_desc, "sizes": sizes,
           "h2d_src": pinned_i64(hp), "h2d_dst": pinned_i64(gp),
@@ -258,7 +258,7 @@ def c2_setup(page, seed=SEED0 + 1):
     return st
 
 
-def c2_run(st, h2d, flags=0):
+def swap_run(st, h2d, flags=0):
     k = kvo()
     if h2d:
         k.kvo_swap_blocks_batch(st["h2d_src"], st["h2d_dst"], st["sizes"], st["n_desc"],
@@ -268,50 +268,50 @@ def c2_run(st, h2d, flags=0):
                                 k.KVO_SWAP_D2H | flags)
 
 
-# ----------------------------------------------------------------- C3 decode
+# ----------------------------------------------------------------- q8_0 tiered decode
 
-C3_HQ, C3_HKV, C3_D = 48, 8, 128
-C3_LS = (29696, 96256, 184320)
-C3_NS = (8192, 94208)
+DEC_HQ, DEC_HKV, DEC_D = 48, 8, 128
+DEC_LS = (29696, 96256, 184320)
+DEC_NS = (8192, 94208)
 
 
-def c3_setup(seed=SEED0 + 2, l_max=max(C3_LS), n_max=max(C3_NS)):
+def dec_setup(seed=SEED0 + 2, l_max=max(DEC_LS), n_max=max(DEC_NS)):
     """llama.cpp-style tiered decode, q8_0 K/V (blocks of 32 int8 uniform in
     [-127, 127] and an fp16 scale ~U(0.001, 0.02)), one layer, batch 1."""
     t = torch()
     g = synth.rng(seed, 1)
-    rb = C3_HKV * (C3_D // 32) * 34
+    rb = DEC_HKV * (DEC_D // 32) * 34
     k_all = pinned(l_max * rb)
     v_all = pinned(l_max * rb)
     chunk = 16384
     for c0 in range(0, l_max, chunk):
         n = min(chunk, l_max - c0)
-        k_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, C3_HKV, C3_D, g).reshape(-1)
-        v_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, C3_HKV, C3_D, g).reshape(-1)
-    q = synth.normal_bits((1, C3_HQ, C3_D), "f16", g)
+        k_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, DEC_HKV, DEC_D, g).reshape(-1)
+        v_all.numpy()[c0 * rb:(c0 + n) * rb] = synth.q8_0_rows(n, DEC_HKV, DEC_D, g).reshape(-1)
+    q = synth.normal_bits((1, DEC_HQ, DEC_D), "f16", g)
     st = {"rb": rb, "k_host": k_all, "v_host": v_all,
           "k_dev": k_all[:n_max * rb].cuda(), "v_dev": v_all[:n_max * rb].cuda(),
           "k_dev_all": k_all.cuda(), "v_dev_all": v_all.cuda(),
           "q_np": q, "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
-          "out": t.empty(C3_HQ * C3_D, dtype=t.float32, device="cuda"),
+          "out": t.empty(DEC_HQ * DEC_D, dtype=t.float32, device="cuda"),
           "stage_k": dev(l_max * rb), "stage_v": dev(l_max * rb)}
-    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(1, C3_HQ, C3_D, l_max)
+    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(1, DEC_HQ, DEC_D, l_max)
     st["ws"] = dev(st["ws_bytes"])
     st["ctx"] = {}
     return st
 
 
-def c3_ctx(st, L):
+def dec_ctx(st, L):
     t = torch()
     if L not in st["ctx"]:
         st["ctx"][L] = t.tensor([L], dtype=t.int32, device="cuda")
     return st["ctx"][L]
 
 
-def c3_run(st, L, N, staging=False, all_vram=False, q=None, out=None):
+def dec_run(st, L, N, staging=False, all_vram=False, q=None, out=None):
     k = kvo()
     rb = st["rb"]
-    ws_bytes = k.kvo_attn_decode_workspace_bytes(1, C3_HQ, C3_D, L)
+    ws_bytes = k.kvo_attn_decode_workspace_bytes(1, DEC_HQ, DEC_D, L)
     if all_vram:
         kh, vh, kt, vt, n = st["k_dev_all"], st["v_dev_all"], None, None, L
     else:
@@ -319,113 +319,113 @@ def c3_run(st, L, N, staging=False, all_vram=False, q=None, out=None):
         kh, vh = st["k_dev"], st["v_dev"]
         kt = st["k_host"].data_ptr() + n * rb
         vt = st["v_host"].data_ptr() + n * rb
-    k.kvo_attn_decode_tiered(q if q is not None else st["q"], k.F16, 1, C3_HQ, C3_HKV, C3_D,
-                             kh, vh, n, kt, vt, L - n, k.Q8_0, c3_ctx(st, L), L, n,
-                             1.0 / math.sqrt(C3_D),
+    k.kvo_attn_decode_tiered(q if q is not None else st["q"], k.F16, 1, DEC_HQ, DEC_HKV, DEC_D,
+                             kh, vh, n, kt, vt, L - n, k.Q8_0, dec_ctx(st, L), L, n,
+                             1.0 / math.sqrt(DEC_D),
                              st["stage_k"] if staging else None, st["stage_v"] if staging else None,
                              out if out is not None else st["out"], st["ws"], ws_bytes)
 
 
-def c3_bytes(L, N):
-    rb2 = 2 * C3_HKV * (C3_D // 32) * 34
+def dec_bytes(L, N):
+    rb2 = 2 * DEC_HKV * (DEC_D // 32) * 34
     return max(L - N, 0) * rb2, min(L, N) * rb2
 
 
-# ----------------------------------------------------------------- C4 gather + sparse decode
+# ----------------------------------------------------------------- top-k block gather + sparse decode
 
-C4_S, C4_T, C4_HQ, C4_HKV, C4_D, C4_BLK, C4_K = 8, 1 << 20, 16, 4, 128, 64, 64
+TOPK_S, TOPK_T, TOPK_HQ, TOPK_HKV, TOPK_D, TOPK_BLK, TOPK_K = 8, 1 << 20, 16, 4, 128, 64, 64
 
 
-def c4_setup(seed=SEED0 + 3):
+def topk_setup(seed=SEED0 + 3):
     """QSA-style sparse decode: bf16 K/V planes [8][2^20][4][128] in pinned
     host memory, 64 of 16,384 blocks per (sequence, kv head) selected
     without replacement (the last block always), gathered into VRAM, then
     decode over the 4096 gathered tokens."""
     t = torch()
-    plane = C4_S * C4_T * C4_HKV * C4_D
+    plane = TOPK_S * TOPK_T * TOPK_HKV * TOPK_D
     k_plane = pinned(plane * 2)
     v_plane = pinned(plane * 2)
     synth.fill_normal_bits_large(k_plane.numpy().view(np.uint16), "bf16", seed, 1)
     synth.fill_normal_bits_large(v_plane.numpy().view(np.uint16), "bf16", seed, 2)
     g = synth.rng(seed, 3)
-    sel = synth.topk_selection(C4_S, C4_HKV, C4_T // C4_BLK, C4_K, g)
-    q = synth.normal_bits((C4_S, C4_HQ, C4_D), "bf16", g)
-    tok = C4_K * C4_BLK
-    out_bytes = C4_S * tok * C4_HKV * C4_D * 2
+    sel = synth.topk_selection(TOPK_S, TOPK_HKV, TOPK_T // TOPK_BLK, TOPK_K, g)
+    q = synth.normal_bits((TOPK_S, TOPK_HQ, TOPK_D), "bf16", g)
+    tok = TOPK_K * TOPK_BLK
+    out_bytes = TOPK_S * tok * TOPK_HKV * TOPK_D * 2
     st = {"k_plane": k_plane, "v_plane": v_plane, "sel_np": sel,
           "sel": t.from_numpy(sel.reshape(-1).copy()).cuda(),
           "kg": dev(out_bytes), "vg": dev(out_bytes), "q_np": q,
           "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
-          "ctx": t.full((C4_S,), tok, dtype=t.int32, device="cuda"),
-          "out": t.empty(C4_S * C4_HQ * C4_D, dtype=t.float32, device="cuda"),
+          "ctx": t.full((TOPK_S,), tok, dtype=t.int32, device="cuda"),
+          "out": t.empty(TOPK_S * TOPK_HQ * TOPK_D, dtype=t.float32, device="cuda"),
           "gather_bytes": 2 * out_bytes}
-    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(C4_S, C4_HQ, C4_D, tok)
+    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(TOPK_S, TOPK_HQ, TOPK_D, tok)
     st["ws"] = dev(st["ws_bytes"])
     return st
 
 
-def c4_gather(st):
+def topk_gather(st):
     k = kvo()
-    k.kvo_gather_blocks(st["k_plane"], st["v_plane"], C4_S, C4_T, C4_HKV, C4_D, k.BF16, C4_BLK,
-                        st["sel"], C4_K, st["kg"], st["vg"])
+    k.kvo_gather_blocks(st["k_plane"], st["v_plane"], TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, k.BF16, TOPK_BLK,
+                        st["sel"], TOPK_K, st["kg"], st["vg"])
 
 
-def c4_decode(st):
+def topk_decode(st):
     k = kvo()
-    tok = C4_K * C4_BLK
-    k.kvo_attn_decode_tiered(st["q"], k.BF16, C4_S, C4_HQ, C4_HKV, C4_D, st["kg"], st["vg"], tok,
-                             None, None, 0, k.BF16, st["ctx"], tok, tok, 1.0 / math.sqrt(C4_D),
+    tok = TOPK_K * TOPK_BLK
+    k.kvo_attn_decode_tiered(st["q"], k.BF16, TOPK_S, TOPK_HQ, TOPK_HKV, TOPK_D, st["kg"], st["vg"], tok,
+                             None, None, 0, k.BF16, st["ctx"], tok, tok, 1.0 / math.sqrt(TOPK_D),
                              None, None, st["out"], st["ws"], st["ws_bytes"])
 
 
-# ----------------------------------------------------------------- C5 prefill
+# ----------------------------------------------------------------- tiered chunked prefill
 
-C5_R, C5_POS0, C5_L, C5_HQ, C5_HKV, C5_D, C5_N = 2048, 260096, 262144, 32, 8, 128, 65536
-C5_ARENA, C5_RPL = 32 << 20, 1024
+PF_R, PF_POS0, PF_L, PF_HQ, PF_HKV, PF_D, PF_N = 2048, 260096, 262144, 32, 8, 128, 65536
+PF_ARENA, PF_RPL = 32 << 20, 1024
 # FP32 multiply-adds per second on CUDA cores: 152 SMs x 128 lanes x 2.07 GHz
 FP32_FMA_PEAK = 152 * 128 * 2.07e9
 
 
-def c5_setup(seed=SEED0 + 4):
+def pf_setup(seed=SEED0 + 4):
     """Tiered chunked prefill: 2048 query rows at positions 260,096-262,143,
     bf16 K/V cells [262,144][8][128], cells [0, 65,536) in VRAM, the tail in
     pinned host memory; staged through a 32 MiB arena, 1024 rows a launch."""
     t = torch()
-    rb = C5_HKV * C5_D * 2
+    rb = PF_HKV * PF_D * 2
     g_seed = seed
-    k_host = pinned((C5_L - C5_N) * rb)
-    v_host = pinned((C5_L - C5_N) * rb)
-    k_head = np.empty(C5_N * rb // 2, np.uint16)
-    v_head = np.empty(C5_N * rb // 2, np.uint16)
+    k_host = pinned((PF_L - PF_N) * rb)
+    v_host = pinned((PF_L - PF_N) * rb)
+    k_head = np.empty(PF_N * rb // 2, np.uint16)
+    v_head = np.empty(PF_N * rb // 2, np.uint16)
     synth.fill_normal_bits_large(k_head, "bf16", g_seed, 1)
     synth.fill_normal_bits_large(v_head, "bf16", g_seed, 2)
     synth.fill_normal_bits_large(k_host.numpy().view(np.uint16), "bf16", g_seed, 3)
     synth.fill_normal_bits_large(v_host.numpy().view(np.uint16), "bf16", g_seed, 4)
-    q = synth.normal_bits((C5_R, C5_HQ, C5_D), "bf16", synth.rng(g_seed, 5))
+    q = synth.normal_bits((PF_R, PF_HQ, PF_D), "bf16", synth.rng(g_seed, 5))
     st = {"rb": rb, "k_host": k_host, "v_host": v_host, "k_head_np": k_head, "v_head_np": v_head,
           "k_head": t.from_numpy(k_head.view(np.int16)).cuda(),
           "v_head": t.from_numpy(v_head.view(np.int16)).cuda(), "q_np": q,
           "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
-          "arena": dev(C5_ARENA),
-          "out": t.empty(C5_R * C5_HQ * C5_D, dtype=t.float32, device="cuda")}
-    st["ws_bytes"] = kvo().kvo_attn_prefill_workspace_bytes(C5_R, C5_HQ)
+          "arena": dev(PF_ARENA),
+          "out": t.empty(PF_R * PF_HQ * PF_D, dtype=t.float32, device="cuda")}
+    st["ws_bytes"] = kvo().kvo_attn_prefill_workspace_bytes(PF_R, PF_HQ)
     st["ws"] = dev(st["ws_bytes"])
     return st
 
 
-def c5_run(st, staged=True, q=None, out=None):
+def pf_run(st, staged=True, q=None, out=None):
     k = kvo()
-    k.kvo_attn_prefill_tiered(q if q is not None else st["q"], C5_R, C5_POS0, C5_HQ, C5_HKV, C5_D,
-                              st["k_head"], st["v_head"], st["k_host"], st["v_host"], k.BF16, C5_L,
-                              C5_N, 1.0 / math.sqrt(C5_D),
-                              st["arena"] if staged else None, C5_ARENA if staged else 0, C5_RPL,
+    k.kvo_attn_prefill_tiered(q if q is not None else st["q"], PF_R, PF_POS0, PF_HQ, PF_HKV, PF_D,
+                              st["k_head"], st["v_head"], st["k_host"], st["v_host"], k.BF16, PF_L,
+                              PF_N, 1.0 / math.sqrt(PF_D),
+                              st["arena"] if staged else None, PF_ARENA if staged else 0, PF_RPL,
                               out if out is not None else st["out"], st["ws"], st["ws_bytes"])
 
 
-def c5_flops():
+def pf_flops():
     # causal: row i sees pos0 + i + 1 cells; QK^T and PV are 2 flops per MAC each
-    cells = sum(C5_POS0 + i + 1 for i in range(C5_R))
-    return 4.0 * C5_HQ * C5_D * cells
+    cells = sum(PF_POS0 + i + 1 for i in range(PF_R))
+    return 4.0 * PF_HQ * PF_D * cells
 
 
 # ----------------------------------------------------------------- QSA sparse rows (next row)
@@ -433,58 +433,58 @@ def c5_flops():
 # ExLlamaV3 QSA offload prefill: 2048 query rows, each picking 2080 cache
 # positions, over a paged fp16 host cache of 262,144 positions (1,024 pages
 # of 256 tokens, 32 q / 8 kv heads x 128), staged through a 32 MiB arena.
-C7_R, C7_POS0, C7_L, C7_PS, C7_KPAD = 2048, 260096, 262144, 256, 2080
-C7_HQ, C7_HKV, C7_D, C7_ARENA, C7_RPL = 32, 8, 128, 32 << 20, 1024
+SR_R, SR_POS0, SR_L, SR_PS, SR_KPAD = 2048, 260096, 262144, 256, 2080
+SR_HQ, SR_HKV, SR_D, SR_ARENA, SR_RPL = 32, 8, 128, 32 << 20, 1024
 
 
-def c7_setup(seed=SEED0 + 6):
+def sr_setup(seed=SEED0 + 6):
     t = torch()
-    n_pages = C7_L // C7_PS
-    page_bytes = C7_PS * C7_HKV * C7_D * 2
+    n_pages = SR_L // SR_PS
+    page_bytes = SR_PS * SR_HKV * SR_D * 2
     k_pages = pinned(n_pages * page_bytes)
     v_pages = pinned(n_pages * page_bytes)
     synth.fill_normal_bits_large(k_pages.numpy().view(np.uint16), "f16", seed, 1)
     synth.fill_normal_bits_large(v_pages.numpy().view(np.uint16), "f16", seed, 2)
     g = synth.rng(seed, 3)
     bt = g.permutation(n_pages).astype(np.int32)
-    idx = synth.row_selections(C7_R, C7_KPAD, C7_POS0, C7_KPAD, synth.rng(seed, 4))
-    q = synth.normal_bits((C7_R, C7_HQ, C7_D), "f16", synth.rng(seed, 5))
+    idx = synth.row_selections(SR_R, SR_KPAD, SR_POS0, SR_KPAD, synth.rng(seed, 4))
+    q = synth.normal_bits((SR_R, SR_HQ, SR_D), "f16", synth.rng(seed, 5))
     st = {"n_pages": n_pages, "page_bytes": page_bytes, "k_pages": k_pages, "v_pages": v_pages,
           "bt_np": bt, "idx_np": idx, "q_np": q, "bt": t.from_numpy(bt).cuda(),
           "idx": t.from_numpy(idx.reshape(-1).copy()).cuda(),
-          "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(), "arena": dev(C7_ARENA),
-          "out": t.empty(C7_R * C7_HQ * C7_D, dtype=t.float32, device="cuda")}
+          "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(), "arena": dev(SR_ARENA),
+          "out": t.empty(SR_R * SR_HQ * SR_D, dtype=t.float32, device="cuda")}
     k = kvo()
-    st["ws_bytes"] = max(k.kvo_attn_sparse_rows_workspace_bytes(C7_R, C7_HQ, C7_HKV, C7_D, C7_KPAD, C7_RPL,
-                                                                C7_PS, n_pages, a)
-                         for a in (0, C7_ARENA))
+    st["ws_bytes"] = max(k.kvo_attn_sparse_rows_workspace_bytes(SR_R, SR_HQ, SR_HKV, SR_D, SR_KPAD, SR_RPL,
+                                                                SR_PS, n_pages, a)
+                         for a in (0, SR_ARENA))
     st["ws"] = dev(st["ws_bytes"])
     return st
 
 
-def c7_run(st, staged=True):
+def sr_run(st, staged=True):
     k = kvo()
-    k.kvo_attn_sparse_rows(st["q"], k.F16, C7_R, C7_HQ, C7_HKV, C7_D, st["k_pages"], st["v_pages"], k.F16,
-                           C7_PS, st["n_pages"], st["bt"], st["n_pages"], st["idx"], C7_KPAD,
-                           1.0 / math.sqrt(C7_D), st["arena"] if staged else None, C7_ARENA if staged else 0,
-                           C7_RPL, st["out"], st["ws"], st["ws_bytes"])
+    k.kvo_attn_sparse_rows(st["q"], k.F16, SR_R, SR_HQ, SR_HKV, SR_D, st["k_pages"], st["v_pages"], k.F16,
+                           SR_PS, st["n_pages"], st["bt"], st["n_pages"], st["idx"], SR_KPAD,
+                           1.0 / math.sqrt(SR_D), st["arena"] if staged else None, SR_ARENA if staged else 0,
+                           SR_RPL, st["out"], st["ws"], st["ws_bytes"])
 
 
 # ----------------------------------------------------------------- write path (append)
 
-def c6_setup(seed=SEED0 + 5):
-    """Appends into the host tails of the C3 (q8_0) and C5 (bf16) caches: one
+def append_setup(seed=SEED0 + 5):
+    """Appends into the host tails of the q8_0 decode cache and the bf16 prefill cache: one
     decode token (q8_0) and one 2048-token prefill chunk (q8_0 and bf16)."""
     t = torch()
     g = synth.rng(seed, 1)
     n = 2048
     st = {"n": n}
-    for name, hkv in (("q8", C3_HKV), ("bf", C5_HKV)):
+    for name, hkv in (("q8", DEC_HKV), ("bf", PF_HKV)):
         x = synth.normal_bits((n, hkv * 128), "bf16" if name == "bf" else "f16", g)
         st[name + "_k"] = t.from_numpy(x.view(np.int16).reshape(-1).copy()).cuda()
         st[name + "_v"] = t.from_numpy(x[::-1].copy().view(np.int16).reshape(-1)).cuda()
-    st["q8_rb"] = C3_HKV * 4 * 34
-    st["bf_rb"] = C5_HKV * 128 * 2
+    st["q8_rb"] = DEC_HKV * 4 * 34
+    st["bf_rb"] = PF_HKV * 128 * 2
     cap = 8192 + 4096
     st["cap"] = cap
     st["q8_tail_k"] = pinned((cap - 8192) * st["q8_rb"])
@@ -496,44 +496,44 @@ def c6_setup(seed=SEED0 + 5):
     return st
 
 
-def c6_run(st, which, n_tokens):
+def append_run(st, which, n_tokens):
     k = kvo()
     q8 = which == "q8"
     k.kvo_append_kv_tiered(st[which + "_k"], st[which + "_v"], k.F16 if q8 else k.BF16, n_tokens,
-                           8192 + 1000, C3_HKV if q8 else C5_HKV, 128, st[which + "_head"],
+                           8192 + 1000, DEC_HKV if q8 else PF_HKV, 128, st[which + "_head"],
                            st[which + "_head"], st[which + "_tail_k"], st[which + "_tail_v"],
                            k.Q8_0 if q8 else k.BF16, 8192, st["cap"])
 
 
 # ----------------------------------------------------------------- CPU oracle arm
 
-def oracle_c3_step(L, heads=C3_HQ):
+def oracle_c3_step(L, heads=DEC_HQ):
     """fp64 oracle decode of the headline workload (q8_0, L cells, N split),
     on host copies of the same seeded inputs."""
     import oracle
     g = synth.rng(SEED0 + 2, 1)
-    rb = C3_HKV * (C3_D // 32) * 34
+    rb = DEC_HKV * (DEC_D // 32) * 34
     k = np.empty((L, rb), np.uint8)
     v = np.empty((L, rb), np.uint8)
     chunk = 16384
-    for c0 in range(0, max(C3_LS), chunk):
-        n = min(chunk, max(C3_LS) - c0)
-        kk = synth.q8_0_rows(n, C3_HKV, C3_D, g)
-        vv = synth.q8_0_rows(n, C3_HKV, C3_D, g)
+    for c0 in range(0, max(DEC_LS), chunk):
+        n = min(chunk, max(DEC_LS) - c0)
+        kk = synth.q8_0_rows(n, DEC_HKV, DEC_D, g)
+        vv = synth.q8_0_rows(n, DEC_HKV, DEC_D, g)
         if c0 < L:
             m = min(n, L - c0)
             k[c0:c0 + m] = kk[:m]
             v[c0:c0 + m] = vv[:m]
-    q = synth.normal_bits((1, C3_HQ, C3_D), "f16", g)
+    q = synth.normal_bits((1, DEC_HQ, DEC_D), "f16", g)
     N = 8192
     kh, vh = np.ascontiguousarray(k[:N]), np.ascontiguousarray(v[:N])
     kt, vt = np.ascontiguousarray(k[N:]), np.ascontiguousarray(v[N:])
-    cache = oracle.make_cache(kh, vh, kt, vt, N, L - N, N, oracle.Q8_0, C3_HKV, C3_D)
+    cache = oracle.make_cache(kh, vh, kt, vt, N, L - N, N, oracle.Q8_0, DEC_HKV, DEC_D)
     keep = (kh, vh, kt, vt)
     qs = np.ascontiguousarray(q[:, :heads])
 
     def step():
-        return oracle.attn_decode(cache, qs, oracle.F16, 1, heads, [L], 1.0 / math.sqrt(C3_D))
+        return oracle.attn_decode(cache, qs, oracle.F16, 1, heads, [L], 1.0 / math.sqrt(DEC_D))
     return step, keep
 
 
@@ -541,7 +541,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     threads = oracle.set_threads(os.cpu_count() or 1)
-    L = max(C3_LS)
+    L = max(DEC_LS)
     # Bounded sample: the oracle decodes 8 of the 48 query heads per step
     # (one kv head's worth of GQA rows is 6; 8 keeps the time per step near
     # a second on 16 Grace cores), scaled to a full step by 48/8.
@@ -553,16 +553,16 @@ def run_reference(args):
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    us = dt / args.steps * 1e6 * (C3_HQ / heads)
-    host_b, dev_b = c3_bytes(L, 8192)
+    us = dt / args.steps * 1e6 * (DEC_HQ / heads)
+    host_b, dev_b = dec_bytes(L, 8192)
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": HEADLINE, "L": L, "n_vram_cells": 8192, "q_heads": C3_HQ,
-                       "kv_heads": C3_HKV, "head_dim": C3_D, "kv_dtype": "q8_0", "batch": 1},
+            "config": {"workload": HEADLINE, "L": L, "n_vram_cells": 8192, "q_heads": DEC_HQ,
+                       "kv_heads": DEC_HKV, "head_dim": DEC_D, "kv_dtype": "q8_0", "batch": 1},
             "cpu_baseline": {"value": us, "unit": "us/step", "cores": threads, "kind": "oracle",
-                             "sample": f"{heads} of {C3_HQ} query heads per step, scaled x{C3_HQ // heads}"},
+                             "sample": f"{heads} of {DEC_HQ} query heads per step, scaled x{DEC_HQ // heads}"},
             "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "host_gbs_equiv": host_b / (us * 1e-6) / 1e9}
     return line
@@ -592,8 +592,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of head (headline decode only), c1, c2, c3, c4, c5, c6 (append), "
-                         "c7 (QSA sparse rows), c3vram (the 184,320-cell all-VRAM decode alone; not in "
+                    help="comma list of head (headline decode only), tiny, swap, decode, topk, prefill, "
+                         "append, sparse (QSA sparse rows), decode_vram (the 184,320-cell all-VRAM decode alone; not in "
                          "'all') (default: all rows at one GPU, the headline alone under torchrun)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -620,7 +620,7 @@ def main(argv=None):
     if args.rows == "all" and world > 1:
         rows = {"head"}
     elif args.rows == "all":
-        rows = {"head", "c1", "c2", "c3", "c4", "c5", "c6", "c7"}
+        rows = {"head", "tiny", "swap", "decode", "topk", "prefill", "append", "sparse"}
     else:
         rows = set(args.rows.split(","))
     timer = Timer()
@@ -637,110 +637,110 @@ def main(argv=None):
         t.cuda.synchronize()
 
     clocks = Clocks()
-    # ---- headline: C3 decode at L = 184,320, N = 8,192, direct
+    # ---- headline: q8_0 tiered decode at L = 184,320, N = 8,192, direct
     head = None
-    if "c3" in rows or "head" in rows:
-        st3 = c3_setup()
+    if "decode" in rows or "head" in rows:
+        st3 = dec_setup()
         bar()
-        tot, ms = timer.run(lambda: c3_run(st3, 184320, 8192), K, W)
+        tot, ms = timer.run(lambda: dec_run(st3, 184320, 8192), K, W)
         tot = max_over_ranks(tot, world)
         us = tot / K * 1e3
-        hb, db = c3_bytes(184320, 8192)
+        hb, db = dec_bytes(184320, 8192)
         head = {"us": us, "host_bytes": hb, "dev_bytes": db, "ms": ms}
         results[HEADLINE] = {"us_per_step": us, "host_gbs": hb / (us * 1e-6) / 1e9,
                              "frac_link_peak": hb / (us * 1e-6) / 1e9 / peaks["h2d"]}
         # e2e through the C-ABI with host buffers: q from pinned host, out back to pinned host
         q_h = t.from_numpy(st3["q_np"].view(np.int16).reshape(-1).copy()).pin_memory()
-        o_h = t.empty(C3_HQ * C3_D, dtype=t.float32).pin_memory()
+        o_h = t.empty(DEC_HQ * DEC_D, dtype=t.float32).pin_memory()
         q_d = t.empty_like(st3["q"])
         o_d = t.empty_like(st3["out"])
 
         def e2e_step():
             q_d.copy_(q_h, non_blocking=True)
-            c3_run(st3, 184320, 8192, q=q_d, out=o_d)
+            dec_run(st3, 184320, 8192, q=q_d, out=o_d)
             o_h.copy_(o_d, non_blocking=True)
         tot_e, _ = timer.run(e2e_step, K, W)
         tot_e = max_over_ranks(tot_e, world)
         head["e2e_us"] = tot_e / K * 1e3
         head["e2e_h2d"] = q_h.numel() * 2
         head["e2e_d2h"] = o_h.numel() * 4
-        if "c3" in rows:
-            for L in C3_LS:
-                for N in C3_NS:
+        if "decode" in rows:
+            for L in DEC_LS:
+                for N in DEC_NS:
                     for staging in (False, True):
                         if L <= N and staging:
                             continue
-                        tot, _ = timer.run(lambda: c3_run(st3, L, N, staging=staging), K, W)
+                        tot, _ = timer.run(lambda: dec_run(st3, L, N, staging=staging), K, W)
                         us_r = max_over_ranks(tot, world) / K * 1e3
-                        hb_r, db_r = c3_bytes(L, N)
+                        hb_r, db_r = dec_bytes(L, N)
                         if staging:
                             db_r += 2 * hb_r
-                        key = f"c3_q8_0_decode_L{L}_N{N}_{'staged' if staging else 'direct'}"
+                        key = f"q8_0_decode_L{L}_N{N}_{'staged' if staging else 'direct'}"
                         t_star = max(hb_r / (peaks['h2d'] * 1e9), db_r / (hbm * 1e9))
                         results[key] = {"us_per_step": us_r, "host_gbs": hb_r / (us_r * 1e-6) / 1e9,
                                         "roofline_frac": t_star / (us_r * 1e-6)}
-                tot, _ = timer.run(lambda: c3_run(st3, L, 0, all_vram=True), K, W)
+                tot, _ = timer.run(lambda: dec_run(st3, L, 0, all_vram=True), K, W)
                 us_r = max_over_ranks(tot, world) / K * 1e3
-                db_r = L * 2 * C3_HKV * (C3_D // 32) * 34
-                results[f"c3_q8_0_decode_L{L}_all_vram"] = {
+                db_r = L * 2 * DEC_HKV * (DEC_D // 32) * 34
+                results[f"q8_0_decode_L{L}_all_vram"] = {
                     "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
                     "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
         del st3
-    if "c3vram" in rows and "c3" not in rows:
-        st3 = c3_setup()
-        L = max(C3_LS)
-        tot, _ = timer.run(lambda: c3_run(st3, L, 0, all_vram=True), K, W)
+    if "decode_vram" in rows and "decode" not in rows:
+        st3 = dec_setup()
+        L = max(DEC_LS)
+        tot, _ = timer.run(lambda: dec_run(st3, L, 0, all_vram=True), K, W)
         us_r = max_over_ranks(tot, world) / K * 1e3
-        db_r = L * 2 * C3_HKV * (C3_D // 32) * 34
-        results[f"c3_q8_0_decode_L{L}_all_vram"] = {
+        db_r = L * 2 * DEC_HKV * (DEC_D // 32) * 34
+        results[f"q8_0_decode_L{L}_all_vram"] = {
             "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
             "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
         del st3
-    # ---- C1 tiny (latency-bound: microseconds, fractions not meaningful)
-    if "c1" in rows:
-        st1 = c1_setup()
+    # ---- tiny paged cache (latency-bound: microseconds, fractions not meaningful)
+    if "tiny" in rows:
+        st1 = tiny_setup()
         for h2d in (True, False):
-            tot, _ = timer.run(lambda: c2_run(st1, h2d), K, W)
+            tot, _ = timer.run(lambda: swap_run(st1, h2d), K, W)
             us_r = max_over_ranks(tot, world) / K * 1e3
-            results[f"c1_swap_64blocks_{'h2d' if h2d else 'd2h'}"] = {
+            results[f"tiny_swap_64blocks_{'h2d' if h2d else 'd2h'}"] = {
                 "us_per_step": us_r, "host_gbs": st1["bytes"] / (us_r * 1e-6) / 1e9}
         for staging in (False, True):
-            tot, _ = timer.run(lambda: c1_decode(st1, staging), K, W)
+            tot, _ = timer.run(lambda: tiny_decode(st1, staging), K, W)
             us_r = max_over_ranks(tot, world) / K * 1e3
-            results[f"c1_f16_decode_L1024_N512_{'staged' if staging else 'direct'}"] = {"us_per_step": us_r}
+            results[f"tiny_f16_decode_L1024_N512_{'staged' if staging else 'direct'}"] = {"us_per_step": us_r}
         del st1
-    # ---- C2 swap
-    if "c2" in rows:
+    # ---- 32-layer offload swap
+    if "swap" in rows:
         for page in (32768, 2048):
-            st2 = c2_setup(page)
+            st2 = swap_setup(page)
             for h2d in (True, False):
-                tot, _ = timer.run(lambda: c2_run(st2, h2d), K, W)
+                tot, _ = timer.run(lambda: swap_run(st2, h2d), K, W)
                 us_r = max_over_ranks(tot, world) / K * 1e3
                 gbs = st2["bytes"] / (us_r * 1e-6) / 1e9
                 pk = peaks["h2d" if h2d else "d2h"]
-                results[f"c2_swap_{page // 1024}KiB_{'h2d' if h2d else 'd2h'}"] = {
+                results[f"swap_{page // 1024}KiB_{'h2d' if h2d else 'd2h'}"] = {
                     "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / pk,
                     "descriptors": st2["n_desc"], "mode": "sm"}
             del st2
             t.cuda.empty_cache()
-    # ---- C4 gather + sparse decode
-    if "c4" in rows:
-        st4 = c4_setup()
-        tot, _ = timer.run(lambda: c4_gather(st4), K, W)
+    # ---- top-k gather + sparse decode
+    if "topk" in rows:
+        st4 = topk_setup()
+        tot, _ = timer.run(lambda: topk_gather(st4), K, W)
         us_r = max_over_ranks(tot, world) / K * 1e3
         gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
-        results["c4_gather"] = {"us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["h2d"]}
-        c4_gather(st4)
-        tot, _ = timer.run(lambda: c4_decode(st4), K, W)
+        results["topk_gather_8seq_64blocks"] = {"us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["h2d"]}
+        topk_gather(st4)
+        tot, _ = timer.run(lambda: topk_decode(st4), K, W)
         us_r = max_over_ranks(tot, world) / K * 1e3
         gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
-        results["c4_sparse_decode"] = {"us_per_step": us_r, "hbm_gbs": gbs, "roofline_frac": gbs / hbm}
+        results["topk_sparse_decode_8x4096"] = {"us_per_step": us_r, "hbm_gbs": gbs, "roofline_frac": gbs / hbm}
         del st4
     # ---- write path: appends into the host tail
-    if "c6" in rows:
-        st6 = c6_setup()
+    if "append" in rows:
+        st6 = append_setup()
         for which, n_tok in (("q8", 1), ("q8", 2048), ("bf", 2048)):
-            tot, _ = timer.run(lambda: c6_run(st6, which, n_tok), K, W)
+            tot, _ = timer.run(lambda: append_run(st6, which, n_tok), K, W)
             us_r = max_over_ranks(tot, world) / K * 1e3
             host_b = 2 * n_tok * st6[which + "_rb"]
             gbs = host_b / (us_r * 1e-6) / 1e9
@@ -749,38 +749,38 @@ def main(argv=None):
                 "host_bytes": host_b}
         del st6
     # ---- QSA sparse rows (staged through the arena vs direct)
-    if "c7" in rows:
-        st7 = c7_setup()
+    if "sparse" in rows:
+        st7 = sr_setup()
         host_staged = 2 * st7["n_pages"] * st7["page_bytes"]
-        host_direct = 2 * C7_R * C7_KPAD * C7_HKV * C7_D * 2
-        fma = 2.0 * C7_R * C7_KPAD * C7_HQ * C7_D
+        host_direct = 2 * SR_R * SR_KPAD * SR_HKV * SR_D * 2
+        fma = 2.0 * SR_R * SR_KPAD * SR_HQ * SR_D
         for staged in (True, False):
             steps = K if staged else max(1, min(K, 2))
-            tot, _ = timer.run(lambda: c7_run(st7, staged), steps, min(W, 3))
+            tot, _ = timer.run(lambda: sr_run(st7, staged), steps, min(W, 3))
             us_r = max_over_ranks(tot, world) / steps * 1e3
             hb = host_staged if staged else host_direct
             gbs = hb / (us_r * 1e-6) / 1e9
             t_star = max(hb / (peaks["h2d"] * 1e9), fma / FP32_FMA_PEAK)
-            results[f"c7_qsa_sparse_rows_{'staged' if staged else 'direct'}"] = {
+            results[f"qsa_sparse_rows_R2048_K2080_{'staged' if staged else 'direct'}"] = {
                 "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": t_star / (us_r * 1e-6),
-                "rows_per_s": C7_R / (us_r * 1e-6)}
+                "rows_per_s": SR_R / (us_r * 1e-6)}
         del st7
-    # ---- C5 prefill
-    if "c5" in rows:
-        st5 = c5_setup()
-        fl = c5_flops()
-        tail_b = (C5_L - C5_N) * st5["rb"] * 2
+    # ---- tiered chunked prefill
+    if "prefill" in rows:
+        st5 = pf_setup()
+        fl = pf_flops()
+        tail_b = (PF_L - PF_N) * st5["rb"] * 2
         bf16 = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops", 1932.2) \
             if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
         for staged in (True, False):
             steps = K if staged else max(1, min(K, 3))
-            tot, _ = timer.run(lambda: c5_run(st5, staged), steps, min(W, 3))
+            tot, _ = timer.run(lambda: pf_run(st5, staged), steps, min(W, 3))
             us_r = max_over_ranks(tot, world) / steps * 1e3
             tfs = fl / (us_r * 1e-6) / 1e12
             t_star = max(fl / (bf16 * 1e12), tail_b / (peaks["h2d"] * 1e9))
-            results[f"c5_prefill_{'staged' if staged else 'direct'}"] = {
+            results[f"prefill_R2048_L262144_N65536_{'staged' if staged else 'direct'}"] = {
                 "us_per_step": us_r, "tflops": tfs, "tensor_frac": tfs / bf16,
-                "roofline_frac": t_star / (us_r * 1e-6), "tokens_per_s": C5_R / (us_r * 1e-6)}
+                "roofline_frac": t_star / (us_r * 1e-6), "tokens_per_s": PF_R / (us_r * 1e-6)}
         del st5
     clk = clocks.stop()
 
@@ -799,14 +799,14 @@ def main(argv=None):
             "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "q8_0 K/V x f16 q, f32 accumulate",
             "data": "synthetic (seeded)",
-            "config": {"workload": HEADLINE, "L": 184320, "n_vram_cells": 8192, "q_heads": C3_HQ,
-                       "kv_heads": C3_HKV, "head_dim": C3_D, "kv_dtype": "q8_0", "batch": 1,
+            "config": {"workload": HEADLINE, "L": 184320, "n_vram_cells": 8192, "q_heads": DEC_HQ,
+                       "kv_heads": DEC_HKV, "head_dim": DEC_D, "kv_dtype": "q8_0", "batch": 1,
                        "staging": False, "l2": "flushed between timed steps (256 MiB write)"},
             "host_gbs": achieved, "link_peak_gbs": peaks,
             "roofline": {"bound": "host_link", "achieved": achieved, "peak": peaks["h2d"], "unit": "GB/s",
                          "frac": achieved / peaks["h2d"], "traffic": profiled_traffic(),
                          "traffic_note": "dram__bytes_read+write of decode_split_kernel per launch (ncu, "
-                                         "profiles/decode_split_kernel_c3_headline.md); host-link bytes "
+                                         "profiles/decode_split_kernel_q8_0_L184320_N8192_headline.md); host-link bytes "
                                          "are not DRAM traffic",
                          "peak_source": "pinned cudaMemcpyAsync H2D 1 GiB, best of 5, measured in this run",
                          "kernel": "decode_split_kernel + decode_combine_kernel (one C-ABI call)"},
@@ -836,7 +836,7 @@ def profiled_traffic():
     """DRAM bytes per launch of the headline decode kernel, as recorded by the
     committed ncu summary; None if the summary is missing or was taken on a
     different decode kernel source than the one built now."""
-    path = os.path.join(ROOT, "profiles", "decode_split_kernel_c3_headline.md")
+    path = os.path.join(ROOT, "profiles", "decode_split_kernel_q8_0_L184320_N8192_headline.md")
     traffic = sha = None
     try:
         for line in open(path):
@@ -852,31 +852,31 @@ def profiled_traffic():
 def gpu_launch_count(K, rows):
     """Kernels of libkvo launched in the timed regions (own kernels only)."""
     n = 0
-    if "c3" in rows or "head" in rows:
+    if "decode" in rows or "head" in rows:
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
-    if "c3" in rows:
+    if "decode" in rows:
         n += 2 * K * (3 * 2 * 2 - 1 + 3)           # 11 tiered variants + 3 all-VRAM, 2 kernels each
-    elif "c3vram" in rows:
+    elif "decode_vram" in rows:
         n += 2 * K                                 # the 184,320-cell all-VRAM decode
-    if "c1" in rows:
+    if "tiny" in rows:
         n += K * 2 + K * 2 * 2                     # swap both ways; decode direct + staged (2 kernels)
-    if "c2" in rows:
+    if "swap" in rows:
         n += K * 4                                 # 2 pages x 2 directions, one swap kernel each
-    if "c4" in rows:
+    if "topk" in rows:
         n += K + 2 * K                             # gather; decode split + combine
-    if "c6" in rows:
+    if "append" in rows:
         n += 3 * K                                 # three appends, one kernel each
-    if "c5" in rows:
+    if "prefill" in rows:
         # staged: VRAM head (2 row blocks) + 48 arena buckets of 4096 cells x 2 row blocks;
         # direct: head + host tail, 2 row blocks each
         n += K * (2 + 48 * 2) + min(K, 3) * 4
-    if "c7" in rows:
+    if "sparse" in rows:
         # staged: partition + buckets x (page gather + 2 row blocks x (split + combine)), the
         # arena holding two slots of arena / (4 page_bytes) pages; direct: 2 row blocks x
         # (split + combine)
-        page_bytes = C7_PS * C7_HKV * C7_D * 2
-        slot = C7_ARENA // (4 * page_bytes)
-        buckets = -(-(C7_L // C7_PS) // slot)
+        page_bytes = SR_PS * SR_HKV * SR_D * 2
+        slot = SR_ARENA // (4 * page_bytes)
+        buckets = -(-(SR_L // SR_PS) // slot)
         n += K * (1 + buckets * (1 + 2 * 2)) + max(1, min(K, 2)) * 4
     return n
 
@@ -888,7 +888,7 @@ def cpu_baseline():
     oracle.build()
     threads = oracle.set_threads(os.cpu_count() or 1)
     heads = 8
-    step, keep = oracle_c3_step(max(C3_LS), heads)
+    step, keep = oracle_c3_step(max(DEC_LS), heads)
     step()
     t0 = time.perf_counter()
     n = 0
@@ -896,9 +896,9 @@ def cpu_baseline():
         step()
         n += 1
     dt = (time.perf_counter() - t0) / n
-    out = {"value": dt * 1e6 * (C3_HQ / heads), "unit": "us/step", "cores": threads, "kind": "oracle",
-           "sample": f"{heads} of {C3_HQ} query heads per step over the full 184,320 cells, "
-                     f"{n} steps, scaled x{C3_HQ // heads}"}
+    out = {"value": dt * 1e6 * (DEC_HQ / heads), "unit": "us/step", "cores": threads, "kind": "oracle",
+           "sample": f"{heads} of {DEC_HQ} query heads per step over the full 184,320 cells, "
+                     f"{n} steps, scaled x{DEC_HQ // heads}"}
     out["rows"] = cpu_rows(threads)
     return out
 
@@ -929,42 +929,42 @@ def cpu_rows(threads):
     d_ptr = (dst.ctypes.data + np.arange(nd, dtype=np.uint64) * page).astype(np.uint64)
     sizes = np.full(nd, page, np.int64)
     dt = _timed(lambda: oracle.swap_blocks(s_ptr, d_ptr, sizes))
-    res["c2_swap_32KiB"] = {"value": dt * 1e6 * (131072 / nd), "unit": "us/step",
+    res["swap_swap_32KiB"] = {"value": dt * 1e6 * (131072 / nd), "unit": "us/step",
                             "sample": f"{nd} of 131,072 descriptors, scaled x{131072 // nd}", "cores": 1}
     del src, dst
     # gather: 64 blocks of 64 tokens per (sequence, kv head), 8 x 4 x 128 bf16 planes of 65,536 tokens
     # (the same 64 MiB copied as the full 2^20-token planes)
     T = 65536
-    plane = np.zeros((C4_S, T, C4_HKV, C4_D), np.uint16)
-    sel = synth.topk_selection(C4_S, C4_HKV, T // 64, 64, synth.rng(SEED0 + 3, 9))
-    dt = _timed(lambda: oracle.gather_blocks(plane, C4_S, T, C4_HKV, C4_D, 2, 64, sel))
-    res["c4_gather"] = {"value": dt * 1e6 * 2, "unit": "us/step",
+    plane = np.zeros((TOPK_S, T, TOPK_HKV, TOPK_D), np.uint16)
+    sel = synth.topk_selection(TOPK_S, TOPK_HKV, T // 64, 64, synth.rng(SEED0 + 3, 9))
+    dt = _timed(lambda: oracle.gather_blocks(plane, TOPK_S, T, TOPK_HKV, TOPK_D, 2, 64, sel))
+    res["topk_gather_8seq_64blocks"] = {"value": dt * 1e6 * 2, "unit": "us/step",
                         "sample": "K plane only (x2 for K and V), 65,536-token planes, full selection",
                         "cores": 1}
     del plane
     # sparse decode over the 4,096 gathered cells: full size
     g = synth.rng(SEED0 + 3, 10)
-    cells = C4_S * 4096
-    kb = synth.normal_bits((cells, C4_HKV * C4_D), "bf16", g).view(np.uint8)
-    vb = synth.normal_bits((cells, C4_HKV * C4_D), "bf16", g).view(np.uint8)
-    qb = synth.normal_bits((C4_S, C4_HQ, C4_D), "bf16", g)
-    cache = oracle.make_cache(kb, vb, None, None, 4096, 0, 4096, oracle.BF16, C4_HKV, C4_D)
-    dt = _timed(lambda: oracle.attn_decode(cache, qb, oracle.BF16, C4_S, C4_HQ, [4096] * C4_S,
-                                           1.0 / math.sqrt(C4_D)))
-    res["c4_sparse_decode"] = {"value": dt * 1e6, "unit": "us/step", "sample": "full step", "cores": threads}
+    cells = TOPK_S * 4096
+    kb = synth.normal_bits((cells, TOPK_HKV * TOPK_D), "bf16", g).view(np.uint8)
+    vb = synth.normal_bits((cells, TOPK_HKV * TOPK_D), "bf16", g).view(np.uint8)
+    qb = synth.normal_bits((TOPK_S, TOPK_HQ, TOPK_D), "bf16", g)
+    cache = oracle.make_cache(kb, vb, None, None, 4096, 0, 4096, oracle.BF16, TOPK_HKV, TOPK_D)
+    dt = _timed(lambda: oracle.attn_decode(cache, qb, oracle.BF16, TOPK_S, TOPK_HQ, [4096] * TOPK_S,
+                                           1.0 / math.sqrt(TOPK_D)))
+    res["topk_sparse_decode_8x4096"] = {"value": dt * 1e6, "unit": "us/step", "sample": "full step", "cores": threads}
     del kb, vb
     # prefill: 2 of the 2,048 rows (all 32 heads) over the full 262,144 cells
-    rb = C5_HKV * C5_D * 2
-    kc = np.empty(C5_L * rb // 2, np.uint16)
-    vc = np.empty(C5_L * rb // 2, np.uint16)
+    rb = PF_HKV * PF_D * 2
+    kc = np.empty(PF_L * rb // 2, np.uint16)
+    vc = np.empty(PF_L * rb // 2, np.uint16)
     synth.fill_normal_bits_large(kc, "bf16", SEED0 + 4, 11)
     synth.fill_normal_bits_large(vc, "bf16", SEED0 + 4, 12)
-    q5 = synth.normal_bits((2, C5_HQ, C5_D), "bf16", synth.rng(SEED0 + 4, 13))
-    cache = oracle.make_cache(kc.view(np.uint8), vc.view(np.uint8), None, None, C5_L, 0, C5_L, oracle.BF16,
-                              C5_HKV, C5_D)
-    dt = _timed(lambda: oracle.attn_prefill(cache, q5, oracle.BF16, 2, C5_POS0 + C5_R - 2, C5_HQ, C5_L,
-                                            1.0 / math.sqrt(C5_D)), budget_s=0.0, max_n=1, warm=False)
-    res["c5_prefill"] = {"value": dt * 1e6 * (C5_R / 2), "unit": "us/step",
+    q5 = synth.normal_bits((2, PF_HQ, PF_D), "bf16", synth.rng(SEED0 + 4, 13))
+    cache = oracle.make_cache(kc.view(np.uint8), vc.view(np.uint8), None, None, PF_L, 0, PF_L, oracle.BF16,
+                              PF_HKV, PF_D)
+    dt = _timed(lambda: oracle.attn_prefill(cache, q5, oracle.BF16, 2, PF_POS0 + PF_R - 2, PF_HQ, PF_L,
+                                            1.0 / math.sqrt(PF_D)), budget_s=0.0, max_n=1, warm=False)
+    res["pf_prefill"] = {"value": dt * 1e6 * (PF_R / 2), "unit": "us/step",
                          "sample": "2 of 2,048 rows (the last positions, 64 tasks), one run, scaled x1024",
                          "cores": threads}
     del kc, vc

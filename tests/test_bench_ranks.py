@@ -49,5 +49,5 @@ def test_single_rank_is_identity():
 
 def test_gpu_launch_count_is_positive_for_every_row_set():
     import bench
-    for rows in ({"c2"}, {"c3"}, {"c4"}, {"c5"}, {"c2", "c3", "c4", "c5"}):
+    for rows in ({"swap"}, {"decode"}, {"topk"}, {"prefill"}, {"swap", "decode", "topk", "prefill"}):
         assert bench.gpu_launch_count(10, rows) > 0

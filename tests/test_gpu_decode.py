@@ -140,17 +140,17 @@ def test_argument_errors():
 @pytest.mark.parametrize("L", [29696, 96256, 184320])
 def test_c3_full_size_tiered_staged_all_vram_bit_identical(L):
     # llama.cpp-style q8_0 decode, 48/8 heads x 128; N in {8192, 94208}; staging on/off.
-    from bench import C3_D, C3_HKV, C3_HQ, c3_run, c3_setup
+    from bench import DEC_D, DEC_HKV, DEC_HQ, dec_run, dec_setup
     t = torch()
-    st = c3_setup()
+    st = dec_setup()
     outs = {}
     for N in (8192, 94208):
         for staging in (False, True):
-            o = t.empty(C3_HQ * C3_D, dtype=t.float32, device="cuda")
-            c3_run(st, L, N, staging=staging, out=o)
+            o = t.empty(DEC_HQ * DEC_D, dtype=t.float32, device="cuda")
+            dec_run(st, L, N, staging=staging, out=o)
             outs[(N, staging)] = o
-    o = t.empty(C3_HQ * C3_D, dtype=t.float32, device="cuda")
-    c3_run(st, L, 0, all_vram=True, out=o)
+    o = t.empty(DEC_HQ * DEC_D, dtype=t.float32, device="cuda")
+    dec_run(st, L, 0, all_vram=True, out=o)
     t.cuda.synchronize()
     allv = o.cpu().numpy()
     for key, x in outs.items():
@@ -158,28 +158,28 @@ def test_c3_full_size_tiered_staged_all_vram_bit_identical(L):
     rb = st["rb"]
     kh = st["k_host"].numpy()[:L * rb].reshape(L, rb)
     vh = st["v_host"].numpy()[:L * rb].reshape(L, rb)
-    cache = oracle.make_cache(None, None, kh, vh, 0, L, 0, oracle.Q8_0, C3_HKV, C3_D)
-    ref = oracle.attn_decode(cache, st["q_np"], oracle.F16, 1, C3_HQ, [L], 1.0 / math.sqrt(C3_D))
-    got = allv.reshape(1, C3_HQ, C3_D)
+    cache = oracle.make_cache(None, None, kh, vh, 0, L, 0, oracle.Q8_0, DEC_HKV, DEC_D)
+    ref = oracle.attn_decode(cache, st["q_np"], oracle.F16, 1, DEC_HQ, [L], 1.0 / math.sqrt(DEC_D))
+    got = allv.reshape(1, DEC_HQ, DEC_D)
     assert normwise_rel_err(got, ref) <= REL_TOL
     assert np.abs(got - ref).max() <= Q8_ABS_TOL
 
 
 def test_c4_sparse_decode_over_gathered_tokens():
-    from bench import C4_D, C4_HKV, C4_HQ, C4_K, C4_BLK, C4_S, c4_decode, c4_gather, c4_setup
-    st = c4_setup()
-    c4_gather(st)
-    c4_decode(st)
+    from bench import TOPK_D, TOPK_HKV, TOPK_HQ, TOPK_K, TOPK_BLK, TOPK_S, topk_decode, topk_gather, topk_setup
+    st = topk_setup()
+    topk_gather(st)
+    topk_decode(st)
     torch().cuda.synchronize()
-    from bench import C4_T
-    tok = C4_K * C4_BLK
+    from bench import TOPK_T
+    tok = TOPK_K * TOPK_BLK
     # the oracle's own gather of the same host planes (never the GPU's output)
-    kg = oracle.gather_blocks(st["k_plane"].numpy(), C4_S, C4_T, C4_HKV, C4_D, 2, C4_BLK,
-                              st["sel_np"]).reshape(C4_S * tok, -1)
-    vg = oracle.gather_blocks(st["v_plane"].numpy(), C4_S, C4_T, C4_HKV, C4_D, 2, C4_BLK,
-                              st["sel_np"]).reshape(C4_S * tok, -1)
-    cache = oracle.make_cache(kg, vg, None, None, tok, 0, tok, oracle.BF16, C4_HKV, C4_D)
-    ref = oracle.attn_decode(cache, st["q_np"], oracle.BF16, C4_S, C4_HQ, [tok] * C4_S,
-                             1.0 / math.sqrt(C4_D))
-    out = st["out"].cpu().numpy().reshape(C4_S, C4_HQ, C4_D)
+    kg = oracle.gather_blocks(st["k_plane"].numpy(), TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, 2, TOPK_BLK,
+                              st["sel_np"]).reshape(TOPK_S * tok, -1)
+    vg = oracle.gather_blocks(st["v_plane"].numpy(), TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, 2, TOPK_BLK,
+                              st["sel_np"]).reshape(TOPK_S * tok, -1)
+    cache = oracle.make_cache(kg, vg, None, None, tok, 0, tok, oracle.BF16, TOPK_HKV, TOPK_D)
+    ref = oracle.attn_decode(cache, st["q_np"], oracle.BF16, TOPK_S, TOPK_HQ, [tok] * TOPK_S,
+                             1.0 / math.sqrt(TOPK_D))
+    out = st["out"].cpu().numpy().reshape(TOPK_S, TOPK_HQ, TOPK_D)
     assert normwise_rel_err(out, ref) <= REL_TOL

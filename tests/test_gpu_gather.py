@@ -81,14 +81,14 @@ def test_gather_rejects_pageable_and_q8_0():
 def test_c4_full_size_gather_bit_exact():
     # 8 sequences x 2^20 tokens x 4 kv heads x 128 bf16 planes (8 GiB each) in
     # pinned host memory; 64 blocks of 64 tokens per (sequence, kv head).
-    from bench import C4_BLK, C4_D, C4_HKV, C4_K, C4_S, C4_T, c4_gather, c4_setup
-    st = c4_setup()
-    c4_gather(st)
+    from bench import TOPK_BLK, TOPK_D, TOPK_HKV, TOPK_K, TOPK_S, TOPK_T, topk_gather, topk_setup
+    st = topk_setup()
+    topk_gather(st)
     torch().cuda.synchronize()
     kp = st["k_plane"].numpy()
     vp = st["v_plane"].numpy()
-    exp_k = oracle.gather_blocks(kp, C4_S, C4_T, C4_HKV, C4_D, 2, C4_BLK, st["sel_np"])
-    exp_v = oracle.gather_blocks(vp, C4_S, C4_T, C4_HKV, C4_D, 2, C4_BLK, st["sel_np"])
+    exp_k = oracle.gather_blocks(kp, TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, 2, TOPK_BLK, st["sel_np"])
+    exp_v = oracle.gather_blocks(vp, TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, 2, TOPK_BLK, st["sel_np"])
     assert np.array_equal(st["kg"].cpu().numpy(), exp_k)
     assert np.array_equal(st["vg"].cpu().numpy(), exp_v)
     assert kvo.kvo_device_errors() == 0

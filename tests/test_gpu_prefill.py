@@ -105,20 +105,20 @@ def test_prefill_argument_errors():
 def test_c5_full_size_sampled_rows(staged):
     # 2048 rows at positions 260,096..262,143 over 262,144 bf16 cells, 32/8 heads,
     # N = 65,536, 32 MiB arena, 1024 rows per launch -- the benchmark's launch.
-    from bench import (C5_D, C5_HKV, C5_HQ, C5_L, C5_N, C5_POS0, C5_R, c5_run, c5_setup)
-    st = c5_setup()
-    c5_run(st, staged=staged)
+    from bench import (PF_D, PF_HKV, PF_HQ, PF_L, PF_N, PF_POS0, PF_R, pf_run, pf_setup)
+    st = pf_setup()
+    pf_run(st, staged=staged)
     torch().cuda.synchronize()
-    out = st["out"].cpu().numpy().reshape(C5_R, C5_HQ, C5_D)
+    out = st["out"].cpu().numpy().reshape(PF_R, PF_HQ, PF_D)
     rb = st["rb"]
-    kh = st["k_head_np"].view(np.uint8).reshape(C5_N, rb)
-    vh = st["v_head_np"].view(np.uint8).reshape(C5_N, rb)
-    kt = st["k_host"].numpy().reshape(C5_L - C5_N, rb)
-    vt = st["v_host"].numpy().reshape(C5_L - C5_N, rb)
-    cache = oracle.make_cache(kh, vh, kt, vt, C5_N, C5_L - C5_N, C5_N, oracle.BF16, C5_HKV, C5_D)
+    kh = st["k_head_np"].view(np.uint8).reshape(PF_N, rb)
+    vh = st["v_head_np"].view(np.uint8).reshape(PF_N, rb)
+    kt = st["k_host"].numpy().reshape(PF_L - PF_N, rb)
+    vt = st["v_host"].numpy().reshape(PF_L - PF_N, rb)
+    cache = oracle.make_cache(kh, vh, kt, vt, PF_N, PF_L - PF_N, PF_N, oracle.BF16, PF_HKV, PF_D)
     g = synth.rng(77, int(staged))
-    rows = sorted(set([0, 1, 1023, 1024, 2046, 2047] + g.choice(C5_R, 10, replace=False).tolist()))
+    rows = sorted(set([0, 1, 1023, 1024, 2046, 2047] + g.choice(PF_R, 10, replace=False).tolist()))
     for i in rows:
-        ref = oracle.attn_prefill(cache, st["q_np"][i:i + 1], oracle.BF16, 1, C5_POS0 + i, C5_HQ,
-                                  C5_L, 1.0 / math.sqrt(C5_D))
+        ref = oracle.attn_prefill(cache, st["q_np"][i:i + 1], oracle.BF16, 1, PF_POS0 + i, PF_HQ,
+                                  PF_L, 1.0 / math.sqrt(PF_D))
         assert normwise_rel_err(out[i:i + 1], ref) <= REL_TOL, i

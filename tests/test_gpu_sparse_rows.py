@@ -166,19 +166,19 @@ def test_full_size_qsa_prefill_sampled_rows():
     # 2048 rows x 2080 picks over 262,144 fp16 positions in 1,024 host pages of 256,
     # 32 q / 8 kv heads x 128, staged through a 32 MiB arena (32 buckets) and direct;
     # 24 sampled rows against the oracle.
-    from bench import C7_D, C7_HKV, C7_HQ, C7_KPAD, C7_PS, c7_run, c7_setup
+    from bench import SR_D, SR_HKV, SR_HQ, SR_KPAD, SR_PS, sr_run, sr_setup
     t = torch()
-    st = c7_setup()
+    st = sr_setup()
     kp = st["k_pages"].numpy()
     vp = st["v_pages"].numpy()
     rows = np.linspace(0, 2047, 24).astype(int)
-    ref = oracle.attn_sparse_rows(kp, vp, oracle.F16, C7_PS, C7_HKV, C7_D, st["bt_np"], st["n_pages"],
-                                  st["idx_np"][rows], st["q_np"][rows], oracle.F16, C7_HQ,
-                                  1.0 / math.sqrt(C7_D))
+    ref = oracle.attn_sparse_rows(kp, vp, oracle.F16, SR_PS, SR_HKV, SR_D, st["bt_np"], st["n_pages"],
+                                  st["idx_np"][rows], st["q_np"][rows], oracle.F16, SR_HQ,
+                                  1.0 / math.sqrt(SR_D))
     for staged in (True, False):
         st["out"].fill_(float("nan"))
-        c7_run(st, staged)
+        sr_run(st, staged)
         t.cuda.synchronize()
-        out = st["out"].cpu().numpy().reshape(-1, C7_HQ, C7_D)
+        out = st["out"].cpu().numpy().reshape(-1, SR_HQ, SR_D)
         assert np.all(np.isfinite(out)), staged
         assert normwise_rel_err(out[rows], ref) <= REL_TOL, staged

@@ -200,12 +200,12 @@ def test_descriptor_arrays_must_be_mapped():
 
 @pytest.mark.parametrize("page", [32768, 2048])
 def test_c2_full_size_swap_sampled(page):
-    # Full C2: 64 tensors (32 layers x K,V), 2048 blocks per direction, bpc 4,
+    # The full 32-layer offload swap: 64 tensors (32 layers x K,V), 2048 blocks per direction, bpc 4,
     # skip 1, host stride 1.5 x row: the launch configuration the benchmark times.
-    from bench import c2_setup, c2_run
-    st = c2_setup(page, seed=1235)
-    c2_run(st, h2d=False)
-    c2_run(st, h2d=True)
+    from bench import swap_setup, swap_run
+    st = swap_setup(page, seed=1235)
+    swap_run(st, h2d=False)
+    swap_run(st, h2d=True)
     torch().cuda.synchronize()
     g = synth.rng(99, page)
     host = st["host"].numpy()
