@@ -58,3 +58,25 @@ def test_noalloc_rejects_what_does_not_fit():
         kvo.kvo_attn_decode_tiered_noalloc(x, kvo.F16, 8192, 8, 8, 128, x, x, 1, None, None, 0,
                                            kvo.F16, ctx, 1, 1, 0.1, None, None, o)
     assert e.value.status == -6
+
+
+def test_noalloc_lengthens_the_split_when_the_partials_do_not_fit():
+    # 64 sequences x 48 heads: the regular chunks' partials exceed the 8 MiB
+    # scratch, so the no-workspace call runs with longer chunks; the result must
+    # still meet the decode tolerance against the oracle and the workspace call.
+    t = torch()
+    B, hq, hkv, d, L = 64, 48, 8, 128, 3000
+    g = synth.rng(4322)
+    k, v = cells(B * L, hkv, d, oracle.F16, g)
+    tc = Tiered(k.reshape(B * L, -1), v.reshape(B * L, -1), 1000, batch=B)
+    lens = [L - 37 * i for i in range(B)]
+    ctx = t.tensor(lens, dtype=t.int32, device="cuda")
+    q = synth.normal_bits((B, hq, d), "f16", g)
+    qd = t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda()
+    scale = 1 / math.sqrt(d)
+    assert kvo.kvo_attn_decode_workspace_bytes(B, hq, d, L) > 8 << 20
+    got = _noalloc(tc, qd, hq, hkv, d, oracle.F16, ctx, scale)
+    ref = run_decode(tc, qd, kvo.F16, hq, hkv, d, oracle.F16, ctx, scale)
+    assert normwise_rel_err(got, ref.astype(np.float64)) <= REL_TOL
+    want = oracle.attn_decode(tc.oracle_cache(oracle.F16, hkv, d), q, oracle.F16, B, hq, lens, scale)
+    assert normwise_rel_err(got, want) <= REL_TOL
