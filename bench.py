@@ -854,12 +854,21 @@ def gpu_launch_count(K, rows):
     n = 0
     if "decode" in rows or "head" in rows:
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
+    k = kvo()
     if "decode" in rows:
-        n += 2 * K * (3 * 2 * 2 - 1 + 3)           # 11 tiered variants + 3 all-VRAM, 2 kernels each
+        # 11 tiered variants (a staged call runs the split kernel once per copy part) + 3
+        # all-VRAM (split + combine)
+        for L in DEC_LS:
+            for N in DEC_NS:
+                for staging in (False, True):
+                    if not (L <= N and staging):
+                        n += K * k.kvo_attn_decode_launches(1, L, DEC_D, N, staging)
+            n += 2 * K
     elif "decode_vram" in rows:
         n += 2 * K                                 # the 184,320-cell all-VRAM decode
     if "tiny" in rows:
-        n += K * 2 + K * 2 * 2                     # swap both ways; decode direct + staged (2 kernels)
+        # swap both ways; decode direct + staged
+        n += K * 2 + K * sum(k.kvo_attn_decode_launches(1, 1024, 128, 512, s) for s in (False, True))
     if "swap" in rows:
         n += K * 4                                 # 2 pages x 2 directions, one swap kernel each
     if "topk" in rows:

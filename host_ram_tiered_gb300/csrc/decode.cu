@@ -1,5 +1,7 @@
 // Tiered decode: split geometry, workspace size and dtype dispatch.  The
 // kernels themselves live in decode_impl.cuh.
+#include <mutex>
+
 #include "kvo_internal.cuh"
 
 namespace kvo {
@@ -47,6 +49,100 @@ int launch_decode(const DecodeArgs &a, cudaStream_t st) {
   else if (a.kv_dtype == KVO_BF16) e = dec::launch_kv<KVO_BF16, false>(a, st);
   else e = dec::launch_kv<KVO_F16, false>(a, st);
   return cuda_status(e, "decode kernel launch");
+}
+
+StagedPlan staged_plan(int64_t batch, int split_cells, int n_splits, int64_t n_vram) {
+  // The chunks wholly in VRAM are decoded first, then the chunks of each copy
+  // part as soon as it has landed while the next part is in flight.  A launch
+  // lasts about one chunk time per wave of its items over the SMs, so this
+  // only pays when the items fill more than one wave: then there is one part
+  // per wave of host chunks (at most four), else a single part and a single
+  // launch after the whole copy.
+  StagedPlan pl;
+  const int64_t sms = num_sms();
+  const bool multi_wave = batch * n_splits > sms;
+  pl.c_v = multi_wave ? n_vram / split_cells : 0;
+  const int64_t hc = n_splits - pl.c_v;          // >= 1: the last chunk holds host rows
+  const int64_t waves = (batch * hc + sms - 1) / sms;
+  pl.parts = multi_wave ? (waves < 4 ? (int)waves : 4) : 1;
+  for (int p = 0; p < pl.parts; ++p) {           // even parts of the chunks [c_v, n_splits)
+    pl.ch_lo[p] = pl.c_v + hc * p / pl.parts;
+    pl.ch_hi[p] = pl.c_v + hc * (p + 1) / pl.parts;
+  }
+  return pl;
+}
+
+int launch_decode_staged(DecodeArgs a, const void *k_host, const void *v_host, int64_t host_stride,
+                         void *staging_k, void *staging_v, cudaStream_t st) {
+  // The copy runs on a library stream in the parts of staged_plan.  A chunk's
+  // partial is the same whichever launch computes it, so the one combine at
+  // the end gives the bits of a single launch over an all-VRAM cache.
+  const int64_t C = a.split_cells, n_lo = a.n_vram, n_hi = a.max_ctx - a.n_vram;
+  const size_t rb = (size_t)a.row_bytes;
+  const StagedPlan pl = staged_plan(a.batch, a.split_cells, a.n_splits, n_lo);
+  const int parts = pl.parts;
+  const int64_t c_v = pl.c_v;
+  if (parts == 1 && c_v == 0) {                  // one wave: copy, then one launch, on `st`
+    for (int64_t b = 0; b < a.batch; ++b) {
+      const size_t bytes = (size_t)n_hi * rb;
+      const size_t src = (size_t)b * host_stride * rb, dst = (size_t)b * n_hi * rb;
+      int e = cuda_status(cudaMemcpyAsync((uint8_t *)staging_k + dst, (const uint8_t *)k_host + src, bytes,
+                                          cudaMemcpyDefault, st), "staging copy K");
+      if (!e) e = cuda_status(cudaMemcpyAsync((uint8_t *)staging_v + dst, (const uint8_t *)v_host + src, bytes,
+                                              cudaMemcpyDefault, st), "staging copy V");
+      if (e) return e;
+    }
+    a.k_hi = (const uint8_t *)staging_k;
+    a.v_hi = (const uint8_t *)staging_v;
+    a.hi_seq_stride_rows = n_hi;
+    a.hi_device = 1;
+    return launch_decode(a, st);
+  }
+  static std::mutex mu;                          // one staged call at a time uses the events
+  std::lock_guard<std::mutex> lock(mu);
+  Ring *rg = ring(2);
+  if (!rg) return fail(KVO_ERR_CUDA, "staged decode: library streams unavailable");
+  int e = cuda_status(cudaEventRecord(rg->fork, st), "cudaEventRecord");
+  if (!e) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->fork, 0), "cudaStreamWaitEvent");
+  if (e) return e;
+  const int64_t *ch_lo = pl.ch_lo, *ch_hi = pl.ch_hi;
+  for (int p = 0; p < parts; ++p) {
+    const int64_t r0 = ch_lo[p] * C > n_lo ? ch_lo[p] * C : n_lo;
+    const int64_t r1 = ch_hi[p] * C < a.max_ctx ? ch_hi[p] * C : a.max_ctx;
+    for (int64_t b = 0; b < a.batch && r1 > r0; ++b) {
+      const size_t bytes = (size_t)(r1 - r0) * rb;
+      const size_t src = ((size_t)b * host_stride + (size_t)(r0 - n_lo)) * rb;
+      const size_t dst = ((size_t)b * n_hi + (size_t)(r0 - n_lo)) * rb;
+      e = cuda_status(cudaMemcpyAsync((uint8_t *)staging_k + dst, (const uint8_t *)k_host + src, bytes,
+                                      cudaMemcpyDefault, rg->side), "staging copy K");
+      if (!e) e = cuda_status(cudaMemcpyAsync((uint8_t *)staging_v + dst, (const uint8_t *)v_host + src, bytes,
+                                              cudaMemcpyDefault, rg->side), "staging copy V");
+      if (e) return e;
+    }
+    e = cuda_status(cudaEventRecord(rg->part[p], rg->side), "cudaEventRecord");
+    if (e) return e;
+  }
+  a.k_hi = (const uint8_t *)staging_k;
+  a.v_hi = (const uint8_t *)staging_v;
+  a.hi_seq_stride_rows = n_hi;
+  a.hi_device = 1;
+  a.phase = 1;
+  if (c_v > 0) {
+    a.item_lo = 0;
+    a.item_hi = c_v * a.batch;
+    e = launch_decode(a, st);
+    if (e) return e;
+  }
+  for (int p = 0; p < parts; ++p) {
+    e = cuda_status(cudaStreamWaitEvent(st, rg->part[p], 0), "cudaStreamWaitEvent");
+    if (e) return e;
+    a.item_lo = ch_lo[p] * a.batch;
+    a.item_hi = ch_hi[p] * a.batch;
+    e = launch_decode(a, st);
+    if (e) return e;
+  }
+  a.phase = 2;
+  return launch_decode(a, st);
 }
 
 }  // namespace kvo

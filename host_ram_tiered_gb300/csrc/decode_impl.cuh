@@ -437,7 +437,8 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   const int64_t n_items = (int64_t)a.batch * a.n_splits;
   const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
 
-  for (int64_t w = blockIdx.x; w < n_items; w += gridDim.x) {
+  const int64_t w_end = a.item_hi < 0 ? n_items : a.item_hi;
+  for (int64_t w = a.item_lo + blockIdx.x; w < w_end; w += gridDim.x) {
     const int chunk = (int)(w / a.batch), b = (int)(w % a.batch);
     int64_t ctx, sel0 = 0;                   // selection mode: row b's slots sel0 .. sel0 + ctx
     if constexpr (SP) {
@@ -769,11 +770,14 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   auto k = decode_split_kernel<KVT, QT, G, D, SP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int64_t items = (int64_t)a.batch * a.n_splits;
-  const int64_t grid = items < num_sms() ? items : num_sms();
-  k<<<(unsigned)grid, 32 * a.n_kv_heads * (a.group / G), smem, st>>>(a, n_stages);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (a.phase != 2) {
+    const int64_t items = (a.item_hi < 0 ? (int64_t)a.batch * a.n_splits : a.item_hi) - a.item_lo;
+    const int64_t grid = items < num_sms() ? items : num_sms();
+    if (grid > 0) k<<<(unsigned)grid, 32 * a.n_kv_heads * (a.group / G), smem, st>>>(a, n_stages);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (a.phase == 1) return cudaSuccess;
   if (a.n_splits <= kSmallCombineChunks) {
     const int64_t items = (int64_t)a.batch * a.n_q_heads;
     decode_combine_small_kernel<D><<<(unsigned)((items + kCombineWarps - 1) / kCombineWarps),

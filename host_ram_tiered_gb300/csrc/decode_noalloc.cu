@@ -133,21 +133,7 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
   a.part_acc = scratch;
   a.part_ml = scratch + (size_t)batch * n_splits * n_q_heads * head_dim;
 
-  if (n_hi > 0 && staged) {
-    for (int64_t b = 0; b < batch; ++b) {
-      const size_t bytes = (size_t)n_hi * rb;
-      const uint8_t *ks = (const uint8_t *)k_host + (size_t)b * host_seq_stride_rows * rb;
-      const uint8_t *vs = (const uint8_t *)v_host + (size_t)b * host_seq_stride_rows * rb;
-      uint8_t *kd = (uint8_t *)staging_k + (size_t)b * n_hi * rb;
-      uint8_t *vd = (uint8_t *)staging_v + (size_t)b * n_hi * rb;
-      int e = cuda_status(cudaMemcpyAsync(kd, ks, bytes, cudaMemcpyDefault, st), "staging copy K");
-      if (e) return e;
-      e = cuda_status(cudaMemcpyAsync(vd, vs, bytes, cudaMemcpyDefault, st), "staging copy V");
-      if (e) return e;
-    }
-    a.k_hi = (const uint8_t *)staging_k; a.v_hi = (const uint8_t *)staging_v;
-    a.hi_seq_stride_rows = n_hi;
-    a.hi_device = 1;
-  }
+  if (n_hi > 0 && staged)
+    return launch_decode_staged(a, k_host, v_host, host_seq_stride_rows, staging_k, staging_v, st);
   return launch_decode(a, st);
 }

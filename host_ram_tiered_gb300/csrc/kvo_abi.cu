@@ -48,16 +48,17 @@ int classify(const void *p, size_t bytes) {
 }
 
 Ring *ring(int which) {
-  static Ring rings[2][64];
+  static Ring rings[3][64];
   int dev = 0;
-  if (which < 0 || which > 1 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (which < 0 || which > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   Ring &r = rings[which][dev];
   if (!r.side) {
     cudaStream_t s = nullptr, s2 = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
     if (cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    cudaEvent_t *ev[9] = {&r.fork, &r.join, &r.join2, &r.ready[0], &r.ready[1],
-                          &r.freed[0], &r.freed[1], &r.done2[0], &r.done2[1]};
+    cudaEvent_t *ev[13] = {&r.fork, &r.join, &r.join2, &r.ready[0], &r.ready[1],
+                           &r.freed[0], &r.freed[1], &r.done2[0], &r.done2[1],
+                           &r.part[0], &r.part[1], &r.part[2], &r.part[3]};
     for (cudaEvent_t *e : ev)
       if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     r.comp2 = s2;
@@ -305,6 +306,17 @@ size_t kvo_attn_decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t
   return decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx);
 }
 
+int kvo_attn_decode_launches(int64_t batch, int64_t max_ctx, int64_t head_dim, int64_t n_vram_cells,
+                             int staged) {
+  if (batch < 0 || max_ctx < 0 || head_dim < 0 || n_vram_cells < 0) return KVO_ERR_ARG;
+  if (batch == 0) return 0;
+  if (!staged || n_vram_cells >= max_ctx) return 2;
+  int sc = 0, ns = 0;
+  decode_geometry(batch, max_ctx, head_dim, &sc, &ns);
+  const StagedPlan pl = staged_plan(batch, sc, ns, n_vram_cells);
+  return (pl.c_v > 0 ? 1 : 0) + pl.parts + 1;
+}
+
 static int64_t kv_row_bytes(int dt, int64_t hkv, int64_t d) {
   if (dt == KVO_F16 || dt == KVO_BF16) return hkv * d * 2;
   if (dt == KVO_Q8_0) return (d % 32) ? -1 : hkv * (d / 32) * 34;
@@ -382,24 +394,8 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
   a.part_acc = (float *)workspace;
   a.part_ml = a.part_acc + (size_t)batch * a.n_splits * n_q_heads * head_dim;
 
-  if (n_hi > 0 && staged) {
-    // Copy-engine staging of the host rows [N, max_ctx) into VRAM; the kernel
-    // then reads the all-VRAM view.  Same arithmetic, so the same bits.
-    for (int64_t b = 0; b < batch; ++b) {
-      const size_t bytes = (size_t)n_hi * rb;
-      const uint8_t *ks = (const uint8_t *)k_host + (size_t)b * host_seq_stride_rows * rb;
-      const uint8_t *vs = (const uint8_t *)v_host + (size_t)b * host_seq_stride_rows * rb;
-      uint8_t *kd = (uint8_t *)staging_k + (size_t)b * n_hi * rb;
-      uint8_t *vd = (uint8_t *)staging_v + (size_t)b * n_hi * rb;
-      int s1 = cuda_status(cudaMemcpyAsync(kd, ks, bytes, cudaMemcpyDefault, st), "staging copy K");
-      if (s1) return s1;
-      s1 = cuda_status(cudaMemcpyAsync(vd, vs, bytes, cudaMemcpyDefault, st), "staging copy V");
-      if (s1) return s1;
-    }
-    a.k_hi = (const uint8_t *)staging_k; a.v_hi = (const uint8_t *)staging_v;
-    a.hi_seq_stride_rows = n_hi;
-    a.hi_device = 1;
-  }
+  if (n_hi > 0 && staged)
+    return launch_decode_staged(a, k_host, v_host, host_seq_stride_rows, staging_k, staging_v, st);
   return launch_decode(a, st);
 }
 

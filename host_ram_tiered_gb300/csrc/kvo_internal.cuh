@@ -27,14 +27,15 @@ int num_sms();                       // SMs of the current device (cached)
 // Library streams for staged work: a side stream that fills one arena slot
 // while the caller's stream scores the other, and a second launch stream so
 // that two row blocks run concurrently.  One set per user (0: prefill,
-// 1: sparse rows) and device, created on first use; every use forks from and
+// 1: sparse rows, 2: staged decode) and device, created on first use; every use forks from and
 // joins back into the caller's stream, under the user's own mutex.
 struct Ring {
   cudaStream_t side = nullptr, comp2 = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr, join2 = nullptr;
   cudaEvent_t ready[2] = {nullptr, nullptr}, freed[2] = {nullptr, nullptr}, done2[2] = {nullptr, nullptr};
+  cudaEvent_t part[4] = {nullptr, nullptr, nullptr, nullptr};
 };
-Ring *ring(int which);               // nullptr when the streams cannot be created
+Ring *ring(int which);               // nullptr when the streams cannot be created (which: 0..2)
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Device-side error bits set by kernels that skipped an out-of-range item.
@@ -63,6 +64,10 @@ struct DecodeArgs {
   float *out;
   float *part_acc, *part_ml;   // workspace: [B][splits][Hq][D], [B][splits][Hq][2]
   int split_cells, n_splits;
+  // Items this launch computes: [item_lo, item_hi) (item_hi < 0: all).
+  // phase 0: split kernel then combine; 1: split kernel only; 2: combine only.
+  int64_t item_lo = 0, item_hi = -1;
+  int phase = 0;
   // Running softmax state folded by the combine kernel (null: plain decode,
   // out = the normalised result).  init: this launch starts the state;
   // finalize: this launch writes out = acc / max(l, 1e-30).
@@ -90,6 +95,22 @@ void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *spli
 size_t decode_workspace_bytes(int64_t batch, int64_t n_q_heads, int64_t head_dim,
                               int64_t max_ctx);
 int launch_decode(const DecodeArgs &a, cudaStream_t st);   // kvo_status
+// Staged decode schedule: chunks [0, c_v) are decoded while the copy runs,
+// then copy part p covers chunks [ch_lo[p], ch_hi[p]) (cut at chunk
+// boundaries, the host rows among them).
+struct StagedPlan {
+  int64_t c_v = 0;
+  int parts = 1;
+  int64_t ch_lo[4] = {0, 0, 0, 0}, ch_hi[4] = {0, 0, 0, 0};
+};
+StagedPlan staged_plan(int64_t batch, int split_cells, int n_splits, int64_t n_vram);
+// Staged decode: the host rows [a.n_vram, a.max_ctx) of every sequence
+// (k_host / v_host, host_stride rows apart) are copied to staging_k /
+// staging_v ([batch][max_ctx - n_vram] rows) on a library stream in parts cut
+// at chunk boundaries; each part's chunks are decoded once it has landed, the
+// combine runs last.  Takes a's all-VRAM view fields from the arguments.
+int launch_decode_staged(DecodeArgs a, const void *k_host, const void *v_host, int64_t host_stride,
+                         void *staging_k, void *staging_v, cudaStream_t st);   // kvo_status
 // Sparse rows: the split kernel in selection mode (fp16 / bf16 caches), then
 // the combine (with the running-state fold when a.run_acc is set).
 int launch_sparse_rows(const DecodeArgs &a, cudaStream_t st);   // kvo_status

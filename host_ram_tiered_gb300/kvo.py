@@ -41,6 +41,7 @@ SIGNATURES = {
     "kvo_gather_blocks": (_int, [_vp, _vp, _i64, _i64, _i64, _i64, _int, _i64, _vp, _i64, _vp,
                                  _vp, _vp]),
     "kvo_attn_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
+    "kvo_attn_decode_launches": (_int, [_i64, _i64, _i64, _i64, _int]),
     "kvo_attn_decode_tiered": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp,
                                       _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz,
                                       _vp]),
@@ -167,6 +168,10 @@ def kvo_gather_blocks(k_plane, v_plane, n_seq, seq_stride_tokens, n_kv_heads, he
 
 def kvo_attn_decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx) -> int:
     return load().kvo_attn_decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx)
+
+
+def kvo_attn_decode_launches(batch, max_ctx, head_dim, n_vram_cells, staged) -> int:
+    return load().kvo_attn_decode_launches(batch, max_ctx, head_dim, n_vram_cells, int(bool(staged)))
 
 
 def kvo_attn_decode_tiered(q, q_dtype, batch, n_q_heads, n_kv_heads, head_dim, k_vram, v_vram,

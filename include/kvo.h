@@ -226,8 +226,15 @@ int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
  * ctx_len: device int32 [batch], each in [0, max_ctx].
  * staging_k / staging_v: NULL = the kernel reads host cells directly
  *   (SM loads through the device mapping).  Otherwise VRAM buffers of
- *   batch * (max_ctx - N) rows each: the host rows [N, max_ctx) are first
- *   copied there by the copy engine, and the kernel reads that all-VRAM view.
+ *   batch * (max_ctx - N) rows each: the host rows [N, max_ctx) are copied
+ *   there by the copy engine, and the kernel reads that all-VRAM view.  The
+ *   copy runs on a library stream (ordered after the work already on
+ *   `stream`, and `stream` waits for it before the call's last kernel), in
+ *   up to four parts cut at split boundaries when the decode spans more than
+ *   one wave of CTAs; each part's splits are decoded while the next part is
+ *   in flight.  The results are bit-identical to the direct read and to an
+ *   all-VRAM cache.  Staged calls from several host threads are serialised
+ *   inside the library while they enqueue.
  * out: device fp32 [batch][n_q_heads][head_dim].
  * workspace: device, at least kvo_attn_decode_workspace_bytes(...) bytes,
  *   16-byte aligned (split partials).
@@ -236,6 +243,15 @@ int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
  * ---------------------------------------------------------------------- */
 size_t kvo_attn_decode_workspace_bytes(int64_t batch, int64_t n_q_heads,
                                        int64_t head_dim, int64_t max_ctx);
+
+/* kvo_attn_decode_launches -- how many kernels one kvo_attn_decode_tiered
+ * call with these sizes launches on its stream (0 for batch 0, a negative
+ * kvo_status for a negative size).  Direct: 2 (split, combine).  Staged with
+ * host rows: the split kernel runs once per copy part (plus once for the
+ * chunks wholly in VRAM when it overlaps the copy), then the combine: 2 to
+ * 6.  Depends on the current device's SM count.  Host function. */
+int kvo_attn_decode_launches(int64_t batch, int64_t max_ctx, int64_t head_dim,
+                             int64_t n_vram_cells, int staged);
 
 int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch,
                            int64_t n_q_heads, int64_t n_kv_heads,

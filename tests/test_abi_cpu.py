@@ -98,6 +98,21 @@ def test_workspace_sizes_are_deterministic(kvo_lib):
     assert kvo.kvo_attn_prefill_workspace_bytes(-1, 32) == 0
 
 
+def test_decode_launch_counts(kvo_lib):
+    # direct: split + combine; nothing for an empty batch; an error for a negative size
+    assert kvo.kvo_attn_decode_launches(1, 184320, 128, 8192, 0) == 2
+    assert kvo.kvo_attn_decode_launches(0, 184320, 128, 8192, 1) == 0
+    assert kvo.kvo_attn_decode_launches(-1, 184320, 128, 8192, 1) < 0
+    # staged with no host rows is the direct call
+    assert kvo.kvo_attn_decode_launches(1, 4096, 128, 4096, 1) == 2
+    # one wave of splits: one split launch after the whole copy, then the combine
+    assert kvo.kvo_attn_decode_launches(1, 1024, 128, 512, 1) == 2
+    # many waves: the VRAM splits, one launch per copy part (at most four), the combine
+    n = kvo.kvo_attn_decode_launches(1, 184320, 128, 8192, 1)
+    assert 4 <= n <= 6
+    assert kvo.kvo_attn_decode_launches(1, 184320, 128, 0, 1) == n - 1
+
+
 # ---------------------------------------------------------------- canonical fragments
 
 RUNS = [(0, 1024, 0, 256, 4, 256), (4096, 0, 1024, 0, 1, 512), (2048, 64, 3000, 96, 3, 32)]

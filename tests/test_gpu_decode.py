@@ -87,6 +87,29 @@ def test_batch_with_ragged_and_empty_contexts():
     assert np.array_equal(out.view(np.uint32), allv.view(np.uint32))
 
 
+def test_staged_copy_in_parts_is_bit_identical():
+    # Four sequences of up to 30,000 cells: 188 chunks of 160 cells each, 752
+    # work items or five waves of CTAs, so the staged call decodes the chunks wholly in VRAM
+    # while the host tail is copied in four parts, and each part's chunks as
+    # it lands.  Ragged lengths: full, inside the VRAM head, ending inside a
+    # part, one short of full.
+    g = synth.rng(31, 23)
+    B, L, hq, hkv, d, N = 4, 30000, 8, 2, 128, 5000
+    k, v = cells(B * L, hkv, d, oracle.BF16, g)
+    q, qd = _q(B, hq, d, "bf16", g)
+    lens = [L, 2500, 11111, L - 1]
+    s = scale_for(d)
+    assert kvo.kvo_attn_decode_launches(B, L, d, N, 1) == 6
+    tc = Tiered(k, v, N, batch=B)
+    staged = run_decode(tc, qd, kvo.BF16, hq, hkv, d, kvo.BF16, _ctx(lens), s, staging=True)
+    direct = run_decode(tc, qd, kvo.BF16, hq, hkv, d, kvo.BF16, _ctx(lens), s)
+    allv = run_decode(Tiered(k, v, L, batch=B), qd, kvo.BF16, hq, hkv, d, kvo.BF16, _ctx(lens), s)
+    assert np.array_equal(staged.view(np.uint32), direct.view(np.uint32))
+    assert np.array_equal(staged.view(np.uint32), allv.view(np.uint32))
+    ref = _oracle(tc, q, oracle.BF16, hq, hkv, d, oracle.BF16, lens, s)
+    assert normwise_rel_err(staged, ref) <= REL_TOL
+
+
 @pytest.mark.parametrize("hq,hkv,d,kvdt", [(8, 8, 128, oracle.F16), (64, 8, 128, oracle.BF16),
                                            (12, 4, 64, oracle.Q8_0), (7, 1, 64, oracle.F16),
                                            (40, 8, 64, oracle.BF16)])
