@@ -880,13 +880,13 @@ def gpu_launch_count(K, rows):
         # direct: head + host tail, 2 row blocks each
         n += K * (2 + 48 * 2) + min(K, 3) * 4
     if "sparse" in rows:
-        # staged: partition + buckets x (page gather + 2 row blocks x (split + combine)), the
-        # arena holding two slots of arena / (4 page_bytes) pages; direct: 2 row blocks x
-        # (split + combine)
+        # staged: partition + buckets x (page gather + 2 row blocks x a split kernel that folds
+        # its one chunk per row itself), the arena holding two slots of arena / (4 page_bytes)
+        # pages; direct: 2 row blocks x (split + combine)
         page_bytes = SR_PS * SR_HKV * SR_D * 2
         slot = SR_ARENA // (4 * page_bytes)
         buckets = -(-(SR_L // SR_PS) // slot)
-        n += K * (1 + buckets * (1 + 2 * 2)) + max(1, min(K, 2)) * 4
+        n += K * (1 + buckets * (1 + 2)) + max(1, min(K, 2)) * 4
     return n
 
 

@@ -231,17 +231,19 @@ __device__ __forceinline__ const uint8_t *sparse_row(const DecodeArgs &a, int64_
   return (is_v ? a.v_hi : a.k_hi) + (page * a.page_size + j % a.page_size) * a.row_bytes;
 }
 
-// Slots [s0, s0 + n) of work row b's selection list, K and V, into one stage.
-// Warp w takes slots w, w + warps, ...; a padding slot gets a zero V row (its
-// weight is 0 and must meet finite values).  Async: 16-byte cp.async copies
-// (device-resident arena); else 16-byte loads through the mapping.
+// The n (<= 32) slots of a tile, K and V, into one stage; lane r of every
+// warp holds slot r's cache position in jl (one coalesced load per warp, made
+// ahead of time by the caller).  Warp w takes slots w, w + warps, ...; a
+// padding slot gets a zero V row (its weight is 0 and must meet finite
+// values).  Async: 16-byte cp.async copies (device-resident arena); else
+// 16-byte loads through the mapping.
 template <bool ASYNC>
-__device__ __forceinline__ void fill_sparse(const DecodeArgs &a, int b, int64_t s0, int n,
-                                            uint8_t *sk, uint8_t *sv, int64_t pitch) {
+__device__ __forceinline__ void fill_sparse(const DecodeArgs &a, int32_t jl, int n, uint8_t *sk,
+                                            uint8_t *sv, int64_t pitch) {
   const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpr = (int)(a.row_bytes >> 4);
-  for (int r = warp; r < n; r += warps) {
-    const int64_t j = a.indices[(int64_t)b * a.max_ctx + s0 + r];
+  for (int r = warp; r < n; r += warps) {    // warp-uniform; r < n <= 32
+    const int64_t j = __shfl_sync(0xffffffffu, jl, r);
     const int4 *ks = (const int4 *)sparse_row(a, j, false);
     const int4 *vs = (const int4 *)sparse_row(a, j, true);
     if (!ks && lane == 0 && j >= a.win_lo && j < a.win_hi) atomicOr(a.err, kErrPageTable);
@@ -338,17 +340,24 @@ __device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const ui
   }
 }
 
-// Scores of the tile's 32 cells: lane c ends with the G scores of cell c.
+// Scores of the tile's 32 cells: lane c ends with the G scores of cell c
+// (meaningful for c < n only: a pass whose cells all lie past n is skipped).
 template <int KVT, int G, int D>
 __device__ __forceinline__ void qk_tile(const WarpState<KVT, G, D> &ws, const uint8_t *sk,
-                                        int64_t pitch, int g, int lane, float scale_log2,
+                                        int64_t pitch, int g, int lane, float scale_log2, int n,
                                         float *s) {
   using S = Shape<KVT, G, D>;
   const int qq = lane / S::CPP, cl = lane % S::CPP;
   float v[S::NP][G];
 #pragma unroll
-  for (int ps = 0; ps < S::NP; ++ps)
-    qk_cell<KVT, G, D>(ws, sk + (int64_t)(cl + S::CPP * ps) * pitch, g, qq, scale_log2, v[ps]);
+  for (int ps = 0; ps < S::NP; ++ps) {
+    if (ps == 0 || ps * S::CPP < n) {        // warp-uniform
+      qk_cell<KVT, G, D>(ws, sk + (int64_t)(cl + S::CPP * ps) * pitch, g, qq, scale_log2, v[ps]);
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) v[ps][h] = 0.f;
+    }
+  }
   // Transposing butterfly: stage k pairs passes that differ in bit k and
   // keeps the one whose bit k equals bit k of qq, adding the partner lane's
   // (lane ^ (CPP << k)) other half.  After log2(LPC) stages the remaining
@@ -438,142 +447,195 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
 
   const int64_t w_end = a.item_hi < 0 ? n_items : a.item_hi;
-  for (int64_t w = a.item_lo + blockIdx.x; w < w_end; w += gridDim.x) {
-    const int chunk = (int)(w / a.batch), b = (int)(w % a.batch);
-    int64_t ctx, sel0 = 0;                   // selection mode: row b's slots sel0 .. sel0 + ctx
-    if constexpr (SP) {
+
+  // Work item w = (chunk w / batch, row or sequence w % batch); nt = 0 for a
+  // chunk beyond the context (never combined).
+  struct Item {
+    int64_t w, cs, ce, sel0;
+    int chunk, b, nt;
+  };
+  auto item_at = [&](int64_t w) {
+    Item it;
+    it.w = w;
+    it.nt = 0;
+    it.cs = it.ce = it.sel0 = 0;
+    it.chunk = it.b = 0;
+    if (w >= w_end) return it;
+    it.chunk = (int)(w / a.batch);
+    it.b = (int)(w % a.batch);
+    int64_t ctx;
+    if constexpr (SP) {                      // selection mode: the row's slots sel0 .. sel0 + ctx
       ctx = a.max_ctx;
       if (a.offs) {
-        const int32_t *ob = a.offs + (int64_t)b * a.offs_stride + a.bucket;
-        sel0 = ob[0];
+        const int32_t *ob = a.offs + (int64_t)it.b * a.offs_stride + a.bucket;
+        it.sel0 = ob[0];
         ctx = ob[1] - ob[0];
       }
     } else {
-      ctx = a.ctx_len[b] < a.max_ctx ? a.ctx_len[b] : a.max_ctx;
+      ctx = a.ctx_len[it.b] < a.max_ctx ? a.ctx_len[it.b] : a.max_ctx;
     }
-    const int64_t cs = (int64_t)chunk * a.split_cells;
-    const int64_t ce = cs + a.split_cells < ctx ? cs + a.split_cells : ctx;
-    if (cs >= ce) continue;                  // chunk beyond the context: never combined
-    const int ntiles = (int)((ce - cs + kTile - 1) / kTile);
-
-    WarpState<KVT, G, D> ws;
-    {
-      // query slice of each of the warp's heads: dims [qq*DL, qq*DL + DL)
-      const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)b * a.n_q_heads + (size_t)h0) * D;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < S::DL / 8; ++i) {
-          const uint4 u = qp[i];
-          ws.q[h][4 * i] = u.x; ws.q[h][4 * i + 1] = u.y;
-          ws.q[h][4 * i + 2] = u.z; ws.q[h][4 * i + 3] = u.w;
-          if constexpr (KVT == KVO_Q8_0) {
-            const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sum += h2f(uw[e] & 0xffff, QT) + h2f(uw[e] >> 16, QT);
-          }
-        }
-        ws.qb[h] = __fmul_rn(-1152.f, sum);
-        ws.m[h] = -INFINITY;
-        ws.l[h] = 0.f;
-#pragma unroll
-        for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = 0ull;
-      }
+    it.cs = (int64_t)it.chunk * a.split_cells;
+    it.ce = it.cs + a.split_cells < ctx ? it.cs + a.split_cells : ctx;
+    if (it.cs < it.ce) it.nt = (int)((it.ce - it.cs + kTile - 1) / kTile);
+    return it;
+  };
+  // One chunk per row (selection mode, staged): fold the chunk's (m, l, acc)
+  // straight into the row's running state (the per-bucket fold of the
+  // ExLlamaV3 qsa-kv-offload patch, in log2 units), or finish the row:
+  //   m' = max(m, m_b); alpha = 2^(m - m') (0 if m = -inf); beta = 2^(m_b - m') (0 if m_b = -inf)
+  //   acc = alpha acc + beta acc_b; l = alpha l + beta l_b
+  // This warp alone owns the (row, head) pairs it folds.
+  auto fold = [&](const Item &it, int h, float m_b, float l_b, const float *acc_b) {
+    const size_t oi = (size_t)it.b * a.n_q_heads + h0 + h;
+    float m_run = -INFINITY, l_run = 0.f;
+    if (!a.init) {
+      m_run = a.run_ml[oi * 2];
+      l_run = a.run_ml[oi * 2 + 1];
     }
-
-    // Device-resident chunk: the ring.  Anything else: tile by tile.
-    const bool ring = n_stages >= 2 && (SP ? a.sparse_staged != 0 : (ce <= a.n_vram || a.hi_device));
-    __syncthreads();                         // smem of the previous chunk fully consumed
-    if (ring) {
-      for (int t = 0; t < n_stages - 1; ++t) {
-        if (t < ntiles) {
-          const int64_t t0 = cs + (int64_t)t * kTile;
-          uint8_t *st = smem + t * stage_bytes;
-          const int nt = (int)(ce - t0 < kTile ? ce - t0 : kTile);
-          if constexpr (SP) fill_sparse<true>(a, b, sel0 + t0, nt, st, st + kTile * pitch, pitch);
-          else fill_async(a, b, t0, nt, st, st + kTile * pitch, pitch, cpr);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-      }
+    const float m_new = fmaxf(m_run, m_b);
+    const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+    const float beta = m_b == -INFINITY ? 0.f : exp2f(m_b - m_new);
+    const float l_new = alpha * l_run + beta * l_b;
+    float *ra = a.run_acc + oi * D + lane * S::DV;
+    float *o = a.out + oi * D + lane * S::DV;
+#pragma unroll
+    for (int i = 0; i < S::DV; ++i) {
+      const float acc_new = alpha * (a.init ? 0.f : ra[i]) + beta * acc_b[i];
+      if (a.finalize) o[i] = acc_new / fmaxf(l_new, 1e-30f);
+      else ra[i] = acc_new;
     }
-    for (int t = 0; t < ntiles; ++t) {
-      const int64_t t0 = cs + (int64_t)t * kTile;
-      const int n = (int)(ce - t0 < kTile ? ce - t0 : kTile);
-      uint8_t *st;
-      if (ring) {
-        if (n_stages == 3) asm volatile("cp.async.wait_group 1;" ::: "memory");
-        else asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();                     // tile t landed; tile t-1 fully consumed
-        const int tn = t + n_stages - 1;
-        if (tn < ntiles) {
-          const int64_t tn0 = cs + (int64_t)tn * kTile;
-          uint8_t *sn = smem + (tn % n_stages) * stage_bytes;
-          const int nn = (int)(ce - tn0 < kTile ? ce - tn0 : kTile);
-          if constexpr (SP) fill_sparse<true>(a, b, sel0 + tn0, nn, sn, sn + kTile * pitch, pitch);
-          else fill_async(a, b, tn0, nn, sn, sn + kTile * pitch, pitch, cpr);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        st = smem + (t % n_stages) * stage_bytes;
-      } else {
-        if (t > 0) __syncthreads();          // previous tile fully consumed
-        st = smem;
-        if constexpr (SP) fill_sparse<false>(a, b, sel0 + t0, n, st, st + kTile * pitch, pitch);
-        else fill_sync(a, b, t0, n, st, st + kTile * pitch, pitch, cpr);
-        __syncthreads();
-      }
-      const uint8_t *sk = st, *sv = st + kTile * pitch;
-
-      // scores of cell `lane`, then the online softmax
-      float s[G];
-      qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, s);
-      bool valid = lane < n;
-      if constexpr (SP)                      // staged picks are grouped inside the window already
-        if (!a.offs) valid = valid && sparse_row(a, a.indices[(int64_t)b * a.max_ctx + sel0 + t0 + lane], false);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float sv_h = valid ? s[h] : -INFINITY;
-        const float tmax = warp_max(sv_h);
-        if (tmax > ws.m[h] + 8.f) {          // warp-uniform: move the reference
-          const float alpha = exp2f(__fsub_rn(ws.m[h], tmax));
-          const uint64_t aa = pk2(alpha, alpha);
-          ws.l[h] = __fmul_rn(ws.l[h], alpha);
-#pragma unroll
-          for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = fmul2(ws.acc[h][i], aa);
-          ws.m[h] = tmax;
-        }
-        const float p = valid ? exp2f(__fsub_rn(sv_h, ws.m[h])) : 0.f;
-        ws.l[h] = __fadd_rn(ws.l[h], p);
-        pbuf[lane * GP + h] = pk2(p, p);
-      }
-      __syncwarp();
-      for (int c = 0; c < n; ++c) {
-        uint64_t vp[S::DV / 2];
-        v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
-        const uint64_t *pc = pbuf + c * GP;
-        uint64_t pp[G];
-#pragma unroll
-        for (int h = 0; h + 1 < G; h += 2) {
-          const ulonglong2 u = *(const ulonglong2 *)(pc + h);   // h and GP even: 16-byte aligned
-          pp[h] = u.x; pp[h + 1] = u.y;
-        }
-        if constexpr (G & 1) pp[G - 1] = pc[G - 1];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = ffma2(pp[h], vp[i], ws.acc[h][i]);
-      }
-      __syncwarp();                          // pbuf reads done before the next tile's writes
+    __syncwarp();                            // every lane has read run_ml
+    if (!a.finalize && lane == 0) {
+      a.run_ml[oi * 2] = m_new;
+      a.run_ml[oi * 2 + 1] = l_new;
     }
-    if (ring) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  };
+  // A row with no picks in this bucket: the running state only needs to be
+  // started (first bucket) or finished (last bucket).
+  auto fold_empty = [&](const Item &it) {
+    if (!(a.init || a.finalize)) return;
+    float z[S::DV];
+#pragma unroll
+    for (int i = 0; i < S::DV; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int h = 0; h < G; ++h) fold(it, h, -INFINITY, 0.f, z);
+  };
 
-    // partial of this chunk: acc (this lane's dims), m, l
+  // First non-empty item at or after w (stride gridDim.x); fold_empties: the
+  // skipped items of a launch that folds in the split kernel are folded here.
+  auto next_item = [&](int64_t w, bool fold_empties) {
+    Item it = item_at(w);
+    while (it.w < w_end && it.nt == 0) {
+      if (SP && fold_empties && a.fold_in_split) fold_empty(it);
+      it = item_at(it.w + gridDim.x);
+    }
+    return it;
+  };
+  // Selection mode: lane r's cache position for slot r of tile t of `it`
+  // (meaningless past the tile's end or past the launch's items).
+  auto picks = [&](const Item &it, int t) -> int32_t {
+    if constexpr (SP) {
+      const int64_t t0 = it.cs + (int64_t)t * kTile;
+      if (it.w < w_end && t0 + lane < it.ce) return a.indices[(int64_t)it.b * a.max_ctx + it.sel0 + t0 + lane];
+    }
+    return -1;
+  };
+  // Device-resident rows: asynchronous copies into a ring stage (jl: picks()).
+  auto issue = [&](const Item &it, int t, uint8_t *st, int32_t jl) {
+    const int64_t t0 = it.cs + (int64_t)t * kTile;
+    const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
+    if constexpr (SP) fill_sparse<true>(a, jl, n, st, st + kTile * pitch, pitch);
+    else fill_async(a, it.b, t0, n, st, st + kTile * pitch, pitch, cpr);
+  };
+
+  WarpState<KVT, G, D> ws;
+  auto init_item = [&](const Item &it) {
+    // query slice of each of the warp's heads: dims [qq*DL, qq*DL + DL)
+    const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)it.b * a.n_q_heads + (size_t)h0) * D;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < S::DL / 8; ++i) {
+        const uint4 u = qp[i];
+        ws.q[h][4 * i] = u.x; ws.q[h][4 * i + 1] = u.y;
+        ws.q[h][4 * i + 2] = u.z; ws.q[h][4 * i + 3] = u.w;
+        if constexpr (KVT == KVO_Q8_0) {
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sum += h2f(uw[e] & 0xffff, QT) + h2f(uw[e] >> 16, QT);
+        }
+      }
+      ws.qb[h] = __fmul_rn(-1152.f, sum);
+      ws.m[h] = -INFINITY;
+      ws.l[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = 0ull;
+    }
+  };
+
+  // One tile of item `it` (tile t, rows in st): scores of cell `lane`, the
+  // online softmax, then P*V.
+  auto compute_tile = [&](const Item &it, int t, const uint8_t *st) {
+    const int64_t t0 = it.cs + (int64_t)t * kTile;
+    const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
+    const uint8_t *sk = st, *sv = st + kTile * pitch;
+    float s[G];
+    qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, n, s);
+    bool valid = lane < n;
+    if constexpr (SP)                        // staged picks are grouped inside the window already
+      if (!a.offs) valid = valid && sparse_row(a, a.indices[(int64_t)it.b * a.max_ctx + it.sel0 + t0 + lane], false);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float sv_h = valid ? s[h] : -INFINITY;
+      const float tmax = warp_max(sv_h);
+      if (tmax > ws.m[h] + 8.f) {            // warp-uniform: move the reference
+        const float alpha = exp2f(__fsub_rn(ws.m[h], tmax));
+        const uint64_t aa = pk2(alpha, alpha);
+        ws.l[h] = __fmul_rn(ws.l[h], alpha);
+#pragma unroll
+        for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = fmul2(ws.acc[h][i], aa);
+        ws.m[h] = tmax;
+      }
+      const float p = valid ? exp2f(__fsub_rn(sv_h, ws.m[h])) : 0.f;
+      ws.l[h] = __fadd_rn(ws.l[h], p);
+      pbuf[lane * GP + h] = pk2(p, p);
+    }
+    __syncwarp();
+    for (int c = 0; c < n; ++c) {
+      uint64_t vp[S::DV / 2];
+      v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
+      const uint64_t *pc = pbuf + c * GP;
+      uint64_t pp[G];
+#pragma unroll
+      for (int h = 0; h + 1 < G; h += 2) {
+        const ulonglong2 u = *(const ulonglong2 *)(pc + h);   // h and GP even: 16-byte aligned
+        pp[h] = u.x; pp[h + 1] = u.y;
+      }
+      if constexpr (G & 1) pp[G - 1] = pc[G - 1];
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = ffma2(pp[h], vp[i], ws.acc[h][i]);
+    }
+    __syncwarp();                            // pbuf reads done before the next tile's writes
+  };
+
+  // Partial of an item: acc (this lane's dims), m, l.
+  auto write_partial = [&](const Item &it) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float lsum = warp_sum(ws.l[h]);
+      if (SP && a.fold_in_split) {
+        float x[S::DV];
+#pragma unroll
+        for (int i = 0; i < S::DV / 2; ++i) upk2(ws.acc[h][i], x[2 * i], x[2 * i + 1]);
+        fold(it, h, ws.m[h], lsum, x);
+        continue;
+      }
       const int qh = h0 + h;
-      const size_t pi = ((size_t)b * a.n_splits + chunk) * a.n_q_heads + qh;
+      const size_t pi = ((size_t)it.b * a.n_splits + it.chunk) * a.n_q_heads + qh;
       float *pa = a.part_acc + pi * D + lane * S::DV;
       if constexpr (S::DV == 4) {
         float x0, x1, x2, x3;
@@ -590,6 +652,117 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         a.part_ml[pi * 2 + 1] = lsum;
       }
     }
+  };
+
+  if (SP && a.all_ring) {
+    // Every row of the launch is device-resident: one continuous ring over all
+    // of this CTA's (item, tile) pairs, so the next item's first tiles are in
+    // flight while the current one finishes.  fi/ft: the next tile to fill;
+    // ci/ct: the tile being computed.  With a single stage (wide rows) each
+    // tile is copied asynchronously and waited for before its compute.
+    // fj: the picks of tile (fi, ft), loaded one tile ahead so that their
+    // latency hides behind a tile's compute.
+    Item ci = next_item(a.item_lo + blockIdx.x, true), fi = ci;
+    int ft = 0, ct = 0;
+    if (ci.w >= w_end) return;
+    auto advance = [&](Item &it, int &t) {
+      if (++t == it.nt) {
+        it = next_item(it.w + gridDim.x, false);
+        t = 0;
+      }
+    };
+    int32_t fj = picks(fi, ft);
+    for (int s = 0; s < n_stages - 1; ++s) {
+      if (fi.w < w_end) {
+        issue(fi, ft, smem + s * stage_bytes, fj);
+        advance(fi, ft);
+        fj = picks(fi, ft);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    init_item(ci);
+    for (int64_t k = 0;; ++k) {
+      if (n_stages == 1) {
+        __syncthreads();                     // tile k-1 fully consumed
+        issue(fi, ft, smem, fj);
+        advance(fi, ft);
+        fj = picks(fi, ft);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();                     // tile k landed
+      } else {
+        if (n_stages == 3) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();                     // tile k landed; tile k-1 fully consumed
+        if (fi.w < w_end) {
+          issue(fi, ft, smem + ((k + n_stages - 1) % n_stages) * stage_bytes, fj);
+          advance(fi, ft);
+          fj = picks(fi, ft);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+      compute_tile(ci, ct, smem + (k % n_stages) * stage_bytes);
+      if (ct + 1 == ci.nt) {
+        write_partial(ci);
+        ci = next_item(ci.w + gridDim.x, true);
+        ct = 0;
+        if (ci.w >= w_end) break;
+        init_item(ci);
+      } else {
+        ++ct;
+      }
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    return;
+  }
+
+  // Items one at a time: a device-resident item streams through the ring, an
+  // item with host-resident rows is filled tile by tile.
+  for (int64_t w = a.item_lo + blockIdx.x; w < w_end; w += gridDim.x) {
+    const Item it = item_at(w);
+    if (it.nt == 0) {
+      if (SP && a.fold_in_split) fold_empty(it);
+      continue;
+    }
+    init_item(it);
+    const bool dev = SP ? a.sparse_staged != 0 : (it.ce <= a.n_vram || a.hi_device);
+    const bool ring = n_stages >= 2 && dev;
+    __syncthreads();                         // smem of the previous item fully consumed
+    if (ring) {
+      for (int t = 0; t < n_stages - 1; ++t) {
+        if (t < it.nt) issue(it, t, smem + t * stage_bytes, picks(it, t));
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
+    }
+    for (int t = 0; t < it.nt; ++t) {
+      uint8_t *st;
+      if (ring) {
+        if (n_stages == 3) asm volatile("cp.async.wait_group 1;" ::: "memory");
+        else asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();                     // tile t landed; tile t-1 fully consumed
+        const int tn = t + n_stages - 1;
+        if (tn < it.nt) issue(it, tn, smem + (tn % n_stages) * stage_bytes, picks(it, tn));
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        st = smem + (t % n_stages) * stage_bytes;
+      } else {
+        if (t > 0) __syncthreads();          // previous tile fully consumed
+        st = smem;
+        if (dev) {                           // one stage: copy asynchronously, then wait
+          issue(it, t, st, picks(it, t));
+          asm volatile("cp.async.commit_group;" ::: "memory");
+          asm volatile("cp.async.wait_group 0;" ::: "memory");
+        } else {
+          const int64_t t0 = it.cs + (int64_t)t * kTile;
+          const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
+          if constexpr (SP) fill_sparse<false>(a, picks(it, t), n, st, st + kTile * pitch, pitch);
+          else fill_sync(a, it.b, t0, n, st, st + kTile * pitch, pitch, cpr);
+        }
+        __syncthreads();
+      }
+      compute_tile(it, t, st);
+    }
+    if (ring) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    write_partial(it);
   }
 }
 
@@ -772,7 +945,8 @@ cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (a.phase != 2) {
     const int64_t items = (a.item_hi < 0 ? (int64_t)a.batch * a.n_splits : a.item_hi) - a.item_lo;
-    const int64_t grid = items < num_sms() ? items : num_sms();
+    const int64_t cap = a.grid_cap > 0 && a.grid_cap < num_sms() ? a.grid_cap : num_sms();
+    const int64_t grid = items < cap ? items : cap;
     if (grid > 0) k<<<(unsigned)grid, 32 * a.n_kv_heads * (a.group / G), smem, st>>>(a, n_stages);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -86,6 +86,15 @@ struct DecodeArgs {
   const int32_t *block_table = nullptr;
   int64_t page_size = 1, n_pages_total = 0;
   int sparse_staged = 0;
+  // Every row the launch reads is device-resident: the split kernel runs one
+  // continuous copy ring over all of a CTA's items.
+  int all_ring = 0;
+  // At most this many CTAs for the split kernel (0: one per SM), leaving SMs
+  // free for a kernel that runs beside it on another stream.
+  int grid_cap = 0;
+  // Selection mode with one chunk per row and a running state: the split
+  // kernel folds each row's chunk into run_acc / run_ml itself (no combine).
+  int fold_in_split = 0;
   uint32_t *err = nullptr;     // device error word (sparse: bad page-table entries)
 };
 // Split geometry for a decode: fixed cell ranges that depend on max_ctx and
@@ -116,11 +125,11 @@ int launch_decode_staged(DecodeArgs a, const void *k_host, const void *v_host, i
 int launch_sparse_rows(const DecodeArgs &a, cudaStream_t st);   // kvo_status
 // Copy pages block_table[p0 .. p0 + n) of the K and V planes (page_bytes each)
 // to arena slots 0 .. n-1; entries outside [0, n_pages_total) are skipped and
-// set kErrPageTable.
+// set kErrPageTable.  At most max_ctas CTAs (0: four per SM).
 cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t page_bytes,
                                const int32_t *block_table, int64_t p0, int64_t n,
                                int64_t n_pages_total, void *k_arena, void *v_arena, uint32_t *err,
-                               cudaStream_t st);
+                               int max_ctas, cudaStream_t st);
 
 struct PrefillArgs {
   const uint16_t *q;           // [rows][Hq][D] (rows of this launch start at q)

@@ -23,37 +23,46 @@ template cudaError_t launch_kv<KVO_BF16, true>(const DecodeArgs &a, cudaStream_t
 namespace {
 
 constexpr int kGatherThreads = 256;
+// Staged with two arena slots: the split kernel leaves this many SMs to the
+// next bucket's page gather, which runs beside it on the library stream (a
+// split CTA holds a whole SM's registers, so a gather CTA could not start on
+// an SM it occupies).
+constexpr int kGatherSms = 16;
 constexpr size_t kPartitionSmem = 200 * 1024;   // bucket counters per CTA
 
-// Pages block_table[p0 .. p0 + n) of K and V -> arena slots 0 .. n-1, one
-// (page, tensor) per CTA iteration, 16-byte vectors, 4 loads per thread in
-// flight.
+// Pages block_table[p0 .. p0 + n) of K and V -> arena slots 0 .. n-1.  Work
+// item = (tensor, page, slice): each page is cut into `parts` slices so that
+// enough CTAs (and 16-byte loads, 4 per thread) are in flight to fill the
+// host link; a CTA loops over items with stride gridDim.x.
 __global__ void __launch_bounds__(kGatherThreads)
 page_gather_kernel(const uint8_t *kp, const uint8_t *vp, int64_t page_bytes, const int32_t *bt, int64_t p0,
-                   int64_t n, int64_t n_pages_total, uint8_t *ka, uint8_t *va, uint32_t *err) {
+                   int64_t n, int64_t n_pages_total, uint8_t *ka, uint8_t *va, uint32_t *err, int parts) {
   const int64_t cpp = page_bytes >> 4;
-  for (int64_t item = blockIdx.x; item < 2 * n; item += gridDim.x) {
-    const bool is_v = item >= n;
-    const int64_t i = is_v ? item - n : item;
+  const int64_t per = (cpp + parts - 1) / parts;    // 16-byte chunks per slice
+  for (int64_t item = blockIdx.x; item < 2 * n * parts; item += gridDim.x) {
+    const int64_t pg = item / parts;
+    const int64_t c_lo = (item % parts) * per, c_hi = c_lo + per < cpp ? c_lo + per : cpp;
+    const bool is_v = pg >= n;
+    const int64_t i = is_v ? pg - n : pg;
     const int64_t page = bt[p0 + i];
     if (page < 0 || page >= n_pages_total) {
-      if (threadIdx.x == 0) atomicOr(err, kErrPageTable);
+      if (threadIdx.x == 0 && item % parts == 0) atomicOr(err, kErrPageTable);
       continue;
     }
     const int4 *src = (const int4 *)((is_v ? vp : kp) + page * page_bytes);
     int4 *dst = (int4 *)((is_v ? va : ka) + i * page_bytes);
     constexpr int U = 4;
-    for (int64_t c0 = threadIdx.x; c0 < cpp; c0 += (int64_t)U * kGatherThreads) {
+    for (int64_t c0 = c_lo + threadIdx.x; c0 < c_hi; c0 += (int64_t)U * kGatherThreads) {
       int4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + (int64_t)u * kGatherThreads;
-        if (c < cpp) v[u] = src[c];
+        if (c < c_hi) v[u] = src[c];
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int64_t c = c0 + (int64_t)u * kGatherThreads;
-        if (c < cpp) dst[c] = v[u];
+        if (c < c_hi) dst[c] = v[u];
       }
     }
   }
@@ -172,14 +181,19 @@ SparseWs sparse_workspace(int64_t rows, int64_t n_q_heads, int64_t head_dim, int
 
 cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t page_bytes,
                                const int32_t *block_table, int64_t p0, int64_t n, int64_t n_pages_total,
-                               void *k_arena, void *v_arena, uint32_t *err, cudaStream_t st) {
+                               void *k_arena, void *v_arena, uint32_t *err, int max_ctas, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  int64_t grid = 2 * n;
-  const int64_t cap = (int64_t)num_sms() * 4;
+  const int64_t cap = max_ctas > 0 ? max_ctas : (int64_t)num_sms() * 4;
+  // slices per page: enough items for every CTA, each slice at least 16 KiB
+  int64_t parts = (cap + 2 * n - 1) / (2 * n);
+  const int64_t max_parts = (page_bytes >> 4) / 1024 > 0 ? (page_bytes >> 4) / 1024 : 1;
+  if (parts > max_parts) parts = max_parts;
+  if (parts < 1) parts = 1;
+  int64_t grid = 2 * n * parts;
   if (grid > cap) grid = cap;
   page_gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(
       (const uint8_t *)k_pages, (const uint8_t *)v_pages, page_bytes, block_table, p0, n, n_pages_total,
-      (uint8_t *)k_arena, (uint8_t *)v_arena, err);
+      (uint8_t *)k_arena, (uint8_t *)v_arena, err, (int)parts);
   return cudaGetLastError();
 }
 
@@ -339,7 +353,8 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
         if (e) return e;
       }
       const cudaError_t e = launch_page_gather(k_pages, v_pages, page_bytes, block_table, p0, np, n_pages,
-                                               (void *)base.k_lo, (void *)base.v_lo, err, gs);
+                                               (void *)base.k_lo, (void *)base.v_lo, err,
+                                               rg ? 8 * kGatherSms : 0, gs);
       if (e != cudaSuccess) return cuda_status(e, "page gather launch");
       if (rg) {
         int e2 = cuda_status(cudaEventRecord(rg->ready[slot], gs), "cudaEventRecord");
@@ -359,6 +374,8 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
       a.out = out + (size_t)r0 * n_q_heads * head_dim;
       if (staged) {
         a.sparse_staged = 1;
+        a.all_ring = 1;
+        if (rg && num_sms() > 2 * kGatherSms) a.grid_cap = num_sms() - kGatherSms;
         a.indices = grouped + (size_t)r0 * k_pad;
         a.offs = offs + (size_t)r0 * (n_b + 1);
         a.offs_stride = n_b + 1;
@@ -369,6 +386,10 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
         a.run_ml = run_ml + (size_t)r0 * n_q_heads * 2;
         a.init = bk == 0;
         a.finalize = bk == n_buckets - 1;
+        if (n_chunks == 1) {                 // one chunk per row: the split kernel folds it
+          a.fold_in_split = 1;
+          a.phase = 1;
+        }
       } else {
         a.sparse_staged = 0;
         a.indices = indices + (size_t)r0 * k_pad;
