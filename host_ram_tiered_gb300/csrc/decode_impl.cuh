@@ -575,12 +575,11 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     }
   };
 
-  // One tile of item `it` (tile t, rows in st): scores of cell `lane`, the
-  // online softmax, then P*V.
-  auto compute_tile = [&](const Item &it, int t, const uint8_t *st) {
+  // One tile of item `it` (tile t, K rows at sk, V rows at sv): scores of
+  // cell `lane` and the online softmax (weights to pbuf), then P*V.
+  auto compute_qk = [&](const Item &it, int t, const uint8_t *sk) {
     const int64_t t0 = it.cs + (int64_t)t * kTile;
     const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
-    const uint8_t *sk = st, *sv = st + kTile * pitch;
     float s[G];
     qk_tile<KVT, G, D>(ws, sk, pitch, g, lane, a.scale_log2, n, s);
     bool valid = lane < n;
@@ -603,6 +602,10 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       pbuf[lane * GP + h] = pk2(p, p);
     }
     __syncwarp();
+  };
+  auto compute_pv = [&](const Item &it, int t, const uint8_t *sv) {
+    const int64_t t0 = it.cs + (int64_t)t * kTile;
+    const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
     for (int c = 0; c < n; ++c) {
       uint64_t vp[S::DV / 2];
       v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
@@ -620,6 +623,10 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = ffma2(pp[h], vp[i], ws.acc[h][i]);
     }
     __syncwarp();                            // pbuf reads done before the next tile's writes
+  };
+  auto compute_tile = [&](const Item &it, int t, const uint8_t *st) {
+    compute_qk(it, t, st);
+    compute_pv(it, t, st + kTile * pitch);
   };
 
   // Partial of an item: acc (this lane's dims), m, l.

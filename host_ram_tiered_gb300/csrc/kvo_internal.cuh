@@ -125,11 +125,12 @@ int launch_decode_staged(DecodeArgs a, const void *k_host, const void *v_host, i
 int launch_sparse_rows(const DecodeArgs &a, cudaStream_t st);   // kvo_status
 // Copy pages block_table[p0 .. p0 + n) of the K and V planes (page_bytes each)
 // to arena slots 0 .. n-1; entries outside [0, n_pages_total) are skipped and
-// set kErrPageTable.  At most max_ctas CTAs (0: four per SM).
+// set kErrPageTable.  beside: the copy runs beside a split kernel that
+// leaves it a few SMs (one wide CTA per SM); else up to four CTAs per SM.
 cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t page_bytes,
                                const int32_t *block_table, int64_t p0, int64_t n,
                                int64_t n_pages_total, void *k_arena, void *v_arena, uint32_t *err,
-                               int max_ctas, cudaStream_t st);
+                               bool beside, cudaStream_t st);
 
 struct PrefillArgs {
   const uint16_t *q;           // [rows][Hq][D] (rows of this launch start at q)

@@ -24,17 +24,21 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 // Staged with two arena slots: the split kernel leaves this many SMs to the
-// next bucket's page gather, which runs beside it on the library stream (a
-// split CTA holds a whole SM's registers, so a gather CTA could not start on
-// an SM it occupies).
+// next bucket's page gather, which runs beside it on the library stream.  A
+// split CTA holds a whole SM, so the gather then runs as kGatherSms CTAs of
+// kGatherWideThreads threads that each reserve more than half an SM's shared
+// memory: one per SM, so whichever kernel starts first, the gather never
+// holds more than kGatherSms SMs and the split kernel always finds its own.
 constexpr int kGatherSms = 16;
+constexpr int kGatherWideThreads = 1024;
+constexpr int kGatherWideSmem = 120 * 1024;
 constexpr size_t kPartitionSmem = 200 * 1024;   // bucket counters per CTA
 
 // Pages block_table[p0 .. p0 + n) of K and V -> arena slots 0 .. n-1.  Work
 // item = (tensor, page, slice): each page is cut into `parts` slices so that
 // enough CTAs (and 16-byte loads, 4 per thread) are in flight to fill the
 // host link; a CTA loops over items with stride gridDim.x.
-__global__ void __launch_bounds__(kGatherThreads)
+__global__ void __launch_bounds__(1024)
 page_gather_kernel(const uint8_t *kp, const uint8_t *vp, int64_t page_bytes, const int32_t *bt, int64_t p0,
                    int64_t n, int64_t n_pages_total, uint8_t *ka, uint8_t *va, uint32_t *err, int parts) {
   const int64_t cpp = page_bytes >> 4;
@@ -52,16 +56,17 @@ page_gather_kernel(const uint8_t *kp, const uint8_t *vp, int64_t page_bytes, con
     const int4 *src = (const int4 *)((is_v ? vp : kp) + page * page_bytes);
     int4 *dst = (int4 *)((is_v ? va : ka) + i * page_bytes);
     constexpr int U = 4;
-    for (int64_t c0 = c_lo + threadIdx.x; c0 < c_hi; c0 += (int64_t)U * kGatherThreads) {
+    const int64_t nt = blockDim.x;
+    for (int64_t c0 = c_lo + threadIdx.x; c0 < c_hi; c0 += U * nt) {
       int4 v[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + (int64_t)u * kGatherThreads;
+        const int64_t c = c0 + u * nt;
         if (c < c_hi) v[u] = src[c];
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t c = c0 + (int64_t)u * kGatherThreads;
+        const int64_t c = c0 + u * nt;
         if (c < c_hi) dst[c] = v[u];
       }
     }
@@ -181,9 +186,16 @@ SparseWs sparse_workspace(int64_t rows, int64_t n_q_heads, int64_t head_dim, int
 
 cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t page_bytes,
                                const int32_t *block_table, int64_t p0, int64_t n, int64_t n_pages_total,
-                               void *k_arena, void *v_arena, uint32_t *err, int max_ctas, cudaStream_t st) {
+                               void *k_arena, void *v_arena, uint32_t *err, bool beside, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  const int64_t cap = max_ctas > 0 ? max_ctas : (int64_t)num_sms() * 4;
+  const int64_t cap = beside ? kGatherSms : (int64_t)num_sms() * 4;
+  const int threads = beside ? kGatherWideThreads : kGatherThreads;
+  const int smem = beside ? kGatherWideSmem : 0;
+  if (beside) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(page_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherWideSmem);
+    if (e != cudaSuccess) return e;
+  }
   // slices per page: enough items for every CTA, each slice at least 16 KiB
   int64_t parts = (cap + 2 * n - 1) / (2 * n);
   const int64_t max_parts = (page_bytes >> 4) / 1024 > 0 ? (page_bytes >> 4) / 1024 : 1;
@@ -191,7 +203,7 @@ cudaError_t launch_page_gather(const void *k_pages, const void *v_pages, int64_t
   if (parts < 1) parts = 1;
   int64_t grid = 2 * n * parts;
   if (grid > cap) grid = cap;
-  page_gather_kernel<<<(unsigned)grid, kGatherThreads, 0, st>>>(
+  page_gather_kernel<<<(unsigned)grid, threads, smem, st>>>(
       (const uint8_t *)k_pages, (const uint8_t *)v_pages, page_bytes, block_table, p0, n, n_pages_total,
       (uint8_t *)k_arena, (uint8_t *)v_arena, err, (int)parts);
   return cudaGetLastError();
@@ -354,7 +366,7 @@ extern "C" int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows, in
       }
       const cudaError_t e = launch_page_gather(k_pages, v_pages, page_bytes, block_table, p0, np, n_pages,
                                                (void *)base.k_lo, (void *)base.v_lo, err,
-                                               rg ? 8 * kGatherSms : 0, gs);
+                                               rg != nullptr, gs);
       if (e != cudaSuccess) return cuda_status(e, "page gather launch");
       if (rg) {
         int e2 = cuda_status(cudaEventRecord(rg->ready[slot], gs), "cudaEventRecord");
