@@ -442,6 +442,16 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   // that every cell's entries start on a 16-byte boundary
   constexpr int GP = (G + 1) & ~1;
   uint64_t *pbuf = (uint64_t *)(smem + n_stages * stage_bytes) + (size_t)w_id * kTile * GP;
+  // Rows prefetched into shared memory (selection mode, staged, one stage,
+  // one chunk per row): two slots, each a row's query [Hq][D] and running
+  // state; slot n % 2 holds the n-th row this CTA works on, tagged with it.
+  const bool pre = SP && a.pre_rows && n_stages == 1;
+  const int64_t q_bytes = (int64_t)a.n_q_heads * D * 2;
+  const int64_t rs_bytes = (int64_t)a.n_q_heads * (D + 2) * 4;
+  uint8_t *pre_base = smem + n_stages * stage_bytes + (size_t)(blockDim.x >> 5) * kTile * GP * sizeof(uint64_t);
+  int pre_tag[2] = {-1, -1};
+  const float *pre_rs = nullptr;             // running state of the current row in shared memory
+  const uint16_t *pre_q = nullptr;           // query of the current row in shared memory
   const int qq = lane / S::CPP;
   const int64_t n_items = (int64_t)a.batch * a.n_splits;
   const FastDiv cpr = make_fastdiv((uint32_t)(a.row_bytes >> 4));   // 16-byte chunks per row
@@ -485,12 +495,16 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   //   m' = max(m, m_b); alpha = 2^(m - m') (0 if m = -inf); beta = 2^(m_b - m') (0 if m_b = -inf)
   //   acc = alpha acc + beta acc_b; l = alpha l + beta l_b
   // This warp alone owns the (row, head) pairs it folds.
-  auto fold = [&](const Item &it, int h, float m_b, float l_b, const float *acc_b) {
+  // rs: a shared-memory copy of the row's running state ([Hq][D] acc, then
+  // [Hq][2] (m, l)), or null to read it from global memory.
+  auto fold = [&](const Item &it, int h, float m_b, float l_b, const float *acc_b, const float *rs) {
     const size_t oi = (size_t)it.b * a.n_q_heads + h0 + h;
+    const float *ra_in = rs ? rs + (size_t)(h0 + h) * D + lane * S::DV : a.run_acc + oi * D + lane * S::DV;
+    const float *ml_in = rs ? rs + (size_t)a.n_q_heads * D + (size_t)(h0 + h) * 2 : a.run_ml + oi * 2;
     float m_run = -INFINITY, l_run = 0.f;
     if (!a.init) {
-      m_run = a.run_ml[oi * 2];
-      l_run = a.run_ml[oi * 2 + 1];
+      m_run = ml_in[0];
+      l_run = ml_in[1];
     }
     const float m_new = fmaxf(m_run, m_b);
     const float alpha = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
@@ -500,7 +514,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     float *o = a.out + oi * D + lane * S::DV;
 #pragma unroll
     for (int i = 0; i < S::DV; ++i) {
-      const float acc_new = alpha * (a.init ? 0.f : ra[i]) + beta * acc_b[i];
+      const float acc_new = alpha * (a.init ? 0.f : ra_in[i]) + beta * acc_b[i];
       if (a.finalize) o[i] = acc_new / fmaxf(l_new, 1e-30f);
       else ra[i] = acc_new;
     }
@@ -518,7 +532,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
 #pragma unroll
     for (int i = 0; i < S::DV; ++i) z[i] = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) fold(it, h, -INFINITY, 0.f, z);
+    for (int h = 0; h < G; ++h) fold(it, h, -INFINITY, 0.f, z, nullptr);
   };
 
   // First non-empty item at or after w (stride gridDim.x); fold_empties: the
@@ -551,7 +565,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
   WarpState<KVT, G, D> ws;
   auto init_item = [&](const Item &it) {
     // query slice of each of the warp's heads: dims [qq*DL, qq*DL + DL)
-    const uint16_t *qsrc = (const uint16_t *)a.q + ((size_t)it.b * a.n_q_heads + (size_t)h0) * D;
+    const uint16_t *qsrc = (pre_q ? pre_q : (const uint16_t *)a.q + (size_t)it.b * a.n_q_heads * D) + (size_t)h0 * D;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
@@ -638,7 +652,7 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         float x[S::DV];
 #pragma unroll
         for (int i = 0; i < S::DV / 2; ++i) upk2(ws.acc[h][i], x[2 * i], x[2 * i + 1]);
-        fold(it, h, ws.m[h], lsum, x);
+        fold(it, h, ws.m[h], lsum, x, pre_rs);
         continue;
       }
       const int qh = h0 + h;
@@ -679,6 +693,40 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       }
     };
     int32_t fj = picks(fi, ft);
+    // Prefetch of row n (the raw item w, which holds row w % batch) into
+    // slot n % 2, committed with the next tile copy.
+    int64_t n_pre = 0, n_cur = 0;
+    auto prefetch_row = [&](int64_t w) {
+      const int slot = (int)(n_pre++ & 1);
+      if (w >= w_end) return;
+      const int b = (int)(w % a.batch);
+      uint8_t *dq = pre_base + slot * (q_bytes + rs_bytes);
+      const uint8_t *sq = (const uint8_t *)a.q + (size_t)b * q_bytes;
+      for (int64_t i = threadIdx.x; i < q_bytes / 16; i += blockDim.x)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dq + i * 16)), "l"(sq + i * 16)
+                     : "memory");
+      if (!a.init) {
+        uint8_t *dr = dq + q_bytes;
+        const uint8_t *sa = (const uint8_t *)(a.run_acc + (size_t)b * a.n_q_heads * D);
+        const uint8_t *sm = (const uint8_t *)(a.run_ml + (size_t)b * a.n_q_heads * 2);
+        const int64_t na = (int64_t)a.n_q_heads * D * 4 / 16, nm = (int64_t)a.n_q_heads * 8 / 16;
+        for (int64_t i = threadIdx.x; i < na + nm; i += blockDim.x) {
+          const uint8_t *src = i < na ? sa + i * 16 : sm + (i - na) * 16;
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dr + i * 16)), "l"(src)
+                       : "memory");
+        }
+      }
+      pre_tag[slot] = b;
+    };
+    // Row n_cur is the current item: use its slot when the prefetch was for it.
+    auto take_row = [&](const Item &it) {
+      const int slot = (int)(n_cur++ & 1);
+      const bool hit = pre && pre_tag[slot] == it.b;
+      uint8_t *base = pre_base + slot * (q_bytes + rs_bytes);
+      pre_q = hit ? (const uint16_t *)base : nullptr;
+      pre_rs = hit && !a.init ? (const float *)(base + q_bytes) : nullptr;
+    };
+    if (pre) prefetch_row(ci.w);
     for (int s = 0; s < n_stages - 1; ++s) {
       if (fi.w < w_end) {
         issue(fi, ft, smem + s * stage_bytes, fj);
@@ -687,16 +735,23 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     }
-    init_item(ci);
+    if (!pre) init_item(ci);
+    bool fresh = true;                       // the first tile of ci comes next
     for (int64_t k = 0;; ++k) {
       if (n_stages == 1) {
         __syncthreads();                     // tile k-1 fully consumed
+        if (pre && fresh) prefetch_row(ci.w + gridDim.x);   // its slot's last row is done
         issue(fi, ft, smem, fj);
         advance(fi, ft);
         fj = picks(fi, ft);
         asm volatile("cp.async.commit_group;" ::: "memory");
         asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();                     // tile k landed
+        __syncthreads();                     // tile k (and any prefetch) landed
+        if (pre && fresh) {
+          take_row(ci);
+          init_item(ci);
+        }
+        fresh = false;
       } else {
         if (n_stages == 3) asm volatile("cp.async.wait_group 1;" ::: "memory");
         else asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -714,7 +769,8 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
         ci = next_item(ci.w + gridDim.x, true);
         ct = 0;
         if (ci.w >= w_end) break;
-        init_item(ci);
+        if (pre) fresh = true;
+        else init_item(ci);
       } else {
         ++ct;
       }
@@ -942,10 +998,16 @@ inline size_t split_smem_bytes(const DecodeArgs &a, int g_per_warp, int n_stages
 }
 
 template <int KVT, int QT, int G, int D, bool SP>
-cudaError_t launch_d(const DecodeArgs &a, cudaStream_t st) {
+cudaError_t launch_d(const DecodeArgs &a0, cudaStream_t st) {
+  DecodeArgs a = a0;
   int n_stages = kMaxStages;
   while (n_stages > 1 && split_smem_bytes(a, G, n_stages) > (size_t)kSmemLimit) --n_stages;
-  const size_t smem = split_smem_bytes(a, G, n_stages);
+  size_t smem = split_smem_bytes(a, G, n_stages);
+  // one stage, one chunk per row: prefetch rows' query and running state
+  const size_t pre = 2 * ((size_t)a.n_q_heads * D * 2 + (size_t)a.n_q_heads * (D + 2) * 4);
+  a.pre_rows = SP && a.all_ring && a.fold_in_split && a.n_splits == 1 && n_stages == 1 &&
+               a.n_q_heads % 2 == 0 && smem + pre <= (size_t)kSmemLimit;
+  if (a.pre_rows) smem += pre;
   if (smem > (size_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   auto k = decode_split_kernel<KVT, QT, G, D, SP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -95,6 +95,7 @@ struct DecodeArgs {
   // Selection mode with one chunk per row and a running state: the split
   // kernel folds each row's chunk into run_acc / run_ml itself (no combine).
   int fold_in_split = 0;
+  int pre_rows = 0;             // set by the launcher: rows' query / running state prefetched
   uint32_t *err = nullptr;     // device error word (sparse: bad page-table entries)
 };
 // Split geometry for a decode: fixed cell ranges that depend on max_ctx and
