@@ -839,6 +839,9 @@ constexpr int kCombineWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 decode_combine_kernel(const DecodeArgs a) {
+  // Launched as a programmatic dependent of the split kernel: wait here until
+  // that grid has finished and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   constexpr int DPL = D / 32;
   __shared__ float red[kCombineWarps][D];
   __shared__ float red_l[kCombineWarps];
@@ -933,6 +936,7 @@ constexpr int kSmallCombineChunks = 4;
 template <int D>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 decode_combine_small_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // as in decode_combine_kernel
   constexpr int DPL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * kCombineWarps + warp;
@@ -1021,14 +1025,26 @@ cudaError_t launch_d(const DecodeArgs &a0, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (a.phase == 1) return cudaSuccess;
+  // The combine is a programmatic dependent launch: it is set up while the
+  // split kernel runs and starts as its CTAs exit, then waits on the device
+  // (griddepcontrol.wait) for the whole grid, which hides the launch gap.
+  // (A trigger at the split kernel's start slowed the multi-item decodes.)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (a.n_splits <= kSmallCombineChunks) {
     const int64_t items = (int64_t)a.batch * a.n_q_heads;
-    decode_combine_small_kernel<D><<<(unsigned)((items + kCombineWarps - 1) / kCombineWarps),
-                                     kCombineWarps * 32, 0, st>>>(a);
-  } else {
-    decode_combine_kernel<D><<<dim3(a.n_q_heads, a.batch), kCombineWarps * 32, 0, st>>>(a);
+    cfg.gridDim = dim3((unsigned)((items + kCombineWarps - 1) / kCombineWarps));
+    return cudaLaunchKernelEx(&cfg, decode_combine_small_kernel<D>, a);
   }
-  return cudaGetLastError();
+  cfg.gridDim = dim3(a.n_q_heads, a.batch);
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a);
 }
 
 template <int KVT, int QT, int G, bool SP>
