@@ -6,9 +6,10 @@
 // (-1 padded).  Direct mode: the decode split kernel in selection mode reads
 // every row's picks through the host mapping.  Staged mode: the page range is
 // walked in arena-sized buckets; a bucket's pages are gathered host -> arena
-// once, every row block is scored against it (picks outside the bucket are
-// padding), and the combine kernel folds the bucket's (m, l, acc) into a
-// running state, writing out = acc / max(l, 1e-30) after the last bucket.
+// once, every row block scores its picks in the bucket (grouped by bucket
+// once per call), and the bucket's (m, l, acc) is folded into a running state
+// -- in the split kernel's epilogue when each row has one chunk, else by the
+// combine kernel -- writing out = acc / max(l, 1e-30) after the last bucket.
 #include <cstring>
 #include <mutex>
 
