@@ -326,6 +326,52 @@ def dec_run(st, L, N, staging=False, all_vram=False, q=None, out=None):
                              out if out is not None else st["out"], st["ws"], ws_bytes)
 
 
+VMM_RAN = [False]
+
+
+def vmm_setup(st, L=184320, N=8192):
+    """The headline decode's K/V planes copied into two VMM tiers (a VRAM head of
+    N cells, then a host-NUMA tail in the same device range)."""
+    k = kvo()
+    t = torch()
+    rb = st["rb"]
+    try:
+        tk = k.kvo_vmm_tier_create(0, N * rb, (L - N) * rb)
+        tv = k.kvo_vmm_tier_create(0, N * rb, (L - N) * rb)
+    except k.KvoError as e:
+        return {"unavailable": str(e)}
+    chunk = 1 << 16
+    offs = np.arange(0, L * rb, chunk, dtype=np.int64)
+    sizes = t.from_numpy(np.minimum(chunk, L * rb - offs).astype(np.int64)).cuda()
+    for src, tier in ((st["k_dev_all"], tk), (st["v_dev_all"], tv)):
+        k.kvo_swap_blocks_batch(t.from_numpy(src.data_ptr() + offs).cuda(), t.from_numpy(tier["base"] + offs).cuda(),
+                                sizes, len(offs), k.KVO_SWAP_H2D | k.KVO_SWAP_FORCE_SM)
+    t.cuda.synchronize()
+    return {"tk": tk, "tv": tv, "L": L, "N": N}
+
+
+def vmm_run(st, vm, staging=False):
+    """Decode over the tiers through one base pointer per plane (staging: the
+    host tail copied to a VRAM buffer by the copy engine first)."""
+    k = kvo()
+    L, N = vm["L"], vm["N"]
+    k.kvo_attn_decode_tiered(st["q"], k.F16, 1, DEC_HQ, DEC_HKV, DEC_D, vm["tk"]["base"], vm["tv"]["base"], L,
+                             None, None, L, k.Q8_0, dec_ctx(st, L), L, N, 1.0 / math.sqrt(DEC_D),
+                             st["stage_k"] if staging else None, st["stage_v"] if staging else None,
+                             st["out"], st["ws"], k.kvo_attn_decode_workspace_bytes(1, DEC_HQ, DEC_D, L))
+
+
+def k_launches_staged_headline():
+    return kvo().kvo_attn_decode_launches(1, 184320, DEC_D, 8192, 1)
+
+
+def vmm_free(vm):
+    k = kvo()
+    for key in ("tk", "tv"):
+        if key in vm:
+            k.kvo_vmm_tier_destroy(vm[key]["tier"])
+
+
 def dec_bytes(L, N):
     rb2 = 2 * DEC_HKV * (DEC_D // 32) * 34
     return max(L - N, 0) * rb2, min(L, N) * rb2
@@ -592,9 +638,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of head (headline decode only), tiny, swap, decode, topk, prefill, "
-                         "append, sparse (QSA sparse rows), decode_vram (the 184,320-cell all-VRAM decode alone; not in "
-                         "'all') (default: all rows at one GPU, the headline alone under torchrun)")
+                    help="comma list of head (headline decode only), tiny, swap, decode, vmm (the headline decode "
+                         "over VMM tiers), topk, prefill, append, sparse (QSA sparse rows), decode_vram (the 184,320-"
+                         "cell all-VRAM decode alone; not in 'all') (default: all rows at one GPU, the headline alone "
+                         "under torchrun)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
@@ -620,7 +667,7 @@ def main(argv=None):
     if args.rows == "all" and world > 1:
         rows = {"head"}
     elif args.rows == "all":
-        rows = {"head", "tiny", "swap", "decode", "topk", "prefill", "append", "sparse"}
+        rows = {"head", "tiny", "swap", "decode", "vmm", "topk", "prefill", "append", "sparse"}
     else:
         rows = set(args.rows.split(","))
     timer = Timer()
@@ -639,7 +686,7 @@ def main(argv=None):
     clocks = Clocks()
     # ---- headline: q8_0 tiered decode at L = 184,320, N = 8,192, direct
     head = None
-    if "decode" in rows or "head" in rows:
+    if "decode" in rows or "head" in rows or "vmm" in rows:
         st3 = dec_setup()
         bar()
         tot, ms = timer.run(lambda: dec_run(st3, 184320, 8192), K, W)
@@ -685,6 +732,26 @@ def main(argv=None):
                 results[f"q8_0_decode_L{L}_all_vram"] = {
                     "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
                     "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
+        if "vmm" in rows:
+            # the headline decode over one VMM range per plane (host-NUMA tail)
+            vm = vmm_setup(st3)
+            if "unavailable" in vm:
+                results["q8_0_decode_L184320_N8192_vmm_tier"] = {"unavailable": vm["unavailable"]}
+            else:
+                try:
+                    for staging in (False, True):
+                        tot, _ = timer.run(lambda: vmm_run(st3, vm, staging), K, W)
+                        VMM_RAN[0] = True
+                        us_r = max_over_ranks(tot, world) / K * 1e3
+                        hb_r, db_r = dec_bytes(184320, 8192)
+                        if staging:
+                            db_r += 2 * hb_r
+                        t_star = max(hb_r / (peaks['h2d'] * 1e9), db_r / (hbm * 1e9))
+                        results[f"q8_0_decode_L184320_N8192_vmm_tier_{'staged' if staging else 'direct'}"] = {
+                            "us_per_step": us_r, "host_gbs": hb_r / (us_r * 1e-6) / 1e9,
+                            "roofline_frac": t_star / (us_r * 1e-6)}
+                finally:
+                    vmm_free(vm)
         del st3
     if "decode_vram" in rows and "decode" not in rows:
         st3 = dec_setup()
@@ -852,8 +919,11 @@ def profiled_traffic():
 def gpu_launch_count(K, rows):
     """Kernels of libkvo launched in the timed regions (own kernels only)."""
     n = 0
-    if "decode" in rows or "head" in rows:
+    if "decode" in rows or "head" in rows or "vmm" in rows:
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
+    if "vmm" in rows and VMM_RAN[0]:
+        # the headline decode over VMM tiers, direct and staged
+        n += 2 * K + K * k_launches_staged_headline()
     k = kvo()
     if "decode" in rows:
         # 11 tiered variants (a staged call runs the split kernel once per copy part) + 3

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(PKG, "libkvo.so")
 
 SOURCES = ["kvo_abi.cu", "swap_gather.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu",
            "decode_q8_0.cu", "prefill_mma.cu", "prefill_tc.cu",
-           "decode_noalloc.cu", "append.cu", "sparse_rows.cu"]
+           "decode_noalloc.cu", "append.cu", "sparse_rows.cu", "vmm.cu"]
 HEADERS = [os.path.join(CSRC, "kvo_internal.cuh"), os.path.join(CSRC, "decode_impl.cuh"), os.path.join(ROOT, "include", "kvo.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

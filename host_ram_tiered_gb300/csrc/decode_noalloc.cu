@@ -88,6 +88,12 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
 
   const int64_t n_lo = n_vram_cells < max_ctx ? n_vram_cells : max_ctx;
   const int64_t n_hi = max_ctx - n_lo;
+  if (n_hi > 0 && !k_host && !v_host && k_vram && v_vram) {
+    // one range (a VMM tier): the tail continues right after the VRAM cells
+    k_host = (const uint8_t *)k_vram + (size_t)n_lo * rb;
+    v_host = (const uint8_t *)v_vram + (size_t)n_lo * rb;
+    host_seq_stride_rows = vram_seq_stride_rows;
+  }
   if (n_lo > 0) {
     if (vram_seq_stride_rows < n_lo) return fail(KVO_ERR_ARG, "%s: vram stride < cells", fn);
     const size_t bytes = (size_t)((batch - 1) * vram_seq_stride_rows + n_lo) * rb;
@@ -121,7 +127,8 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
   a.lo_seq_stride_rows = vram_seq_stride_rows;
   a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host;
   a.hi_seq_stride_rows = host_seq_stride_rows;
-  a.hi_device = (n_hi > 0 && classify(k_host, 1) == kDeviceMem && classify(v_host, 1) == kDeviceMem) ? 1 : 0;
+  const size_t hi_bytes = n_hi > 0 ? (size_t)((batch - 1) * host_seq_stride_rows + n_hi) * rb : 0;
+  a.hi_device = (n_hi > 0 && classify(k_host, hi_bytes) == kDeviceMem && classify(v_host, hi_bytes) == kDeviceMem) ? 1 : 0;
   a.kv_dtype = kv_dtype; a.row_bytes = rb;
   a.ctx_len = ctx_len; a.max_ctx = max_ctx; a.n_vram = n_lo;
   a.scale_log2 = scale * 1.4426950408889634f;

@@ -28,6 +28,9 @@ int cuda_status(cudaError_t e, const char *what) {
 }
 
 static int classify_one(const void *p, cudaPointerAttributes *a) {
+  const int vm = vmm_host_backed(p);         // a tier's ranges: known without asking
+  if (vm == 1) return kMappedHost;
+  if (vm == 0) return kDeviceMem;
   if (cudaPointerGetAttributes(a, p) != cudaSuccess) {
     cudaGetLastError();  // clear the sticky-free error of an unknown pointer
     return 0;
@@ -44,7 +47,10 @@ int classify(const void *p, size_t bytes) {
   if (!k || bytes <= 1) return k;
   const char *last = (const char *)p + (bytes - 1);
   int k2 = classify_one(last, &b);
-  return k2 == k ? k : 0;
+  if (!k2) return 0;
+  // both ends device-accessible but of different kinds (a VMM tier's VRAM head
+  // running into its host tail): device-accessible, not all device memory
+  return k2 == k ? k : kMappedHost;
 }
 
 Ring *ring(int which) {
@@ -351,6 +357,12 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
   if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "kvo_attn_decode_tiered: q/out alignment");
   const int64_t n_lo = n_vram_cells < max_ctx ? n_vram_cells : max_ctx;   // rows read from VRAM
   const int64_t n_hi = max_ctx - n_lo;                                     // rows past N
+  if (n_hi > 0 && !k_host && !v_host && k_vram && v_vram) {
+    // one range (a VMM tier): the tail continues right after the VRAM cells
+    k_host = (const uint8_t *)k_vram + (size_t)n_lo * rb;
+    v_host = (const uint8_t *)v_vram + (size_t)n_lo * rb;
+    host_seq_stride_rows = vram_seq_stride_rows;
+  }
   if (n_lo > 0) {
     if (vram_seq_stride_rows < n_lo) return fail(KVO_ERR_ARG, "kvo_attn_decode_tiered: vram stride < cells");
     const size_t bytes = (size_t)((batch - 1) * vram_seq_stride_rows + n_lo) * rb;
@@ -385,7 +397,8 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch, int64_t n_
   a.lo_seq_stride_rows = vram_seq_stride_rows;
   a.k_hi = (const uint8_t *)k_host; a.v_hi = (const uint8_t *)v_host;
   a.hi_seq_stride_rows = host_seq_stride_rows;
-  a.hi_device = (n_hi > 0 && classify(k_host, 1) == kDeviceMem && classify(v_host, 1) == kDeviceMem) ? 1 : 0;
+  const size_t hi_bytes = n_hi > 0 ? (size_t)((batch - 1) * host_seq_stride_rows + n_hi) * rb : 0;
+  a.hi_device = (n_hi > 0 && classify(k_host, hi_bytes) == kDeviceMem && classify(v_host, hi_bytes) == kDeviceMem) ? 1 : 0;
   a.kv_dtype = kv_dtype; a.row_bytes = rb;
   a.ctx_len = ctx_len; a.max_ctx = max_ctx; a.n_vram = n_lo;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -489,6 +502,11 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
   const int64_t c_end = ctx_len < q_pos0 + rows ? ctx_len : q_pos0 + rows;
   const int64_t n_lo = n_vram_cells < c_end ? n_vram_cells : c_end;
   const int64_t n_hi = c_end - n_lo;
+  if (n_hi > 0 && !k_host && !v_host && k_vram && v_vram) {
+    // one range (a VMM tier): the tail continues right after the VRAM cells
+    k_host = (const uint8_t *)k_vram + (size_t)n_vram_cells * rb;
+    v_host = (const uint8_t *)v_vram + (size_t)n_vram_cells * rb;
+  }
   if (n_lo > 0) {
     if (!aligned16(k_vram) || !aligned16(v_vram)) return fail(KVO_ERR_ALIGN, "kvo_attn_prefill_tiered: vram alignment");
     if (classify(k_vram, (size_t)n_lo * rb) != kDeviceMem || classify(v_vram, (size_t)n_lo * rb) != kDeviceMem)

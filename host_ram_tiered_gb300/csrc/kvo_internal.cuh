@@ -21,6 +21,9 @@ enum Access { kDeviceMem = 1, kMappedHost = 2 };
 // device-accessible: unregistered pageable memory, NULL, or a range that ends
 // outside the allocation that holds its first byte).
 int classify(const void *p, size_t bytes);
+// 1: p lies in the host-backed tail of a live VMM tier; 0: in a tier's VRAM
+// range; -1: in no tier.
+int vmm_host_backed(const void *p);
 
 int num_sms();                       // SMs of the current device (cached)
 

@@ -42,6 +42,9 @@ SIGNATURES = {
                                  _vp, _vp]),
     "kvo_attn_decode_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "kvo_attn_decode_launches": (_int, [_i64, _i64, _i64, _i64, _int]),
+    "kvo_vmm_granularity": (_int, [_int, _vp]),
+    "kvo_vmm_tier_create": (_int, [_int, _sz, _sz, _sz, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "kvo_vmm_tier_destroy": (_int, [_vp]),
     "kvo_attn_decode_tiered": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _i64, _vp, _vp,
                                       _i64, _int, _vp, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz,
                                       _vp]),
@@ -172,6 +175,30 @@ def kvo_attn_decode_workspace_bytes(batch, n_q_heads, head_dim, max_ctx) -> int:
 
 def kvo_attn_decode_launches(batch, max_ctx, head_dim, n_vram_cells, staged) -> int:
     return load().kvo_attn_decode_launches(batch, max_ctx, head_dim, n_vram_cells, int(bool(staged)))
+
+
+def kvo_vmm_granularity(device) -> int:
+    """Granularity of a VMM tier's ranges; raises KvoError when VMM is unavailable."""
+    out = ctypes.c_size_t(0)
+    _check(load().kvo_vmm_granularity(device, ctypes.byref(out)), "kvo_vmm_granularity")
+    return out.value
+
+
+def kvo_vmm_tier_create(device, head_bytes, tail_bytes, stage_bytes=0):
+    """One VA range (VRAM head + host tail) and, with stage_bytes > 0, the
+    all-VRAM alias. Returns a dict: base, alias, head, tail, stage (mapped
+    sizes) and tier (the handle for kvo_vmm_tier_destroy)."""
+    base, alias, tier = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
+    hm, tm, sm = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().kvo_vmm_tier_create(device, head_bytes, tail_bytes, stage_bytes, ctypes.byref(base),
+                                      ctypes.byref(alias), ctypes.byref(hm), ctypes.byref(tm), ctypes.byref(sm),
+                                      ctypes.byref(tier)), "kvo_vmm_tier_create")
+    return {"base": base.value, "alias": alias.value, "head": hm.value, "tail": tm.value, "stage": sm.value,
+            "tier": tier.value}
+
+
+def kvo_vmm_tier_destroy(tier) -> None:
+    _check(load().kvo_vmm_tier_destroy(tier), "kvo_vmm_tier_destroy")
 
 
 def kvo_attn_decode_tiered(q, q_dtype, batch, n_q_heads, n_kv_heads, head_dim, k_vram, v_vram,

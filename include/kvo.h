@@ -217,6 +217,14 @@ int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
  *     j <  N: k_vram + (b * vram_seq_stride_rows + j)     * row_bytes
  *     j >= N: k_host + (b * host_seq_stride_rows + j - N) * row_bytes
  * (the same for V).  k_vram/v_vram may be NULL when N == 0.
+ * k_host == v_host == NULL with N > 0: one range per plane, as a VMM tier
+ *   (kvo_vmm_tier_create) holds it -- the tail continues right after the
+ *   VRAM cells: k_host = k_vram + N * row_bytes, host_seq_stride_rows =
+ *   vram_seq_stride_rows.
+ * Memory kinds are taken per range: a range that is device memory
+ *   throughout is read with cp.async; anything else (pinned host memory, the
+ *   host tail of a VMM tier, a range crossing from a tier's VRAM head into its
+ *   tail) with plain 16-byte loads.
  * q: device [batch][n_q_heads][head_dim] of q_dtype: the cache's 16-bit
  *   type for an F16 or BF16 cache, F16 for a Q8_0 cache (other pairs return
  *   KVO_ERR_UNSUPPORTED).
@@ -304,6 +312,49 @@ int kvo_attn_decode_tiered_noalloc(const void *q, int q_dtype, int64_t batch,
                                    int64_t n_vram_cells, float scale,
                                    void *staging_k, void *staging_v,
                                    float *out, void *stream);
+
+/* ------------------------------------------------------------------------
+ * kvo_vmm_tier_create -- one device virtual range holding a VRAM head of
+ * head_bytes, then a host-memory tail of tail_bytes, and optionally a second
+ * range (the all-VRAM alias) that maps the same head pages followed by a
+ * VRAM staging buffer of stage_bytes.
+ *
+ * llama.cpp PR #319 "tiered KV cache (--kv-vram-cells): VRAM head,
+ * pinned-host tail in one VMM range", the tier buffer and its review: the
+ * tail is cuMemCreate memory on the host NUMA node the device reports
+ * (CU_DEVICE_ATTRIBUTE_HOST_NUMA_ID; node 0 where the host has no NUMA),
+ * mapped after the head with device read/write access.  A KV plane of L
+ * cells of row_bytes keeps cells [0, N) in VRAM and [N, L) in host memory
+ * when head_bytes = N * row_bytes; the decode and prefill entry points then
+ * take k_vram = base and k_host = NULL (one base pointer).  Staging through
+ * the alias: staging_k = alias + N * row_bytes holds cells [N, ...) so that
+ * the alias reads as an all-VRAM plane; this needs N * row_bytes ==
+ * head_mapped.
+ *
+ * Each size is rounded up to kvo_vmm_granularity(device) and returned in
+ * *head_mapped, *tail_mapped, *stage_mapped (any may be NULL).  *base and
+ * *alias (NULL when stage_bytes == 0) are device addresses, *tier the handle
+ * for kvo_vmm_tier_destroy.  The host tail is reachable from the device
+ * only: fill it with copies (cudaMemcpy, kvo_swap_blocks_batch, the append
+ * path).  The library knows every live tier's ranges and reads the host part
+ * with plain loads only (never cp.async or TMA).  The caller's current
+ * device is left as it was.
+ * Errors: KVO_ERR_ARG (NULL base/tier, an empty head or tail, stage_bytes
+ *   without alias, no such device), KVO_ERR_UNSUPPORTED (the driver lacks
+ *   the virtual-memory calls, or refuses them), KVO_ERR_CUDA (allocation or
+ *   mapping failed; nothing is left allocated).  Callers that want the
+ *   page's fallback allocate plain device memory on an error.
+ * ---------------------------------------------------------------------- */
+int kvo_vmm_granularity(int device, size_t *bytes);
+
+int kvo_vmm_tier_create(int device, size_t head_bytes, size_t tail_bytes,
+                        size_t stage_bytes, void **base, void **alias,
+                        size_t *head_mapped, size_t *tail_mapped,
+                        size_t *stage_mapped, void **tier);
+
+/* kvo_vmm_tier_destroy -- waits for the tier's device to go idle, then
+ * unmaps and frees every range of the tier.  NULL is a no-op. */
+int kvo_vmm_tier_destroy(void *tier);
 
 /* ------------------------------------------------------------------------
  * kvo_staging_worthwhile -- the staged/direct rule of the sparse rows.
@@ -442,6 +493,8 @@ int kvo_append_kv_tiered(const void *k_new, const void *v_new, int src_dtype,
  *     g = h / (n_q_heads / n_kv_heads).
  * Cells [0, N) are read from k_vram/v_vram, cells [N, ctx_len) from
  * k_host/v_host (row j - N), rows of n_kv_heads * head_dim values.
+ * k_host == v_host == NULL: one range per plane (a VMM tier), the tail at
+ * k_vram + N * row_bytes.
  *
  * Staged mode (arena != NULL; ExLlamaV3 qsa-kv-offload patch,
  * qsa_sparse_attend_rows_staged): the host tail is walked in buckets.  The

@@ -98,6 +98,19 @@ def test_workspace_sizes_are_deterministic(kvo_lib):
     assert kvo.kvo_attn_prefill_workspace_bytes(-1, 32) == 0
 
 
+def test_vmm_tier_host_side_checks_need_no_gpu(kvo_lib):
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_vmm_tier_create(0, 0, 4096)                # empty head
+    assert e.value.status == -1
+    with pytest.raises(kvo.KvoError) as e:
+        kvo.kvo_vmm_tier_create(0, 4096, 0)                # empty tail
+    assert e.value.status == -1
+    kvo.kvo_vmm_tier_destroy(None)                         # no-op
+    with pytest.raises(kvo.KvoError) as e:                 # no GPU here: no device, or no driver
+        kvo.kvo_vmm_granularity(0)
+    assert e.value.status in (-1, -4)
+
+
 def test_decode_launch_counts(kvo_lib):
     # direct: split + combine; nothing for an empty batch; an error for a negative size
     assert kvo.kvo_attn_decode_launches(1, 184320, 128, 8192, 0) == 2
