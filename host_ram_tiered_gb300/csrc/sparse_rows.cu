@@ -437,8 +437,13 @@ extern "C" int kvo_copy_pages_host(const void *src_k, const void *src_v, void *d
   const size_t off_dst = (size_t)to_page * page_tokens * token_bytes;
   const size_t bytes = (size_t)num_tokens * token_bytes;
   const void *ptrs[4] = {src_k, src_v, dst_k, dst_v};
-  for (const void *p : ptrs)
+  for (const void *p : ptrs) {
     if (classify(p, 1) == kDeviceMem) return fail(KVO_ERR_NOT_MAPPED, "%s: planes must be host memory", fn);
+    // a VMM tier's tail is host memory mapped for the device only: the CPU
+    // has no mapping of it
+    if (vmm_host_backed(p) >= 0)
+      return fail(KVO_ERR_NOT_MAPPED, "%s: VMM tier memory is not host-addressable", fn);
+  }
   const cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "cudaStreamSynchronize");
   if (bytes == 0) return KVO_OK;

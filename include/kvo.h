@@ -443,7 +443,8 @@ int kvo_attn_sparse_rows(const void *q, int q_dtype, int64_t rows,
  * bytes) for K (src_k -> dst_k) and V (src_v -> dst_v); overlapping ranges
  * are allowed.  Synchronous; the planes must be host memory (pinned or not).
  * Errors: KVO_ERR_ARG (num_tokens > page_tokens, negative sizes, NULL),
- *   KVO_ERR_NOT_MAPPED (a device pointer), KVO_ERR_CUDA (the drain).
+ *   KVO_ERR_NOT_MAPPED (a device pointer, or a plane inside a VMM tier,
+ *   which the CPU cannot address), KVO_ERR_CUDA (the drain).
  * ---------------------------------------------------------------------- */
 int kvo_copy_pages_host(const void *src_k, const void *src_v, void *dst_k,
                         void *dst_v, int64_t page_tokens, int64_t token_bytes,

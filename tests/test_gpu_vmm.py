@@ -116,6 +116,11 @@ def test_q8_0_tier_boundary_inside_a_granule():
         with pytest.raises(kvo.KvoError) as e:
             _decode(q, hq, hkv, d, kvo.Q8_0, tk["base"], tv["base"], None, None, L, n_bad, s)
         assert e.value.status == -3                        # KVO_ERR_NOT_MAPPED
+        # the CPU page copy cannot address a tier: refused before any access
+        with pytest.raises(kvo.KvoError) as e:
+            kvo.kvo_copy_pages_host(tk["base"] + tk["head"], tv["base"] + tv["head"], tk["base"] + tk["head"],
+                                    tv["base"] + tv["head"], 16, rb, 0, 1, 16)
+        assert e.value.status == -3
         # staging buffers in the host tail: refused (they must be device memory)
         with pytest.raises(kvo.KvoError) as e:
             _decode(q, hq, hkv, d, kvo.Q8_0, tk["base"], tv["base"], None, None, L, N, s,
