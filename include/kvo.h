@@ -3,11 +3,15 @@
  * that lives partly in VRAM and partly in pinned, device-mapped host memory.
  *
  * Conventions shared by every entry point:
- *   - The caller owns every buffer.  The library allocates no memory.
+ *   - The caller owns every buffer.  The library allocates no memory of its
+ *     own accord: only the VMM tiers kvo_vmm_tier_create makes on request
+ *     (freed by kvo_vmm_tier_destroy), and the fixed device scratch array of
+ *     kvo_attn_decode_tiered_noalloc.
  *   - "device-accessible" means device memory (cudaMalloc / a framework's
- *     allocator) or pinned host memory that is mapped into the device's
+ *     allocator), pinned host memory that is mapped into the device's
  *     address space (cudaHostAlloc(..., Mapped) / cudaHostRegister(...,
- *     Mapped)); both are passed by the same unified virtual address.
+ *     Mapped)), or a range of a VMM tier; all are passed by the same unified
+ *     virtual address.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  All calls except kvo_sub_block_ptrs are stream-ordered and
  *     asynchronous: they return once the work is enqueued, do no host
