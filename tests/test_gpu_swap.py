@@ -257,5 +257,12 @@ def test_canonical_fragment_swap(gpu_to_cpu):
     msb, mdb = (mb_dev, mb_host) if gpu_to_cpu else (mb_host, mb_dev)
     rs, rd, rz = oracle.fragment_ptrs(msb, mdb, es, ed, ez)
     oracle.swap_blocks(rs, rd, rz)
-    assert np.array_equal(host.numpy(), host_mirror)
-    assert np.array_equal(dev.cpu().numpy(), dev_mirror)
+    got_host, got_dev = host.numpy(), dev.cpu().numpy()
+    assert np.array_equal(got_host, host_mirror)
+    assert np.array_equal(got_dev, dev_mirror)
+    # the meaning, independent of the plan: a canonical host block is its device block with
+    # the token and head axes exchanged ([16][8][256 B] token-major <-> [8][16][256 B] head-major)
+    for di, hi in zip(dev_ids, host_ids):
+        d_blk = got_dev[di * page:(di + 1) * page].reshape(16, 8, 256)
+        h_blk = got_host[hi * page:(hi + 1) * page].reshape(8, 16, 256)
+        assert np.array_equal(h_blk, d_blk.transpose(1, 0, 2))

@@ -444,35 +444,83 @@ def test_append_places_cells_in_their_tiers():
 
 # ---------------------------------------------------------------- canonical fragments
 
-def _brute_plan(runs, gpu_to_cpu):
-    out = []
-    for lo, ls, co, cs, nf, fz in runs:
-        for i in range(nf):
-            local, canon = lo + i * ls, co + i * cs
-            out.append((local, canon, fz) if gpu_to_cpu else (canon, local, fz))
-    return out
+# vLLM gpu_worker.py, _build_copy_plan and _fill_canonical_ops: the expected lists
+# below are written out by hand from the run definitions, not computed.
+
+_TWO_RUNS = [(64, 1024, 0, 300, 3, 100),      # 3 fragments of 100 B: local 64 + 1024 i, canonical 300 i
+             (5000, 200, 2000, 40, 2, 32)]    # 2 fragments of 32 B: local 5000 + 200 i, canonical 2000 + 40 i
 
 
-@pytest.mark.parametrize("gpu_to_cpu", [True, False])
-def test_copy_plan_unrolls_runs_in_order(gpu_to_cpu):
-    # two runs: 4 head slices of 256 B spread by 1 KiB locally and packed canonically,
-    # then one 512 B tail fragment
-    runs = [(0, 1024, 0, 256, 4, 256), (4096, 0, 1024, 0, 1, 512)]
-    fs, fd, fz = oracle.copy_plan(runs, gpu_to_cpu)
-    assert list(zip(fs.tolist(), fd.tolist(), fz.tolist())) == _brute_plan(runs, gpu_to_cpu)
+def test_copy_plan_gpu_to_cpu_hand_written():
+    fs, fd, fz = oracle.copy_plan(_TWO_RUNS, True)
+    # source = worker-local offsets, destination = canonical offsets, run by run
+    assert fs.tolist() == [64, 1088, 2112, 5000, 5200]
+    assert fd.tolist() == [0, 300, 600, 2000, 2040]
+    assert fz.tolist() == [100, 100, 100, 32, 32]
 
 
-def test_fragment_ptrs_broadcast_block_major():
-    g = synth.rng(34)
-    sb = g.integers(0, 1 << 40, size=5).astype(np.uint64)
-    db = g.integers(0, 1 << 40, size=5).astype(np.uint64)
-    fs, fd, fz = np.array([0, 300, 900]), np.array([10, 20, 30]), np.array([300, 600, 100])
-    os_, od, oz = oracle.fragment_ptrs(sb, db, fs, fd, fz)
-    for b in range(5):
-        for f in range(3):
-            i = b * 3 + f
-            assert os_[i] == sb[b] + np.uint64(fs[f]) and od[i] == db[b] + np.uint64(fd[f])
-            assert oz[i] == fz[f]
+def test_copy_plan_cpu_to_gpu_hand_written():
+    fs, fd, fz = oracle.copy_plan(_TWO_RUNS, False)
+    # source = canonical offsets, destination = worker-local offsets
+    assert fs.tolist() == [0, 300, 600, 2000, 2040]
+    assert fd.tolist() == [64, 1088, 2112, 5000, 5200]
+    assert fz.tolist() == [100, 100, 100, 32, 32]
+
+
+def test_copy_plan_empty_run_contributes_nothing():
+    fs, fd, fz = oracle.copy_plan([(0, 8, 0, 8, 0, 8), (16, 0, 32, 0, 1, 4)], True)
+    assert (fs.tolist(), fd.tolist(), fz.tolist()) == ([16], [32], [4])
+
+
+def test_fragment_ptrs_hand_written_block_major():
+    os_, od, oz = oracle.fragment_ptrs([1000, 50000], [7000, 90000], [0, 300], [10, 20], [300, 600])
+    # block 0's two fragments, then block 1's
+    assert os_.tolist() == [1000, 1300, 50000, 50300]
+    assert od.tolist() == [7010, 7020, 90010, 90020]
+    assert oz.tolist() == [300, 600, 300, 600]
+
+
+def _head_major_runs(tokens, heads, slice_bytes):
+    """One run per head: its `tokens` slices leave the token-major block with the
+    row stride and pack contiguously in the head-major block."""
+    return [(h * slice_bytes, heads * slice_bytes, h * tokens * slice_bytes, slice_bytes, tokens,
+             slice_bytes) for h in range(heads)]
+
+
+def test_canonical_copy_is_the_head_major_transpose():
+    # 6 blocks of 16 tokens x 8 heads x 256 B (128 fp16 dims): the canonical host block is
+    # the token-major device block with its token and head axes exchanged.
+    g = synth.rng(37)
+    T, H, S, nb = 16, 8, 256, 6
+    page = T * H * S
+    local = g.integers(0, 256, size=(nb, T, H, S), dtype=np.uint8)
+    canon = np.zeros((nb, H, T, S), np.uint8)
+    runs = _head_major_runs(T, H, S)
+    fs, fd, fz = oracle.copy_plan(runs, True)
+    lb = np.uint64(local.ctypes.data) + np.arange(nb, dtype=np.uint64) * np.uint64(page)
+    cb = np.uint64(canon.ctypes.data) + np.arange(nb, dtype=np.uint64) * np.uint64(page)
+    oracle.swap_blocks(*oracle.fragment_ptrs(lb, cb, fs, fd, fz))
+    for b in range(nb):
+        assert np.array_equal(canon[b], local[b].reshape(T, H, S).transpose(1, 0, 2))
+    # and back: canonical -> a fresh local buffer restores the token-major blocks
+    back = np.zeros_like(local)
+    bb = np.uint64(back.ctypes.data) + np.arange(nb, dtype=np.uint64) * np.uint64(page)
+    fs, fd, fz = oracle.copy_plan(runs, False)
+    oracle.swap_blocks(*oracle.fragment_ptrs(cb, bb, fs, fd, fz))
+    assert np.array_equal(back, local)
+
+
+def test_canonical_copy_with_a_padded_local_row():
+    # local rows padded to 3 heads' worth of slices for 2 heads: the padding slice of
+    # every token is never read, and the canonical block is still the transpose.
+    g = synth.rng(38)
+    T, H, S = 4, 2, 16
+    local = g.integers(0, 256, size=(T, 3, S), dtype=np.uint8)
+    canon = np.zeros((H, T, S), np.uint8)
+    runs = [(h * S, 3 * S, h * T * S, S, T, S) for h in range(H)]
+    fs, fd, fz = oracle.copy_plan(runs, True)
+    oracle.swap_blocks(*oracle.fragment_ptrs([local.ctypes.data], [canon.ctypes.data], fs, fd, fz))
+    assert np.array_equal(canon, local[:, :H, :].transpose(1, 0, 2))
 
 
 # ---------------------------------------------------------------- sparse rows (QSA staged prefill)
