@@ -872,9 +872,8 @@ def main(argv=None):
             "host_gbs": achieved, "link_peak_gbs": peaks,
             "roofline": {"bound": "host_link", "achieved": achieved, "peak": peaks["h2d"], "unit": "GB/s",
                          "frac": achieved / peaks["h2d"], "traffic": profiled_traffic(),
-                         "traffic_note": "dram__bytes_read+write of decode_split_kernel per launch (ncu, "
-                                         "profiles/decode_split_kernel_q8_0_L184320_N8192_headline.md); host-link bytes "
-                                         "are not DRAM traffic",
+                         "traffic_note": "dram__bytes_read+write of decode_split_kernel per launch (one ncu "
+                                         "capture of this workload); host-link bytes are not DRAM traffic",
                          "peak_source": "pinned cudaMemcpyAsync H2D 1 GiB, best of 5, measured in this run",
                          "kernel": "decode_split_kernel + decode_combine_kernel (one C-ABI call)"},
             "e2e": {"value": head["e2e_us"], "unit": "us/step", "h2d_bytes_per_step": head["e2e_h2d"],
@@ -899,21 +898,19 @@ def decode_source_sha256():
     return h.hexdigest()
 
 
+# DRAM bytes per launch of the headline decode kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum of decode_split_kernel, one ncu capture of the headline
+# workload), with the sha256 of the decode kernel source it was taken on.
+HEADLINE_TRAFFIC = {"bytes_per_launch": 17897984,
+                    "decode_source_sha256": "0dd642f49446d054dbb2e2abf55b277ce995b0450c94738be6cc9e4ef50a51ae"}
+
+
 def profiled_traffic():
-    """DRAM bytes per launch of the headline decode kernel, as recorded by the
-    committed ncu summary; None if the summary is missing or was taken on a
-    different decode kernel source than the one built now."""
-    path = os.path.join(ROOT, "profiles", "decode_split_kernel_q8_0_L184320_N8192_headline.md")
-    traffic = sha = None
-    try:
-        for line in open(path):
-            if line.startswith("traffic_bytes_per_launch:"):
-                traffic = int(line.split(":")[1])
-            elif line.startswith("decode_source_sha256:"):
-                sha = line.split(":")[1].strip()
-    except OSError:
+    """The captured DRAM traffic of the headline decode kernel; None once the
+    decode kernel source differs from the one the capture was taken on."""
+    if HEADLINE_TRAFFIC["decode_source_sha256"] != decode_source_sha256():
         return None
-    return traffic if sha == decode_source_sha256() else None
+    return HEADLINE_TRAFFIC["bytes_per_launch"]
 
 
 def gpu_launch_count(K, rows):

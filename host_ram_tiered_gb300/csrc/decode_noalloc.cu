@@ -4,6 +4,7 @@
 // (arguments, layouts, kernels, result within the decode tolerance) is the
 // same as kvo_attn_decode_tiered.
 #include <cstdio>
+#include <mutex>
 
 #include "kvo_internal.cuh"
 
@@ -16,11 +17,18 @@ namespace {
 __device__ __align__(256) unsigned char g_decode_scratch[KVO_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_decode_scratch, looked up once per device (with that
-// device current) on the first call made on it.
+// device current) on the first call made on it.  The lookup and the cache
+// are guarded by a mutex, so host threads calling at the same time on one
+// device do not race; a failed lookup is retried on the next call.  The
+// address is never looked up again, so a cudaDeviceReset (which reloads the
+// module, and may move the array) leaves the entry point unusable on that
+// device for the rest of the process.
 void *scratch_address() {
+  static std::mutex mu;
   static void *cached[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
   if (!cached[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) {
@@ -71,8 +79,8 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
   if (!out || !q || !ctx_len) return fail(KVO_ERR_ARG, "%s: NULL q/out/ctx_len", fn);
   if (!aligned16(q) || !aligned16(out)) return fail(KVO_ERR_ALIGN, "%s: q/out alignment", fn);
 
-  // Split geometry that fits the scratch: the regular one, with the split
-  // made longer (in steps of 32 cells) until the partials fit.
+  // Split geometry that fits the scratch: the regular one when its partials
+  // fit, else the fewest splits of whole 32-cell tiles that the scratch holds.
   const size_t per_split = (size_t)batch * n_q_heads * (head_dim + 2) * sizeof(float);
   if (per_split > (size_t)KVO_NOALLOC_SCRATCH_BYTES)
     return fail(KVO_ERR_WORKSPACE,
@@ -80,10 +88,11 @@ extern "C" int kvo_attn_decode_tiered_noalloc(
                 fn, per_split, (int)KVO_NOALLOC_SCRATCH_BYTES);
   int split_cells = 0, n_splits = 0;
   decode_geometry(batch, max_ctx, head_dim, &split_cells, &n_splits);
-  while ((size_t)n_splits * per_split > (size_t)KVO_NOALLOC_SCRATCH_BYTES) {
-    split_cells += 32;
+  const int64_t max_splits = (int64_t)((size_t)KVO_NOALLOC_SCRATCH_BYTES / per_split);   // >= 1
+  if (n_splits > max_splits) {
+    const int64_t cells = (max_ctx + max_splits - 1) / max_splits;
+    split_cells = (int)((cells + 31) / 32 * 32);
     n_splits = (int)((max_ctx + split_cells - 1) / split_cells);
-    if (n_splits < 1) n_splits = 1;
   }
 
   const int64_t n_lo = n_vram_cells < max_ctx ? n_vram_cells : max_ctx;

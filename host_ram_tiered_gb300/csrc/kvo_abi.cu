@@ -28,9 +28,6 @@ int cuda_status(cudaError_t e, const char *what) {
 }
 
 static int classify_one(const void *p, cudaPointerAttributes *a) {
-  const int vm = vmm_host_backed(p);         // a tier's ranges: known without asking
-  if (vm == 1) return kMappedHost;
-  if (vm == 0) return kDeviceMem;
   if (cudaPointerGetAttributes(a, p) != cudaSuccess) {
     cudaGetLastError();  // clear the sticky-free error of an unknown pointer
     return 0;
@@ -42,15 +39,38 @@ static int classify_one(const void *p, cudaPointerAttributes *a) {
 
 int classify(const void *p, size_t bytes) {
   if (p == nullptr) return 0;
-  cudaPointerAttributes a, b;
-  int k = classify_one(p, &a);
-  if (!k || bytes <= 1) return k;
-  const char *last = (const char *)p + (bytes - 1);
-  int k2 = classify_one(last, &b);
-  if (!k2) return 0;
-  // both ends device-accessible but of different kinds (a VMM tier's VRAM head
-  // running into its host tail): device-accessible, not all device memory
-  return k2 == k ? k : kMappedHost;
+  const uintptr_t end = (uintptr_t)p + (bytes > 0 ? bytes : 1);
+  uintptr_t cur = (uintptr_t)p;
+  int kind = 0;
+  // Walk the allocations the range spans: each step classifies the byte at
+  // `cur` and jumps past the end of the allocation (or VMM tier range) that
+  // holds it.  A range spans few allocations; one over 1024 is refused.
+  for (int step = 0; cur < end; ++step) {
+    if (step == 1024) return 0;
+    int k;
+    uintptr_t next = 0;
+    const int vm = vmm_host_backed((const void *)cur, &next);   // a tier's ranges: known without asking
+    if (vm >= 0) {
+      k = vm ? kMappedHost : kDeviceMem;
+    } else {
+      cudaPointerAttributes a;
+      k = classify_one((const void *)cur, &a);
+      uintptr_t lo = 0;
+      if (k && !alloc_range((const void *)cur, &lo, &next)) {
+        // the driver gives no range: fall back to the kind of the last byte
+        cudaPointerAttributes b;
+        const int k2 = classify_one((const void *)(end - 1), &b);
+        if (!k2) return 0;
+        k = k2 == k ? k : kMappedHost;
+        next = end;
+      }
+    }
+    if (!k) return 0;
+    kind = kind == 0 || kind == k ? k : kMappedHost;
+    if (next <= cur) return 0;
+    cur = next;
+  }
+  return kind;
 }
 
 Ring *ring(int which) {
@@ -58,6 +78,8 @@ Ring *ring(int which) {
   int dev = 0;
   if (which < 0 || which > 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   Ring &r = rings[which][dev];
+  static std::mutex mu;                      // two host threads never create one ring twice
+  std::lock_guard<std::mutex> lock(mu);
   if (!r.side) {
     cudaStream_t s = nullptr, s2 = nullptr;
     if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;

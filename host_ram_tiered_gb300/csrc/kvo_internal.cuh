@@ -18,12 +18,18 @@ int cuda_status(cudaError_t e, const char *what);
 
 enum Access { kDeviceMem = 1, kMappedHost = 2 };
 // Classify [p, p + bytes): returns kDeviceMem, kMappedHost or 0 (not
-// device-accessible: unregistered pageable memory, NULL, or a range that ends
-// outside the allocation that holds its first byte).
+// device-accessible: unregistered pageable memory, NULL, or a range with a
+// byte in no allocation).  The range is walked allocation by allocation, so a
+// gap between two allocations is found; a range over allocations of both
+// kinds counts as kMappedHost (device-accessible, not all device memory).
 int classify(const void *p, size_t bytes);
 // 1: p lies in the host-backed tail of a live VMM tier; 0: in a tier's VRAM
-// range; -1: in no tier.
-int vmm_host_backed(const void *p);
+// range; -1: in no tier.  *range_end (if given) receives the end of the
+// tier range holding p.
+int vmm_host_backed(const void *p, uintptr_t *range_end = nullptr);
+// [*lo, *hi): the allocation (or reserved range) holding p, from the driver's
+// pointer attributes; false when the driver cannot say.
+bool alloc_range(const void *p, uintptr_t *lo, uintptr_t *hi);
 
 int num_sms();                       // SMs of the current device (cached)
 

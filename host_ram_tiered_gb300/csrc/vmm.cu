@@ -33,6 +33,7 @@ struct Drv {
   CUresult (*granularity)(size_t *, const CUmemAllocationProp *, CUmemAllocationGranularity_flags);
   CUresult (*dev_attr)(int *, CUdevice_attribute, CUdevice);
   CUresult (*dev_get)(CUdevice *, int);
+  CUresult (*ptr_attr)(void *, CUpointer_attribute, CUdeviceptr);   // optional: range queries
   bool ok = false;
 };
 
@@ -62,6 +63,7 @@ const Drv &drv() {
     ok &= get("cuDeviceGetAttribute", (void **)&d.dev_attr);
     ok &= get("cuDeviceGet", (void **)&d.dev_get);
     d.ok = ok;
+    get("cuPointerGetAttribute", (void **)&d.ptr_attr);
   });
   return d;
 }
@@ -159,12 +161,28 @@ void unregister_tier(const Tier *t) {
 
 }  // namespace
 
-int vmm_host_backed(const void *p) {
+int vmm_host_backed(const void *p, uintptr_t *range_end) {
   std::lock_guard<std::mutex> lock(reg_mu);
   const uintptr_t a = (uintptr_t)p;
   for (const Range &r : registry())
-    if (a >= r.lo && a < r.hi) return r.host;
+    if (a >= r.lo && a < r.hi) {
+      if (range_end) *range_end = r.hi;
+      return r.host;
+    }
   return -1;
+}
+
+bool alloc_range(const void *p, uintptr_t *lo, uintptr_t *hi) {
+  const Drv &d = drv();
+  if (!d.ptr_attr) return false;
+  CUdeviceptr start = 0;
+  size_t size = 0;
+  if (d.ptr_attr(&start, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS ||
+      d.ptr_attr(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS)
+    return false;
+  *lo = (uintptr_t)start;
+  *hi = (uintptr_t)start + size;
+  return *lo <= (uintptr_t)p && (uintptr_t)p < *hi;
 }
 
 }  // namespace kvo

@@ -141,12 +141,16 @@ int kvo_fragment_ptrs(const int64_t *src_bases, const int64_t *dst_bases,
  *   page's pooled pinned buffers).  In SM mode the kernel reads them through
  *   the device mapping while it runs; in copy-engine mode the host reads them
  *   during this call.
- * Each src[i] / dst[i] must be device-accessible.  Any alignment and size
+ * Each src[i] / dst[i] must be device-accessible; the library does not
+ *   check descriptor targets (it would have to look up every one of them).
+ *   Any alignment and size
  *   is accepted; descriptors whose two addresses and size are 16-byte
  *   multiples take the 16-byte vector path, others an 8-, 4- or 1-byte path.
  * flags: KVO_SWAP_H2D or KVO_SWAP_D2H (direction, used for the mode
- *   choice); KVO_SWAP_SRC_ORDER_ANY (the source is not written while the copy
- *   runs: the SM kernel may read it through the read-only path);
+ *   choice); KVO_SWAP_SRC_ORDER_ANY (the page's is_src_access_order_any: the
+ *   source is not written while the copy runs) is accepted and has no
+ *   effect -- both modes read every source byte exactly once, in whatever
+ *   order, so there is nothing a read-only or reordered path would save;
  *   KVO_SWAP_FORCE_SM / KVO_SWAP_FORCE_CE force a mode.  Default: the copy
  *   engine when there are at most KVO_SWAP_CE_MAX_DESCRIPTORS descriptors
  *   and each is at least KVO_SWAP_CE_MIN_BYTES, else SM mode -- a crossover
@@ -290,14 +294,22 @@ int kvo_attn_decode_tiered(const void *q, int q_dtype, int64_t batch,
  * device array of KVO_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading
  * the library holds until the process exits; the call itself allocates
  * nothing (no cudaMalloc, no cudaFree).  The split length is the regular
- * one, lengthened in 32-cell steps until the partials fit, so results agree
- * with kvo_attn_decode_tiered within the decode tolerance (not bit for bit
- * when the lengths differ).
+ * one when its partials fit; otherwise the context is cut into the fewest
+ * splits the array holds (KVO_NOALLOC_SCRATCH_BYTES / (batch * n_q_heads *
+ * (head_dim + 2) * 4) of them), each a whole number of 32-cell tiles, so
+ * results agree with kvo_attn_decode_tiered within the decode tolerance
+ * (not bit for bit when the lengths differ).  Staged and direct calls with
+ * the same sizes use the same splits and give the same bits.
  *   - batch * n_q_heads * (head_dim + 2) * 4 > KVO_NOALLOC_SCRATCH_BYTES
  *     returns KVO_ERR_WORKSPACE.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current, under a lock); make
+ *     that first call before any stream capture.  The address is kept for
+ *     the life of the process: after a cudaDeviceReset of a device the
+ *     entry point must not be called on it again.
+ *   - The first staged call on a device whose work spans more than one wave
+ *     of CTAs creates the library's copy stream and events (no device
+ *     memory); make it, too, before any stream capture.
  *   - Every call shares the array and leaves its partials there.  Calls
  *     whose GPU work overlaps (two streams, or two host threads) race on it;
  *     order them on one stream or serialise them.  No part of the array needs
