@@ -583,32 +583,37 @@ def oracle_c3_step(L, heads=DEC_HQ):
     return step, keep
 
 
+def headline_config():
+    return {"workload": HEADLINE, "L": 184320, "n_vram_cells": 8192, "q_heads": DEC_HQ,
+            "kv_heads": DEC_HKV, "head_dim": DEC_D, "kv_dtype": "q8_0", "batch": 1,
+            "staging": False, "l2": "flushed between timed steps (256 MiB write)"}
+
+
 def run_reference(args):
     import oracle
     oracle.build()
     threads = oracle.set_threads(os.cpu_count() or 1)
     L = max(DEC_LS)
-    # Bounded sample: the oracle decodes 8 of the 48 query heads per step
-    # (one kv head's worth of GQA rows is 6; 8 keeps the time per step near
-    # a second on 16 Grace cores), scaled to a full step by 48/8.
-    heads = 8
-    step, keep = oracle_c3_step(L, heads)
+    # Every step is the whole headline decode (all 48 query heads over the
+    # 184,320 cells, parallel over heads on the host's cores): about 2 s on
+    # 16 Grace cores, so the default 20 + 5 steps end within a minute.
+    step, keep = oracle_c3_step(L, DEC_HQ)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    us = dt / args.steps * 1e6 * (DEC_HQ / heads)
+    us = dt / args.steps * 1e6
     host_b, dev_b = dec_bytes(L, 8192)
     line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": HEADLINE, "L": L, "n_vram_cells": 8192, "q_heads": DEC_HQ,
-                       "kv_heads": DEC_HKV, "head_dim": DEC_D, "kv_dtype": "q8_0", "batch": 1},
+            "config": headline_config(),
             "cpu_baseline": {"value": us, "unit": "us/step", "cores": threads, "kind": "oracle",
-                             "sample": f"{heads} of {DEC_HQ} query heads per step, scaled x{DEC_HQ // heads}"},
+                             "sample": f"the whole headline step ({DEC_HQ} query heads x {L} cells), "
+                                       f"{args.steps} timed steps, no scaling"},
             "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "host_gbs_equiv": host_b / (us * 1e-6) / 1e9}
     return line
@@ -866,9 +871,7 @@ def main(argv=None):
             "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "q8_0 K/V x f16 q, f32 accumulate",
             "data": "synthetic (seeded)",
-            "config": {"workload": HEADLINE, "L": 184320, "n_vram_cells": 8192, "q_heads": DEC_HQ,
-                       "kv_heads": DEC_HKV, "head_dim": DEC_D, "kv_dtype": "q8_0", "batch": 1,
-                       "staging": False, "l2": "flushed between timed steps (256 MiB write)"},
+            "config": headline_config(),
             "host_gbs": achieved, "link_peak_gbs": peaks,
             "roofline": {"bound": "host_link", "achieved": achieved, "peak": peaks["h2d"], "unit": "GB/s",
                          "frac": achieved / peaks["h2d"], "traffic": profiled_traffic(),
@@ -990,34 +993,75 @@ def _timed(fn, budget_s=3.0, max_n=20, warm=True):
     return (time.perf_counter() - t0) / n
 
 
+def _pool_run(pool, parts):
+    """Run the callables in `parts` on the thread pool and wait (the oracle's
+    ctypes calls release the GIL, so the parts run on separate cores)."""
+    for f in [pool.submit(p) for p in parts]:
+        f.result()
+
+
+def _split(n, k):
+    return [(n * i // k, n * (i + 1) // k) for i in range(k) if n * i // k < n * (i + 1) // k]
+
+
 def cpu_rows(threads):
     """The oracle on bounded samples of the other rows, scaled to one step of
-    each workload (the swap and gather oracles are single-threaded memcpy
-    loops; the attention oracles run on `threads` cores)."""
+    each workload.  The swap and gather oracles are plain memcpy loops: each is
+    timed on one thread and on `threads` threads that each take a contiguous
+    range of descriptors (swap) or of sequences (gather).  The attention
+    oracles run on `threads` cores."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     res = {}
-    # swap, 32 KiB pages: 4,096 of the 131,072 descriptors, host to host
-    page, nd = 32768, 4096
-    src = np.zeros(nd * page, np.uint8)
-    dst = np.zeros(nd * page, np.uint8)
-    perm = synth.rng(SEED0 + 1, 9).permutation(nd)
-    s_ptr = (src.ctypes.data + perm.astype(np.uint64) * page).astype(np.uint64)
-    d_ptr = (dst.ctypes.data + np.arange(nd, dtype=np.uint64) * page).astype(np.uint64)
-    sizes = np.full(nd, page, np.int64)
-    dt = _timed(lambda: oracle.swap_blocks(s_ptr, d_ptr, sizes))
-    res["swap_swap_32KiB"] = {"value": dt * 1e6 * (131072 / nd), "unit": "us/step",
-                            "sample": f"{nd} of 131,072 descriptors, scaled x{131072 // nd}", "cores": 1}
-    del src, dst
+    pool = ThreadPoolExecutor(threads)
+
+    def swap_rows(name, page, nd, total):
+        src = np.zeros(nd * page, np.uint8)
+        dst = np.zeros(nd * page, np.uint8)
+        perm = synth.rng(SEED0 + 1, 9).permutation(nd)
+        s_ptr = (src.ctypes.data + perm.astype(np.uint64) * page).astype(np.uint64)
+        d_ptr = (dst.ctypes.data + np.arange(nd, dtype=np.uint64) * page).astype(np.uint64)
+        sizes = np.full(nd, page, np.int64)
+        scale = total / nd
+        sample = (f"{nd} of {total:,} descriptors, scaled x{scale:g}" if nd < total
+                  else f"the full {total:,} descriptors")
+        dt1 = _timed(lambda: oracle.swap_blocks(s_ptr, d_ptr, sizes))
+        parts = [lambda a=a, b=b: oracle.swap_blocks(s_ptr[a:b], d_ptr[a:b], sizes[a:b])
+                 for a, b in _split(nd, threads)]
+        dtn = _timed(lambda: _pool_run(pool, parts))
+        res[name] = {"value": dt1 * 1e6 * scale, "unit": "us/step", "sample": sample, "cores": 1,
+                     "all_cores": {"value": dtn * 1e6 * scale, "cores": threads}}
+
+    # C1: 4 tensors x 64 blocks of 32 KiB per direction (the whole step)
+    swap_rows("tiny_swap_64blocks", 32768, 256, 256)
+    # C2: 32 KiB pages, 4,096 of the 131,072 descriptors; 2 KiB pages, all of them
+    swap_rows("swap_32KiB", 32768, 4096, 131072)
+    swap_rows("swap_2KiB", 2048, 131072, 131072)
+    # C1 decode: one sequence, 32 q / 8 kv heads x 128 fp16, 1,024 cells (512 in the head)
+    g = synth.rng(SEED0, 10)
+    kt = synth.normal_bits((1024, 8 * 128), "f16", g).view(np.uint8)
+    vt = synth.normal_bits((1024, 8 * 128), "f16", g).view(np.uint8)
+    qt = synth.normal_bits((1, 32, 128), "f16", g)
+    kh, vh, ktl, vtl = (np.ascontiguousarray(x) for x in (kt[:512], vt[:512], kt[512:], vt[512:]))
+    cache = oracle.make_cache(kh, vh, ktl, vtl, 512, 512, 512, oracle.F16, 8, 128)
+    dt = _timed(lambda: oracle.attn_decode(cache, qt, oracle.F16, 1, 32, [1024], 1.0 / math.sqrt(128)))
+    res["tiny_f16_decode_L1024_N512"] = {"value": dt * 1e6, "unit": "us/step", "sample": "full step",
+                                         "cores": threads}
     # gather: 64 blocks of 64 tokens per (sequence, kv head), 8 x 4 x 128 bf16 planes of 65,536 tokens
     # (the same 64 MiB copied as the full 2^20-token planes)
     T = 65536
     plane = np.zeros((TOPK_S, T, TOPK_HKV, TOPK_D), np.uint16)
     sel = synth.topk_selection(TOPK_S, TOPK_HKV, T // 64, 64, synth.rng(SEED0 + 3, 9))
-    dt = _timed(lambda: oracle.gather_blocks(plane, TOPK_S, T, TOPK_HKV, TOPK_D, 2, 64, sel))
-    res["topk_gather_8seq_64blocks"] = {"value": dt * 1e6 * 2, "unit": "us/step",
-                        "sample": "K plane only (x2 for K and V), 65,536-token planes, full selection",
-                        "cores": 1}
+    dt1 = _timed(lambda: oracle.gather_blocks(plane, TOPK_S, T, TOPK_HKV, TOPK_D, 2, 64, sel))
+    parts = [lambda a=a, b=b: oracle.gather_blocks(plane[a:b], b - a, T, TOPK_HKV, TOPK_D, 2, 64, sel[a:b])
+             for a, b in _split(TOPK_S, min(threads, TOPK_S))]
+    dtn = _timed(lambda: _pool_run(pool, parts))
+    res["topk_gather_8seq_64blocks"] = {
+        "value": dt1 * 1e6 * 2, "unit": "us/step", "cores": 1,
+        "sample": "K plane only (x2 for K and V), 65,536-token planes, full selection",
+        "all_cores": {"value": dtn * 1e6 * 2, "cores": min(threads, TOPK_S)}}
     del plane
+    pool.shutdown()
     # sparse decode over the 4,096 gathered cells: full size
     g = synth.rng(SEED0 + 3, 10)
     cells = TOPK_S * 4096
