@@ -258,14 +258,49 @@ def swap_setup(page, seed=SEED0 + 1):
     return st
 
 
-def swap_run(st, h2d, flags=0):
+def swap_run(st, h2d, flags=0, shard=None):
+    """One swap direction; shard = (lo, hi) takes descriptors [lo, hi) only."""
     k = kvo()
-    if h2d:
-        k.kvo_swap_blocks_batch(st["h2d_src"], st["h2d_dst"], st["sizes"], st["n_desc"],
-                                k.KVO_SWAP_H2D | k.KVO_SWAP_SRC_ORDER_ANY | flags)
-    else:
-        k.kvo_swap_blocks_batch(st["d2h_src"], st["d2h_dst"], st["sizes"], st["n_desc"],
-                                k.KVO_SWAP_D2H | flags)
+    lo, hi = shard if shard is not None else (0, st["n_desc"])
+    if hi <= lo:
+        return
+    src, dst = (st["h2d_src"], st["h2d_dst"]) if h2d else (st["d2h_src"], st["d2h_dst"])
+    k.kvo_swap_blocks_batch(src.data_ptr() + 8 * lo, dst.data_ptr() + 8 * lo, st["sizes"].data_ptr() + 8 * lo,
+                            hi - lo, (k.KVO_SWAP_H2D | k.KVO_SWAP_SRC_ORDER_ANY if h2d else k.KVO_SWAP_D2H) | flags)
+
+
+# SM copies against the copy engine: page sizes (KiB) and descriptor counts of
+# the crossover sweep, each a set of seeded random block ids in 2,560-page pools.
+SWEEP_PAGES_KIB = (2, 8, 32, 128, 1024)
+SWEEP_COUNTS = (64, 2048)
+SWEEP_POOL = 2560
+
+
+def swap_sweep_setup(page, seed=SEED0 + 5):
+    """Device and pinned pools of SWEEP_POOL pages, descriptors for the largest
+    count (smaller counts take a prefix)."""
+    k = kvo()
+    d = dev(SWEEP_POOL * page)
+    h = pinned(SWEEP_POOL * page)
+    synth.fill_bytes_large(h.numpy(), seed, page)
+    g = synth.rng(seed, page)
+    n = max(SWEEP_COUNTS)
+    gids = g.permutation(SWEEP_POOL)[:n].astype(np.int64)
+    hids = g.permutation(SWEEP_POOL)[:n].astype(np.int64)
+    gp = np.empty(n, np.int64)
+    hp = np.empty(n, np.int64)
+    k.kvo_sub_block_ptrs(gids.ctypes.data, n, 1, 0, d.data_ptr(), page, page, gp.ctypes.data, n)
+    k.kvo_sub_block_ptrs(hids.ctypes.data, n, 1, 0, h.data_ptr(), page, page, hp.ctypes.data, n)
+    return {"page": page, "dev": d, "host": h, "gp": pinned_i64(gp), "hp": pinned_i64(hp),
+            "sizes": pinned_i64(np.full(n, page, np.int64))}
+
+
+def swap_sweep_run(st, h2d, n, ce):
+    k = kvo()
+    src, dst = (st["hp"], st["gp"]) if h2d else (st["gp"], st["hp"])
+    k.kvo_swap_blocks_batch(src, dst, st["sizes"], n,
+                            (k.KVO_SWAP_H2D if h2d else k.KVO_SWAP_D2H) |
+                            (k.KVO_SWAP_FORCE_CE if ce else k.KVO_SWAP_FORCE_SM))
 
 
 # ----------------------------------------------------------------- q8_0 tiered decode
@@ -382,44 +417,48 @@ def dec_bytes(L, N):
 TOPK_S, TOPK_T, TOPK_HQ, TOPK_HKV, TOPK_D, TOPK_BLK, TOPK_K = 8, 1 << 20, 16, 4, 128, 64, 64
 
 
-def topk_setup(seed=SEED0 + 3):
+def topk_setup(seed=SEED0 + 3, shard=None):
     """QSA-style sparse decode: bf16 K/V planes [8][2^20][4][128] in pinned
     host memory, 64 of 16,384 blocks per (sequence, kv head) selected
     without replacement (the last block always), gathered into VRAM, then
-    decode over the 4096 gathered tokens."""
+    decode over the 4096 gathered tokens.  shard = (lo, hi): this process
+    holds and computes sequences [lo, hi) only (the other sequences' planes
+    are not allocated)."""
     t = torch()
-    plane = TOPK_S * TOPK_T * TOPK_HKV * TOPK_D
+    lo, hi = shard if shard is not None else (0, TOPK_S)
+    plane = (hi - lo) * TOPK_T * TOPK_HKV * TOPK_D
     k_plane = pinned(plane * 2)
     v_plane = pinned(plane * 2)
     synth.fill_normal_bits_large(k_plane.numpy().view(np.uint16), "bf16", seed, 1)
     synth.fill_normal_bits_large(v_plane.numpy().view(np.uint16), "bf16", seed, 2)
     g = synth.rng(seed, 3)
-    sel = synth.topk_selection(TOPK_S, TOPK_HKV, TOPK_T // TOPK_BLK, TOPK_K, g)
-    q = synth.normal_bits((TOPK_S, TOPK_HQ, TOPK_D), "bf16", g)
+    sel = synth.topk_selection(TOPK_S, TOPK_HKV, TOPK_T // TOPK_BLK, TOPK_K, g)[lo:hi]
+    q = synth.normal_bits((TOPK_S, TOPK_HQ, TOPK_D), "bf16", g)[lo:hi]
     tok = TOPK_K * TOPK_BLK
-    out_bytes = TOPK_S * tok * TOPK_HKV * TOPK_D * 2
-    st = {"k_plane": k_plane, "v_plane": v_plane, "sel_np": sel,
+    n = hi - lo
+    out_bytes = n * tok * TOPK_HKV * TOPK_D * 2
+    st = {"k_plane": k_plane, "v_plane": v_plane, "sel_np": sel, "n_seq": n,
           "sel": t.from_numpy(sel.reshape(-1).copy()).cuda(),
           "kg": dev(out_bytes), "vg": dev(out_bytes), "q_np": q,
           "q": t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda(),
-          "ctx": t.full((TOPK_S,), tok, dtype=t.int32, device="cuda"),
-          "out": t.empty(TOPK_S * TOPK_HQ * TOPK_D, dtype=t.float32, device="cuda"),
+          "ctx": t.full((n,), tok, dtype=t.int32, device="cuda"),
+          "out": t.empty(n * TOPK_HQ * TOPK_D, dtype=t.float32, device="cuda"),
           "gather_bytes": 2 * out_bytes}
-    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(TOPK_S, TOPK_HQ, TOPK_D, tok)
+    st["ws_bytes"] = kvo().kvo_attn_decode_workspace_bytes(n, TOPK_HQ, TOPK_D, tok)
     st["ws"] = dev(st["ws_bytes"])
     return st
 
 
 def topk_gather(st):
     k = kvo()
-    k.kvo_gather_blocks(st["k_plane"], st["v_plane"], TOPK_S, TOPK_T, TOPK_HKV, TOPK_D, k.BF16, TOPK_BLK,
+    k.kvo_gather_blocks(st["k_plane"], st["v_plane"], st["n_seq"], TOPK_T, TOPK_HKV, TOPK_D, k.BF16, TOPK_BLK,
                         st["sel"], TOPK_K, st["kg"], st["vg"])
 
 
 def topk_decode(st):
     k = kvo()
     tok = TOPK_K * TOPK_BLK
-    k.kvo_attn_decode_tiered(st["q"], k.BF16, TOPK_S, TOPK_HQ, TOPK_HKV, TOPK_D, st["kg"], st["vg"], tok,
+    k.kvo_attn_decode_tiered(st["q"], k.BF16, st["n_seq"], TOPK_HQ, TOPK_HKV, TOPK_D, st["kg"], st["vg"], tok,
                              None, None, 0, k.BF16, st["ctx"], tok, tok, 1.0 / math.sqrt(TOPK_D),
                              None, None, st["out"], st["ws"], st["ws_bytes"])
 
@@ -468,9 +507,22 @@ def pf_run(st, staged=True, q=None, out=None):
                               out if out is not None else st["out"], st["ws"], st["ws_bytes"])
 
 
-def pf_flops():
+# Query-row counts of the staged/direct crossover sweep: the last `rows`
+# positions of the 262,144-cell context, the same cells and tiers as above.
+PF_SWEEP_ROWS = (16, 32, 64, 128, 256)
+
+
+def pf_run_rows(st, rows, staged):
+    k = kvo()
+    k.kvo_attn_prefill_tiered(st["q"], rows, PF_L - rows, PF_HQ, PF_HKV, PF_D, st["k_head"], st["v_head"],
+                              st["k_host"], st["v_host"], k.BF16, PF_L, PF_N, 1.0 / math.sqrt(PF_D),
+                              st["arena"] if staged else None, PF_ARENA if staged else 0,
+                              min(PF_RPL, rows), st["out"], st["ws"], st["ws_bytes"])
+
+
+def pf_flops(rows=PF_R, pos0=PF_POS0):
     # causal: row i sees pos0 + i + 1 cells; QK^T and PV are 2 flops per MAC each
-    cells = sum(PF_POS0 + i + 1 for i in range(PF_R))
+    cells = sum(pos0 + i + 1 for i in range(rows))
     return 4.0 * PF_HQ * PF_D * cells
 
 
@@ -643,11 +695,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvo", choices=["kvo", "reference"])
     ap.add_argument("--rows", default="all",
-                    help="comma list of head (headline decode only), tiny, swap, decode, vmm (the headline decode "
+                    help="comma list of head (headline decode only), tiny, swap, swapsweep (SM copies vs the copy "
+                         "engine over page sizes), decode, vmm (the headline decode "
                          "over VMM tiers), topk, prefill, append, sparse (QSA sparse rows), decode_vram (the 184,320-"
                          "cell all-VRAM decode alone; not in 'all') (default: all rows at one GPU, the headline alone "
                          "under torchrun)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--split", default="replicas", choices=["replicas", "shards"],
+                    help="under torchrun: every rank runs the whole workload (replicas, weak scaling), or the "
+                         "swap descriptors and the top-k sequences are divided among the ranks by "
+                         "kvo_shard_range (shards, strong scaling; the headline decode of one sequence stays "
+                         "a replica)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
     rank, world, local = rank_info()
@@ -670,9 +728,10 @@ def main(argv=None):
     # so the default there is the headline alone (the full set would pin about
     # 30 GB of host memory per rank).
     if args.rows == "all" and world > 1:
-        rows = {"head"}
+        rows = {"head", "swap", "topk"} if args.split == "shards" else {"head"}
     elif args.rows == "all":
-        rows = {"head", "tiny", "swap", "decode", "vmm", "topk", "prefill", "append", "sparse"}
+        rows = {"head", "tiny", "swap", "swapsweep", "decode", "vmm", "topk", "prefill", "pfsweep", "append",
+                "sparse"}
     else:
         rows = set(args.rows.split(","))
     timer = Timer()
@@ -681,6 +740,12 @@ def main(argv=None):
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 6800.0
     K, W = args.steps, args.warmup
     results = {}
+
+    def shard(n_units):
+        """This rank's contiguous share [lo, hi) of n_units (everything without --split shards)."""
+        if world == 1 or args.split != "shards":
+            return 0, n_units
+        return k.kvo_shard_range(n_units, world, rank)
 
     def bar():
         if world > 1:
@@ -785,28 +850,54 @@ def main(argv=None):
     if "swap" in rows:
         for page in (32768, 2048):
             st2 = swap_setup(page)
+            sh = shard(st2["n_desc"])
             for h2d in (True, False):
-                tot, _ = timer.run(lambda: swap_run(st2, h2d), K, W)
+                tot, _ = timer.run(lambda: swap_run(st2, h2d, shard=sh), K, W)
                 us_r = max_over_ranks(tot, world) / K * 1e3
-                gbs = st2["bytes"] / (us_r * 1e-6) / 1e9
-                pk = peaks["h2d" if h2d else "d2h"]
+                # whole-job bytes: every rank's share (the whole list once when sharded)
+                job_bytes = st2["bytes"] * (1 if args.split == "shards" else world)
+                gbs = job_bytes / (us_r * 1e-6) / 1e9
+                pk = peaks["h2d" if h2d else "d2h"] * world
                 results[f"swap_{page // 1024}KiB_{'h2d' if h2d else 'd2h'}"] = {
                     "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / pk,
-                    "descriptors": st2["n_desc"], "mode": "sm"}
+                    "descriptors": st2["n_desc"], "mode": "sm",
+                    "scaling": "strong" if args.split == "shards" and world > 1 else "weak"}
             del st2
+            t.cuda.empty_cache()
+    # ---- SM copies vs the copy engine over page sizes and descriptor counts
+    if "swapsweep" in rows:
+        for pk_kib in SWEEP_PAGES_KIB:
+            st8 = swap_sweep_setup(pk_kib << 10)
+            for n in SWEEP_COUNTS:
+                for h2d in (True, False):
+                    for ce in (False, True):
+                        tot, _ = timer.run(lambda: swap_sweep_run(st8, h2d, n, ce), K, W)
+                        us_r = max_over_ranks(tot, world) / K * 1e3
+                        gbs = n * (pk_kib << 10) / (us_r * 1e-6) / 1e9
+                        pk = peaks["h2d" if h2d else "d2h"]
+                        results[f"swapsweep_{pk_kib}KiB_x{n}_{'h2d' if h2d else 'd2h'}_{'ce' if ce else 'sm'}"] = {
+                            "us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / pk}
+            del st8
             t.cuda.empty_cache()
     # ---- top-k gather + sparse decode
     if "topk" in rows:
-        st4 = topk_setup()
+        sh = shard(TOPK_S)
+        st4 = topk_setup(shard=sh)
+        # whole-job bytes: 8 sequences once when sharded, once per rank as replicas
+        full_bytes = 2 * TOPK_S * TOPK_K * TOPK_BLK * TOPK_HKV * TOPK_D * 2
+        job_bytes = full_bytes if args.split == "shards" else full_bytes * world
+        scal = "strong" if args.split == "shards" and world > 1 else "weak"
         tot, _ = timer.run(lambda: topk_gather(st4), K, W)
         us_r = max_over_ranks(tot, world) / K * 1e3
-        gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
-        results["topk_gather_8seq_64blocks"] = {"us_per_step": us_r, "host_gbs": gbs, "roofline_frac": gbs / peaks["h2d"]}
+        gbs = job_bytes / (us_r * 1e-6) / 1e9
+        results["topk_gather_8seq_64blocks"] = {"us_per_step": us_r, "host_gbs": gbs,
+                                                "roofline_frac": gbs / (peaks["h2d"] * world), "scaling": scal}
         topk_gather(st4)
         tot, _ = timer.run(lambda: topk_decode(st4), K, W)
         us_r = max_over_ranks(tot, world) / K * 1e3
-        gbs = st4["gather_bytes"] / (us_r * 1e-6) / 1e9
-        results["topk_sparse_decode_8x4096"] = {"us_per_step": us_r, "hbm_gbs": gbs, "roofline_frac": gbs / hbm}
+        gbs = job_bytes / (us_r * 1e-6) / 1e9
+        results["topk_sparse_decode_8x4096"] = {"us_per_step": us_r, "hbm_gbs": gbs,
+                                                "roofline_frac": gbs / (hbm * world), "scaling": scal}
         del st4
     # ---- write path: appends into the host tail
     if "append" in rows:
@@ -838,13 +929,13 @@ def main(argv=None):
                 "rows_per_s": SR_R / (us_r * 1e-6)}
         del st7
     # ---- tiered chunked prefill
-    if "prefill" in rows:
+    if "prefill" in rows or "pfsweep" in rows:
         st5 = pf_setup()
         fl = pf_flops()
         tail_b = (PF_L - PF_N) * st5["rb"] * 2
         bf16 = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops", 1932.2) \
             if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
-        for staged in (True, False):
+        for staged in ((True, False) if "prefill" in rows else ()):
             steps = K if staged else max(1, min(K, 3))
             tot, _ = timer.run(lambda: pf_run(st5, staged), steps, min(W, 3))
             us_r = max_over_ranks(tot, world) / steps * 1e3
@@ -853,6 +944,17 @@ def main(argv=None):
             results[f"prefill_R2048_L262144_N65536_{'staged' if staged else 'direct'}"] = {
                 "us_per_step": us_r, "tflops": tfs, "tensor_frac": tfs / bf16,
                 "roofline_frac": t_star / (us_r * 1e-6), "tokens_per_s": PF_R / (us_r * 1e-6)}
+        if "pfsweep" in rows:
+            # staged vs direct over the number of query rows: the direct kernel reads the host
+            # tail once per query tile of each kv head, the staged call once per call
+            for r in PF_SWEEP_ROWS:
+                for staged in (True, False):
+                    steps = K if staged else max(1, min(K, 3))
+                    tot, _ = timer.run(lambda: pf_run_rows(st5, r, staged), steps, min(W, 3))
+                    us_r = max_over_ranks(tot, world) / steps * 1e3
+                    results[f"pfsweep_R{r}_{'staged' if staged else 'direct'}"] = {
+                        "us_per_step": us_r, "host_gbs": tail_b / (us_r * 1e-6) / 1e9,
+                        "tflops": pf_flops(r, PF_L - r) / (us_r * 1e-6) / 1e12}
         del st5
     clk = clocks.stop()
 
@@ -941,6 +1043,10 @@ def gpu_launch_count(K, rows):
         n += K * 2 + K * sum(k.kvo_attn_decode_launches(1, 1024, 128, 512, s) for s in (False, True))
     if "swap" in rows:
         n += K * 4                                 # 2 pages x 2 directions, one swap kernel each
+    if "swapsweep" in rows:
+        # SM mode: one swap kernel per row (page sizes x counts x directions); the copy-engine
+        # rows launch no kernel
+        n += K * len(SWEEP_PAGES_KIB) * len(SWEEP_COUNTS) * 2
     if "topk" in rows:
         n += K + 2 * K                             # gather; decode split + combine
     if "append" in rows:
@@ -949,6 +1055,9 @@ def gpu_launch_count(K, rows):
         # staged: VRAM head (2 row blocks) + 48 arena buckets of 4096 cells x 2 row blocks;
         # direct: head + host tail, 2 row blocks each
         n += K * (2 + 48 * 2) + min(K, 3) * 4
+    if "pfsweep" in rows:
+        # one row block per call: staged = VRAM head + 48 buckets, direct = head + tail
+        n += len(PF_SWEEP_ROWS) * (K * 49 + max(1, min(K, 3)) * 2)
     if "sparse" in rows:
         # staged: partition + buckets x (page gather + 2 row blocks x a split kernel that folds
         # its one chunk per row itself), the arena holding two slots of arena / (4 page_bytes)

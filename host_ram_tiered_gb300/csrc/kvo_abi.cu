@@ -179,6 +179,22 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids, int64_t blocks_p
   return KVO_OK;
 }
 
+// ---------------------------------------------------------------- multi-GPU shards
+int kvo_shard_range(int64_t n_units, int64_t world, int64_t rank, int64_t *lo, int64_t *hi) {
+  clear_error();
+  if (!lo || !hi) return fail(KVO_ERR_ARG, "kvo_shard_range: NULL lo/hi");
+  if (n_units < 0 || world < 1 || rank < 0 || rank >= world)
+    return fail(KVO_ERR_ARG, "kvo_shard_range: n_units %lld, world %lld, rank %lld", (long long)n_units,
+                (long long)world, (long long)rank);
+  // floor(n * r / w) without overflow for any n < 2^63 and w < 2^31
+  auto cut = [&](int64_t r) {
+    return (n_units / world) * r + (n_units % world) * r / world;
+  };
+  *lo = cut(rank);
+  *hi = cut(rank + 1);
+  return KVO_OK;
+}
+
 // ---------------------------------------------------------------- canonical fragments
 int kvo_copy_plan(const int64_t *local_offset, const int64_t *local_stride,
                   const int64_t *canonical_offset, const int64_t *canonical_stride,

@@ -35,6 +35,7 @@ SIGNATURES = {
     "kvo_last_error": (ctypes.c_char_p, []),
     "kvo_device_errors": (_int, [_vp, _int]),
     "kvo_sub_block_ptrs": (_int, [_vp, _i64, _i64, _i64, _u64, _i64, _i64, _vp, _i64]),
+    "kvo_shard_range": (_int, [_i64, _i64, _i64, _vp, _vp]),
     "kvo_copy_plan": (_int, [_vp] * 6 + [_i64, _int, _vp, _vp, _vp, _i64, _vp]),
     "kvo_fragment_ptrs": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _i64, _vp, _vp, _vp]),
     "kvo_swap_blocks_batch": (_int, [_vp, _vp, _vp, _i64, _u32, _vp]),
@@ -137,6 +138,14 @@ def kvo_sub_block_ptrs(block_ids, n_ids, blocks_per_chunk, skip_count, base, row
     _check(load().kvo_sub_block_ptrs(_p(block_ids), n_ids, blocks_per_chunk, skip_count, base,
                                      row_stride_bytes, row_bytes, _p(out), n_out),
            "kvo_sub_block_ptrs")
+
+
+def kvo_shard_range(n_units, world, rank) -> tuple[int, int]:
+    """[lo, hi): rank's contiguous share of n_units work units."""
+    lo, hi = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load().kvo_shard_range(n_units, world, rank, ctypes.addressof(lo), ctypes.addressof(hi)),
+           "kvo_shard_range")
+    return lo.value, hi.value
 
 
 def kvo_copy_plan(local_offset, local_stride, canonical_offset, canonical_stride, num_fragments,

@@ -90,6 +90,26 @@ int kvo_sub_block_ptrs(const int64_t *block_ids, int64_t n_ids,
                        int64_t row_bytes, int64_t *out, int64_t n_out);
 
 /* ------------------------------------------------------------------------
+ * kvo_shard_range -- host function, synchronous, no CUDA: the contiguous
+ * share of n_units work units (swap descriptors, sequences of a gather or a
+ * decode batch) that rank `rank` of `world` processes takes.
+ *
+ * vLLM gpu_worker.py (transfer_async: each block's descriptors are
+ * independent) and the ExLlamaV3 qsa-kv-offload patch (each sequence's
+ * selection is independent): the path splits with no exchange step, so one
+ * process per GPU takes
+ *     [*lo, *hi) = [floor(n_units * rank / world), floor(n_units * (rank + 1) / world))
+ * -- the ranks' ranges are disjoint, cover [0, n_units) exactly once, in
+ * rank order, and differ in size by at most one unit.  A rank's call then
+ * passes the descriptor arrays offset by *lo (count *hi - *lo), or the
+ * sequence-indexed buffers offset by *lo sequences.
+ * Errors: KVO_ERR_ARG (n_units < 0, world < 1, rank outside [0, world),
+ *   NULL lo or hi).
+ * ---------------------------------------------------------------------- */
+int kvo_shard_range(int64_t n_units, int64_t world, int64_t rank, int64_t *lo,
+                    int64_t *hi);
+
+/* ------------------------------------------------------------------------
  * kvo_copy_plan / kvo_fragment_ptrs -- host functions, synchronous, no CUDA:
  * descriptors for a canonical host layout, fed to kvo_swap_blocks_batch.
  *

@@ -180,3 +180,24 @@ def test_sparse_rows_workspace_grows_with_buckets(kvo_lib):
     # grouped picks (64 x 96 int32) and offsets (64 x 9 int32) on top
     assert staged - direct >= 64 * 96 * 4 + 64 * 9 * 4
     assert kvo.kvo_attn_sparse_rows_workspace_bytes(0, 8, 2, 128, 96, 64, 16, 40, 0) == 0
+
+
+def test_shard_range_is_a_balanced_contiguous_partition(kvo_lib):
+    for n in (0, 1, 7, 8, 513, 131072):
+        for world in (1, 2, 3, 8):
+            ranges = [kvo.kvo_shard_range(n, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == n
+            for (lo, hi), (lo2, _) in zip(ranges, ranges[1:]):
+                assert hi == lo2                       # contiguous, in rank order
+            sizes = [hi - lo for lo, hi in ranges]
+            assert min(sizes) >= 0 and max(sizes) - min(sizes) <= 1
+    # large counts: no overflow of n * rank
+    lo, hi = kvo.kvo_shard_range((1 << 62) + 5, 7, 6)
+    assert hi == (1 << 62) + 5 and lo == ((1 << 62) + 5) * 6 // 7
+
+
+def test_shard_range_rejects_bad_ranks(kvo_lib):
+    for args in ((-1, 2, 0), (4, 0, 0), (4, 2, 2), (4, 2, -1)):
+        with pytest.raises(kvo.KvoError) as e:
+            kvo.kvo_shard_range(*args)
+        assert e.value.status == -1
