@@ -509,7 +509,7 @@ def pf_run(st, staged=True, q=None, out=None):
 
 # Query-row counts of the staged/direct crossover sweep: the last `rows`
 # positions of the 262,144-cell context, the same cells and tiers as above.
-PF_SWEEP_ROWS = (16, 32, 64, 128, 256)
+PF_SWEEP_ROWS = (1, 4, 16, 64, 256)
 
 
 def pf_run_rows(st, rows, staged):

@@ -53,8 +53,10 @@ uint32_t *device_error_word();       // address of the per-device word (nullptr 
 
 // Launchers implemented in the kernel translation units.  They assume the
 // entry point already validated every argument.
-cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes,
-                           int64_t n, bool src_readonly, cudaStream_t st);
+// max_size: the largest descriptor size when the host knows it (a short
+// batch whose sizes it read), else -1.
+cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes, int64_t n,
+                           int64_t max_size, cudaStream_t st);
 
 cudaError_t launch_gather(const void *k_plane, const void *v_plane, int64_t n_seq,
                           int64_t seq_stride_tokens, int64_t n_kv_heads, int64_t head_bytes,

@@ -43,17 +43,37 @@ __device__ __forceinline__ void warp_copy(const char *s, char *d, int64_t bytes,
   }
 }
 
-// A warp takes `per_warp` (1..32) consecutive descriptors: lane i loads
-// descriptor i (coalesced reads through the mapping instead of dependent
-// ones), then the warp copies them one after another, broadcasting each by
-// shuffle.  per_warp is chosen so the grid fills the GPU even for short
-// batches.
+// Long batches: a warp takes `per_warp` (1..32) consecutive descriptors:
+// lane i loads descriptor i (coalesced reads through the mapping instead of
+// dependent ones), then the warp copies them one after another, broadcasting
+// each by shuffle.  Short batches (parts > 1): each descriptor is cut into
+// `parts` pieces of a whole number of 512-byte units and a warp copies one
+// piece, so that a few large copies still spread over every SM.  The pieces
+// start at multiples of 512 bytes from the descriptor's start, which keeps
+// each piece's alignment class (and so its vector width) that of the whole.
+constexpr int64_t kPartUnit = 512;
+
 __global__ void __launch_bounds__(kSwapThreads)
 swap_kernel(const int64_t *__restrict__ src, const int64_t *__restrict__ dst,
-            const int64_t *__restrict__ sizes, int64_t n, int per_warp) {
+            const int64_t *__restrict__ sizes, int64_t n, int per_warp, int parts) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kSwapThreads + threadIdx.x) >> 5;
   const int64_t n_warps = ((int64_t)gridDim.x * kSwapThreads) >> 5;
+  if (parts > 1) {
+    for (int64_t item = warp; item < n * parts; item += n_warps) {
+      const int64_t i = item / parts;
+      const int64_t p = item - i * parts;
+      const int64_t z = sizes[i];            // every lane reads the same word: one request
+      if (z <= 0) continue;
+      int64_t piece = (z + parts - 1) / parts;
+      piece = (piece + kPartUnit - 1) / kPartUnit * kPartUnit;
+      const int64_t b0 = p * piece;
+      if (b0 >= z) continue;
+      const int64_t b1 = b0 + piece < z ? b0 + piece : z;
+      warp_copy((const char *)(uintptr_t)src[i] + b0, (char *)(uintptr_t)dst[i] + b0, b1 - b0, lane);
+    }
+    return;
+  }
   for (int64_t base = warp * per_warp; base < n; base += n_warps * per_warp) {
     const int64_t i = base + lane;
     int64_t s = 0, d = 0, z = 0;
@@ -146,18 +166,25 @@ uint32_t *device_error_word() {
 }
 
 cudaError_t launch_swap_sm(const int64_t *src, const int64_t *dst, const int64_t *sizes, int64_t n,
-                           bool src_readonly, cudaStream_t st) {
-  // Every copy here is stream-ordered, which already satisfies both source
-  // access orders; the read-only hint needs no separate kernel.
-  (void)src_readonly;
+                           int64_t max_size, cudaStream_t st) {
   const int64_t warps_per_cta = kSwapThreads / 32;
   const int64_t max_warps = (int64_t)num_sms() * 8 * warps_per_cta;   // 8 CTAs of 8 warps per SM
   int64_t per_warp = n / max_warps;
   if (per_warp < 1) per_warp = 1;
   if (per_warp > 32) per_warp = 32;
-  int64_t grid = (n + per_warp * warps_per_cta - 1) / (per_warp * warps_per_cta);
+  // Fewer descriptors than warps: cut each into pieces (at most 256).  When
+  // the host knows the largest size, pieces are at least 4 KiB, so that small
+  // pages do not launch warps with nothing to copy.
+  int64_t parts = n < max_warps ? max_warps / n : 1;
+  if (max_size >= 0) {
+    const int64_t want = (max_size + 4095) / 4096;
+    if (parts > want) parts = want > 0 ? want : 1;
+  }
+  if (parts > 256) parts = 256;
+  int64_t grid = parts > 1 ? (n * parts + warps_per_cta - 1) / warps_per_cta
+                           : (n + per_warp * warps_per_cta - 1) / (per_warp * warps_per_cta);
   if (grid > max_warps / warps_per_cta) grid = max_warps / warps_per_cta;
-  swap_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(src, dst, sizes, n, (int)per_warp);
+  swap_kernel<<<(unsigned)grid, kSwapThreads, 0, st>>>(src, dst, sizes, n, (int)per_warp, (int)parts);
   return cudaGetLastError();
 }
 

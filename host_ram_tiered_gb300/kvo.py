@@ -19,8 +19,7 @@ KVO_SWAP_D2H = 0x2
 KVO_SWAP_SRC_ORDER_ANY = 0x4
 KVO_SWAP_FORCE_SM = 0x8
 KVO_SWAP_FORCE_CE = 0x10
-KVO_SWAP_CE_MIN_BYTES = 1 << 20
-KVO_SWAP_CE_MAX_DESCRIPTORS = 64
+KVO_SWAP_SHORT_BATCH = 64
 KVO_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 STATUS = {0: "KVO_OK", -1: "KVO_ERR_ARG", -2: "KVO_ERR_ALIGN", -3: "KVO_ERR_NOT_MAPPED",

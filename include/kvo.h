@@ -166,19 +166,23 @@ int kvo_fragment_ptrs(const int64_t *src_bases, const int64_t *dst_bases,
  *   Any alignment and size
  *   is accepted; descriptors whose two addresses and size are 16-byte
  *   multiples take the 16-byte vector path, others an 8-, 4- or 1-byte path.
- * flags: KVO_SWAP_H2D or KVO_SWAP_D2H (direction, used for the mode
- *   choice); KVO_SWAP_SRC_ORDER_ANY (the page's is_src_access_order_any: the
- *   source is not written while the copy runs) is accepted and has no
- *   effect -- both modes read every source byte exactly once, in whatever
- *   order, so there is nothing a read-only or reordered path would save;
- *   KVO_SWAP_FORCE_SM / KVO_SWAP_FORCE_CE force a mode.  Default: the copy
- *   engine when there are at most KVO_SWAP_CE_MAX_DESCRIPTORS descriptors
- *   and each is at least KVO_SWAP_CE_MIN_BYTES, else SM mode -- a crossover
- *   measured on GB300: SM copies reach the same link bandwidth as the copy
- *   engine from 2 KiB pages up, while a copy-engine call costs ~2.7 us to
- *   issue, so the copy engine is only worth it (it leaves the SMs free) for
- *   a few large copies.  The rule reads no more than
- *   KVO_SWAP_CE_MAX_DESCRIPTORS sizes on the host.
+ * flags: KVO_SWAP_H2D or KVO_SWAP_D2H (the direction; informational: both
+ *   modes serve both); KVO_SWAP_SRC_ORDER_ANY (the page's
+ *   is_src_access_order_any: the source is not written while the copy runs)
+ *   is accepted and has no effect -- both modes read every source byte
+ *   exactly once, in whatever order, so there is nothing a read-only or
+ *   reordered path would save; KVO_SWAP_FORCE_CE selects the copy engine (one
+ *   cudaMemcpyAsync per run of descriptors whose source and destination both
+ *   continue the previous one; the host reads the descriptors during the
+ *   call).  Default (and KVO_SWAP_FORCE_SM): the SM kernel, which reads the
+ *   descriptors through the device mapping while it runs.  The default is a
+ *   crossover measured on GB300 (2 KiB - 1 MiB pages, 64 and 2,048
+ *   descriptors, both directions): the SM kernel is the faster mode in every
+ *   cell -- a copy-engine call costs ~1.7 us to issue, and the copy engine
+ *   moves 1 MiB copies at 126-147 GB/s against the SM kernel's 205-211 GB/s.
+ *   A batch of at most KVO_SWAP_SHORT_BATCH descriptors in pinned host memory
+ *   has its sizes read on the host (to cut large copies into pieces that
+ *   spread over every SM).
  * n == 0 is a no-op.
  * Errors: KVO_ERR_ARG (n < 0, NULL arrays, both FORCE flags),
  *   KVO_ERR_NOT_MAPPED (descriptor arrays not device-accessible in SM mode,
@@ -189,8 +193,7 @@ int kvo_fragment_ptrs(const int64_t *src_bases, const int64_t *dst_bases,
 #define KVO_SWAP_SRC_ORDER_ANY 0x4u
 #define KVO_SWAP_FORCE_SM 0x8u
 #define KVO_SWAP_FORCE_CE 0x10u
-#define KVO_SWAP_CE_MIN_BYTES (1 << 20)
-#define KVO_SWAP_CE_MAX_DESCRIPTORS 64
+#define KVO_SWAP_SHORT_BATCH 64
 
 int kvo_swap_blocks_batch(const int64_t *src, const int64_t *dst,
                           const int64_t *sizes, int64_t n, uint32_t flags,
