@@ -21,14 +21,19 @@
 // more warps), the scores of the tile's 32 cells, an online softmax in the
 // log2 domain, and P*V:
 //   * QK: lane = (quarter or eighth of the head dims, cell).  The lane's
-//     query slice lives in registers as fp16/bf16 pairs for the whole chunk;
-//     each pass takes CPP cells, and the LPC partial dot products of a cell
-//     are added by a transposing butterfly, after which lane c holds the G
-//     scores of cell c.  Products are fp16 x fp16 (or bf16 x bf16) with an
-//     fp32 accumulator (exact products, fp32 sums).  A q8_0 value x enters as
-//     the exact fp16 number 1152 + x (its byte with the sign bit flipped under
-//     an 0x64 exponent byte); the 1152 * sum(q) term is removed once per
-//     block before the block scale d multiplies the sum.
+//     query slice lives in registers for the whole chunk; each pass takes CPP
+//     cells, and the LPC partial dot products of a cell are added by a
+//     transposing butterfly, after which lane c holds the G scores of cell c.
+//     fp16/bf16 caches: the slice as 16-bit pairs, products fp16 x fp16 (or
+//     bf16 x bf16) into an fp32 accumulator (exact products, fp32 sums).
+//     q8_0 caches: the slice is rounded once per chunk to 16-bit integers
+//     n = round(q / s), s = max|q| / 32767 over the lane's dims of the head,
+//     so that |q - s n| <= s / 2; the block's 32 int8 values then meet them
+//     in exact integer dot products (dp2a: two int16 x int8 products per
+//     instruction, int32 sums), and the block scale d times s scales the
+//     integer sum once.  dp2a issues at the same multiply-add rate as fp32
+//     FMA, twice that of the mixed fp16-operand FMA, and reads the int8
+//     bytes as they are stored (no conversion).
 //   * softmax: per-head tile maxima by warp butterflies; the running maximum
 //     moves only when a tile exceeds it by more than 2^8 (all p stay <= 256);
 //     l is kept per lane and summed once per chunk.
@@ -103,6 +108,19 @@ __device__ __forceinline__ float mfma_hi(uint32_t a, uint32_t b, float c) {
     asm("{.reg .b16 a0,a1,b0,b1;\n mov.b32 {a0,a1}, %1;\n mov.b32 {b0,b1}, %2;\n"
         " fma.rn.f32.f16 %0, a1, b1, %3;}" : "=f"(r) : "r"(a), "r"(b), "f"(c));
   return r;
+}
+
+// c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) or b.byte2 / b.byte3 (hi),
+// signed, exact in int32.
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
 // Packed fp32 pairs.
@@ -270,8 +288,8 @@ __device__ __forceinline__ void fill_sparse(const DecodeArgs &a, int32_t jl, int
 template <int KVT, int G, int D>
 struct WarpState {
   using S = Shape<KVT, G, D>;
-  uint32_t q[G][S::QW];      // this lane's query slice, 16-bit pairs
-  float qb[G];               // q8_0: -1152 * sum of the slice (the offset term)
+  uint32_t q[G][S::QW];      // this lane's query slice, 16-bit pairs (q8_0: int16 pairs)
+  float qs[G];               // q8_0: s * scale_log2, the slice's integer step times the score scale
   uint64_t acc[G][S::DV / 2];// PV accumulators, fp32 pairs
   float m[G], l[G];          // running max (log2 units) and this lane's share of l
 };
@@ -283,11 +301,8 @@ template <int KVT, int G, int D>
 __device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const uint8_t *row, int g,
                                         int qq, float scale_log2, float *part) {
   using S = Shape<KVT, G, D>;
-  float sb[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) sb[h] = 0.f;
   if constexpr (KVT == KVO_Q8_0) {
-    constexpr int DL = S::DL;                            // 16 or 32 values, one block
+    constexpr int DL = S::DL;                            // 16 or 32 values of one block
     const int blk = (qq * DL) / 32, wo = (qq * DL) % 32;
     const int o = (g * S::NB + blk) * 34;                // block start in the row
     const float d = __half2float(__ushort_as_half(*(const uint16_t *)(row + o)));
@@ -297,30 +312,27 @@ __device__ __forceinline__ void qk_cell(const WarpState<KVT, G, D> &ws, const ui
     uint32_t w[DL / 4 + 1];
 #pragma unroll
     for (int i = 0; i <= DL / 4; ++i) w[i] = wp[i];
-    float sc[G];                                         // second chain per head
+    int acc[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) sc[h] = 0.f;
+    for (int h = 0; h < G; ++h) acc[h] = 0;
 #pragma unroll
     for (int i = 0; i < DL / 4; ++i) {
-      const uint32_t x = __funnelshift_r(w[i], w[i + 1], sh) ^ 0x80808080u;
-      const uint32_t k0 = __byte_perm(x, 0x64646464u, 0x4140);   // (1152 + x0, 1152 + x1)
-      const uint32_t k1 = __byte_perm(x, 0x64646464u, 0x4342);   // (1152 + x2, 1152 + x3)
+      const uint32_t x = __funnelshift_r(w[i], w[i + 1], sh);   // values 4i .. 4i+3
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        sb[h] = mfma_lo<KVT>(ws.q[h][2 * i], k0, sb[h]);
-        sc[h] = mfma_hi<KVT>(ws.q[h][2 * i], k0, sc[h]);
-        sb[h] = mfma_lo<KVT>(ws.q[h][2 * i + 1], k1, sb[h]);
-        sc[h] = mfma_hi<KVT>(ws.q[h][2 * i + 1], k1, sc[h]);
+        acc[h] = dp2a_lo(ws.q[h][2 * i], x, acc[h]);
+        acc[h] = dp2a_hi(ws.q[h][2 * i + 1], x, acc[h]);
       }
     }
     // explicit roundings (never contracted into FMAs): the same bits whatever
     // code the compiler generates around them
-    const float ds = __fmul_rn(d, scale_log2);
 #pragma unroll
-    for (int h = 0; h < G; ++h) part[h] = __fmul_rn(ds, __fadd_rn(__fadd_rn(sb[h], sc[h]), ws.qb[h]));
+    for (int h = 0; h < G; ++h) part[h] = __fmul_rn(__fmul_rn(d, ws.qs[h]), __int2float_rn(acc[h]));
   } else {
     const uint4 *kp = (const uint4 *)(row + g * S::HB + qq * S::DL * 2);
-    float sc[G];                                         // second chain per head
+    float sb[G], sc[G];                                  // two chains per head
+#pragma unroll
+    for (int h = 0; h < G; ++h) sb[h] = 0.f;
 #pragma unroll
     for (int h = 0; h < G; ++h) sc[h] = 0.f;
 #pragma unroll
@@ -569,19 +581,28 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const uint4 *qp = (const uint4 *)(qsrc + (size_t)h * D + qq * S::DL);
-      float sum = 0.f;
 #pragma unroll
       for (int i = 0; i < S::DL / 8; ++i) {
         const uint4 u = qp[i];
         ws.q[h][4 * i] = u.x; ws.q[h][4 * i + 1] = u.y;
         ws.q[h][4 * i + 2] = u.z; ws.q[h][4 * i + 3] = u.w;
-        if constexpr (KVT == KVO_Q8_0) {
-          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sum += h2f(uw[e] & 0xffff, QT) + h2f(uw[e] >> 16, QT);
-        }
       }
-      ws.qb[h] = __fmul_rn(-1152.f, sum);
+      if constexpr (KVT == KVO_Q8_0) {
+        // round the slice to 16-bit integers: step s = max|q| / 32767
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < S::QW; ++i)
+          amax = fmaxf(amax, fmaxf(fabsf(h2f(ws.q[h][i] & 0xffff, QT)), fabsf(h2f(ws.q[h][i] >> 16, QT))));
+        const float inv = amax > 0.f ? __fdiv_rn(32767.f, amax) : 0.f;
+#pragma unroll
+        for (int i = 0; i < S::QW; ++i) {
+          const float x0 = h2f(ws.q[h][i] & 0xffff, QT), x1 = h2f(ws.q[h][i] >> 16, QT);
+          const int n0 = max(-32767, min(32767, __float2int_rn(__fmul_rn(x0, inv))));
+          const int n1 = max(-32767, min(32767, __float2int_rn(__fmul_rn(x1, inv))));
+          ws.q[h][i] = ((uint32_t)n0 & 0xffffu) | ((uint32_t)n1 << 16);
+        }
+        ws.qs[h] = __fmul_rn(__fdiv_rn(amax, 32767.f), a.scale_log2);
+      }
       ws.m[h] = -INFINITY;
       ws.l[h] = 0.f;
 #pragma unroll
@@ -599,28 +620,35 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     bool valid = lane < n;
     if constexpr (SP)                        // staged picks are grouped inside the window already
       if (!a.offs) valid = valid && sparse_row(a, a.indices[(int64_t)it.b * a.max_ctx + it.sel0 + t0 + lane], false);
+    // tile maxima of all G heads: one butterfly with the heads interleaved, so
+    // that the G shuffle chains overlap instead of running one after another
+    float sv[G], tmax[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) tmax[h] = sv[h] = valid ? s[h] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < G; ++h) tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], o));
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float sv_h = valid ? s[h] : -INFINITY;
-      const float tmax = warp_max(sv_h);
-      if (tmax > ws.m[h] + 8.f) {            // warp-uniform: move the reference
-        const float alpha = exp2f(__fsub_rn(ws.m[h], tmax));
+      if (tmax[h] > ws.m[h] + 8.f) {         // warp-uniform: move the reference
+        const float alpha = exp2f(__fsub_rn(ws.m[h], tmax[h]));
         const uint64_t aa = pk2(alpha, alpha);
         ws.l[h] = __fmul_rn(ws.l[h], alpha);
 #pragma unroll
         for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = fmul2(ws.acc[h][i], aa);
-        ws.m[h] = tmax;
+        ws.m[h] = tmax[h];
       }
-      const float p = valid ? exp2f(__fsub_rn(sv_h, ws.m[h])) : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float p = valid ? exp2f(__fsub_rn(sv[h], ws.m[h])) : 0.f;
       ws.l[h] = __fadd_rn(ws.l[h], p);
       pbuf[lane * GP + h] = pk2(p, p);
     }
     __syncwarp();
   };
-  auto compute_pv = [&](const Item &it, int t, const uint8_t *sv) {
-    const int64_t t0 = it.cs + (int64_t)t * kTile;
-    const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
-    for (int c = 0; c < n; ++c) {
+  auto pv_cell = [&](const uint8_t *sv, int c) {
       uint64_t vp[S::DV / 2];
       v_cell<KVT, G, D>(sv + (int64_t)c * pitch, g, lane, vp);
       const uint64_t *pc = pbuf + c * GP;
@@ -635,6 +663,15 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
       for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int i = 0; i < S::DV / 2; ++i) ws.acc[h][i] = ffma2(pp[h], vp[i], ws.acc[h][i]);
+  };
+  auto compute_pv = [&](const Item &it, int t, const uint8_t *sv) {
+    const int64_t t0 = it.cs + (int64_t)t * kTile;
+    const int n = (int)(it.ce - t0 < kTile ? it.ce - t0 : kTile);
+    if (n == kTile) {                        // full tile: unrolled, so that the next cells'
+#pragma unroll 4                             // shared-memory reads overlap this cell's FMAs
+      for (int c = 0; c < kTile; ++c) pv_cell(sv, c);
+    } else {
+      for (int c = 0; c < n; ++c) pv_cell(sv, c);
     }
     __syncwarp();                            // pbuf reads done before the next tile's writes
   };
@@ -645,9 +682,16 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
 
   // Partial of an item: acc (this lane's dims), m, l.
   auto write_partial = [&](const Item &it) {
+    float lsums[G];                          // the G butterflies interleaved (same sums per head)
+#pragma unroll
+    for (int h = 0; h < G; ++h) lsums[h] = ws.l[h];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int h = 0; h < G; ++h) lsums[h] += __shfl_xor_sync(0xffffffffu, lsums[h], o);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float lsum = warp_sum(ws.l[h]);
+      const float lsum = lsums[h];
       if (SP && a.fold_in_split) {
         float x[S::DV];
 #pragma unroll

@@ -239,9 +239,12 @@ int kvo_gather_blocks(const void *k_plane, const void *v_plane, int64_t n_seq,
  *     out[b][h] = sum_j softmax_j(scale * q[b][h] . k[b][j][g]) v[b][j][g]
  * over cells j < ctx_len[b], computed as split-K flash-decoding: fixed
  * cell ranges (a function of max_ctx, batch and the device's SM count only)
- * give partial (m, l, acc) in fp32, combined in a fixed order.  Products
- * q * k are exact (16-bit x 16-bit, or 16-bit x int8) and summed in fp32;
- * P * V runs in fp32.  An empty context gives 0.
+ * give partial (m, l, acc) in fp32, combined in a fixed order.  F16/BF16
+ * caches: products q * k are exact (16-bit x 16-bit) and summed in fp32.
+ * Q8_0 caches: each query head's slice of dims is rounded once to 16-bit
+ * integers n with step s = max|q| / 32767 (|q - s n| <= s / 2), the block
+ * dot products with the int8 values are exact integer sums, scaled by d * s
+ * in fp32.  P * V runs in fp32.  An empty context gives 0.
  *
  * Cell row j of sequence b (n_kv_heads * head_dim values, or n_kv_heads *
  * head_dim/32 q8_0 blocks):
