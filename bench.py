@@ -997,7 +997,7 @@ def decode_source_sha256():
     """sha256 of the decode kernel source (the kernels the headline times)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("decode_impl.cuh", "decode.cu"):
+    for name in ("decode_impl.cuh", "decode_dispatch.cuh", "decode.cu"):
         with open(os.path.join(ROOT, "host_ram_tiered_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

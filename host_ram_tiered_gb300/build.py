@@ -17,10 +17,15 @@ ROOT = os.path.dirname(PKG)
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libkvo.so")
 
-SOURCES = ["kvo_abi.cu", "swap_gather.cu", "decode.cu", "decode_f16.cu", "decode_bf16.cu",
-           "decode_q8_0.cu", "prefill_mma.cu", "prefill_tc.cu",
-           "decode_noalloc.cu", "append.cu", "sparse_rows.cu", "vmm.cu"]
-HEADERS = [os.path.join(CSRC, "kvo_internal.cuh"), os.path.join(CSRC, "decode_impl.cuh"), os.path.join(ROOT, "include", "kvo.h")]
+# The decode kernels are instantiated in one unit per K/V dtype, head_dim and
+# mode (decode_k_*.cu), the slowest units first, so that they compile in parallel.
+DECODE_KERNEL_UNITS = [f"decode_k_{m}{dt}_{d}.cu" for m, dts in (("sp_", ("f16", "bf16")), ("", ("f16", "bf16", "q8_0")))
+                       for dt in dts for d in (128, 64)]
+SOURCES = DECODE_KERNEL_UNITS + ["prefill_tc.cu", "prefill_mma.cu", "kvo_abi.cu", "swap_gather.cu", "decode.cu",
+                                 "decode_f16.cu", "decode_bf16.cu", "decode_q8_0.cu", "decode_noalloc.cu",
+                                 "append.cu", "sparse_rows.cu", "vmm.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("kvo_internal.cuh", "decode_impl.cuh", "decode_dispatch.cuh")] + \
+    [os.path.join(ROOT, "include", "kvo.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

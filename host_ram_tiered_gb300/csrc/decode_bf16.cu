@@ -1,5 +1,5 @@
-// Decode kernels for bf16 K/V (see decode_impl.cuh).
-#include "decode_impl.cuh"
+// Tiered-decode dispatch for bf16 K/V (kernels: decode_k_bf16_*.cu).
+#include "decode_dispatch.cuh"
 
 namespace kvo {
 namespace dec {

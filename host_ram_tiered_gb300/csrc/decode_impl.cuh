@@ -40,7 +40,8 @@
 //   * PV: lane owns D/32 dims of every head; V is converted to fp32 (q8_0:
 //     exact d * x) and accumulated with packed f32x2 FMAs, weights (p, p)
 //     read from shared memory.
-// Instantiated per K/V dtype in decode_<dtype>.cu.
+// launch_d is instantiated per K/V dtype, head_dim and mode in the
+// decode_k_*.cu units; the dispatch over group shapes is decode_dispatch.cuh.
 #pragma once
 #include <cuda_fp16.h>
 #include <math.h>
@@ -1089,42 +1090,6 @@ cudaError_t launch_d(const DecodeArgs &a0, cudaStream_t st) {
   }
   cfg.gridDim = dim3(a.n_q_heads, a.batch);
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, a);
-}
-
-template <int KVT, int QT, int G, bool SP>
-cudaError_t launch_g(const DecodeArgs &a, cudaStream_t st) {
-  if (a.head_dim == 128) return launch_d<KVT, QT, G, 128, SP>(a, st);
-  return launch_d<KVT, QT, G, 64, SP>(a, st);
-}
-
-// Warps per kv head: the largest power of two w dividing the group with
-// n_kv_heads * w <= 8 warps, or <= 16 warps when each warp is then left with
-// at most two query heads; each warp takes group / w query heads.
-inline int warps_per_kv_head(const DecodeArgs &a) {
-  int w = 1;
-  while (a.group % (w * 2) == 0) {
-    const int warps = a.n_kv_heads * w * 2, heads = a.group / (w * 2);
-    if (warps > (heads <= 2 ? 16 : 8)) break;
-    w *= 2;
-  }
-  return w;
-}
-
-// The query type is the cache's 16-bit type (fp16 for a q8_0 cache); the
-// entry points reject other pairs.
-template <int KVT, bool SP = false>
-cudaError_t launch_kv(const DecodeArgs &a, cudaStream_t st) {
-  constexpr int QT = KVT == KVO_BF16 ? KVO_BF16 : KVO_F16;
-  switch (a.group / warps_per_kv_head(a)) {
-    case 1: return launch_g<KVT, QT, 1, SP>(a, st);
-    case 2: return launch_g<KVT, QT, 2, SP>(a, st);
-    case 3: return launch_g<KVT, QT, 3, SP>(a, st);
-    case 4: return launch_g<KVT, QT, 4, SP>(a, st);
-    case 5: return launch_g<KVT, QT, 5, SP>(a, st);
-    case 6: return launch_g<KVT, QT, 6, SP>(a, st);
-    case 7: return launch_g<KVT, QT, 7, SP>(a, st);
-    default: return launch_g<KVT, QT, 8, SP>(a, st);
-  }
 }
 
 }  // namespace dec

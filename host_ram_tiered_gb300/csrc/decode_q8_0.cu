@@ -1,5 +1,5 @@
-// Decode kernels for q8_0 K/V (see decode_impl.cuh).
-#include "decode_impl.cuh"
+// Tiered-decode dispatch for q8_0 K/V (kernels: decode_k_q8_0_*.cu).
+#include "decode_dispatch.cuh"
 
 namespace kvo {
 namespace dec {

@@ -13,7 +13,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "decode_impl.cuh"
+#include "decode_dispatch.cuh"
 
 namespace kvo {
 namespace dec {
