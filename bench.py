@@ -306,6 +306,9 @@ def swap_sweep_run(st, h2d, n, ce):
 # ----------------------------------------------------------------- q8_0 tiered decode
 
 DEC_HQ, DEC_HKV, DEC_D = 48, 8, 128
+# VRAM heads and host-tail sizes (cells) of the staged/direct decode sweep
+DEC_SWEEP_NS = (8192, 32768, 65536, 94208)
+DEC_SWEEP_TAILS = (1024, 2048, 4096, 8192, 16384, 32768)
 DEC_LS = (29696, 96256, 184320)
 DEC_NS = (8192, 94208)
 
@@ -730,8 +733,8 @@ def main(argv=None):
     if args.rows == "all" and world > 1:
         rows = {"head", "swap", "topk"} if args.split == "shards" else {"head"}
     elif args.rows == "all":
-        rows = {"head", "tiny", "swap", "swapsweep", "decode", "vmm", "topk", "prefill", "pfsweep", "append",
-                "sparse"}
+        rows = {"head", "tiny", "swap", "swapsweep", "decode", "decsweep", "vmm", "topk", "prefill", "pfsweep",
+                "append", "sparse"}
     else:
         rows = set(args.rows.split(","))
     timer = Timer()
@@ -756,7 +759,7 @@ def main(argv=None):
     clocks = Clocks()
     # ---- headline: q8_0 tiered decode at L = 184,320, N = 8,192, direct
     head = None
-    if "decode" in rows or "head" in rows or "vmm" in rows:
+    if "decode" in rows or "head" in rows or "vmm" in rows or "decsweep" in rows:
         st3 = dec_setup()
         bar()
         tot, ms = timer.run(lambda: dec_run(st3, 184320, 8192), K, W)
@@ -802,6 +805,17 @@ def main(argv=None):
                 results[f"q8_0_decode_L{L}_all_vram"] = {
                     "us_per_step": us_r, "hbm_gbs": db_r / (us_r * 1e-6) / 1e9,
                     "roofline_frac": db_r / (hbm * 1e9) / (us_r * 1e-6)}
+        if "decsweep" in rows:
+            # staged vs direct over the size of the host tail, at both VRAM splits
+            for N in DEC_SWEEP_NS:
+                for tail in DEC_SWEEP_TAILS:
+                    L = N + tail
+                    for staging in (False, True):
+                        tot, _ = timer.run(lambda: dec_run(st3, L, N, staging=staging), K, W)
+                        us_r = max_over_ranks(tot, world) / K * 1e3
+                        hb_r, _ = dec_bytes(L, N)
+                        results[f"decsweep_N{N}_tail{tail}_{'staged' if staging else 'direct'}"] = {
+                            "us_per_step": us_r, "host_gbs": hb_r / (us_r * 1e-6) / 1e9}
         if "vmm" in rows:
             # the headline decode over one VMM range per plane (host-NUMA tail)
             vm = vmm_setup(st3)
@@ -1021,7 +1035,7 @@ def profiled_traffic():
 def gpu_launch_count(K, rows):
     """Kernels of libkvo launched in the timed regions (own kernels only)."""
     n = 0
-    if "decode" in rows or "head" in rows or "vmm" in rows:
+    if "decode" in rows or "head" in rows or "vmm" in rows or "decsweep" in rows:
         n += 2 * K * 2                             # headline decode + its e2e: split + combine
     if "vmm" in rows and VMM_RAN[0]:
         # the headline decode over VMM tiers, direct and staged
@@ -1038,6 +1052,10 @@ def gpu_launch_count(K, rows):
             n += 2 * K
     elif "decode_vram" in rows:
         n += 2 * K                                 # the 184,320-cell all-VRAM decode
+    if "decsweep" in rows:
+        for N in DEC_SWEEP_NS:
+            for tail in DEC_SWEEP_TAILS:
+                n += K * sum(k.kvo_attn_decode_launches(1, N + tail, DEC_D, N, s) for s in (False, True))
     if "tiny" in rows:
         # swap both ways; decode direct + staged
         n += K * 2 + K * sum(k.kvo_attn_decode_launches(1, 1024, 128, 512, s) for s in (False, True))

@@ -13,10 +13,15 @@ constexpr int kMaxChunkTiles = 20;   // chunks of at most 640 cells
 void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *split_cells,
                      int *n_splits) {
   (void)head_dim;
-  // Chunk length C (32..640 cells, whole 32-cell tiles) minimising the tiles
+  // Chunk length C (32..640 cells, whole 32-cell tiles) minimising the work
   // of the busiest CTA when batch * ceil(max_ctx / C) chunks are dealt
-  // round-robin to one persistent CTA per SM; ties go to the longer chunk
-  // (fewer partials to combine).
+  // round-robin to one persistent CTA per SM: its waves times (the chunk's
+  // tiles plus a fixed cost of kChunkCostTiles per chunk -- the query load,
+  // the pipeline fill, the partial and its share of the combine); ties go to
+  // the longer chunk (fewer partials to combine).  Without the fixed cost a
+  // context such as 110,592 cells came out as 3,456 chunks of 32 cells
+  // (753 us against 212 us for 102,400 cells).
+  constexpr int64_t kChunkCostTiles = 2;
   const int64_t sms = num_sms();
   const int64_t bt = batch > 0 ? batch : 1;
   int64_t best_c = 32, best_cost = -1;
@@ -24,7 +29,7 @@ void decode_geometry(int64_t batch, int64_t max_ctx, int64_t head_dim, int *spli
     const int64_t c = tiles * 32;
     const int64_t chunks = (max_ctx + c - 1) / c;
     const int64_t waves = (bt * chunks + sms - 1) / sms;
-    const int64_t cost = (waves > 0 ? waves : 1) * tiles;
+    const int64_t cost = (waves > 0 ? waves : 1) * (tiles + kChunkCostTiles);
     if (best_cost < 0 || cost <= best_cost) {
       best_cost = cost;
       best_c = c;
@@ -146,3 +151,10 @@ int launch_decode_staged(DecodeArgs a, const void *k_host, const void *v_host, i
 }
 
 }  // namespace kvo
+
+// Measured staged/direct rule of the dense calls (include/kvo.h).
+extern "C" int kvo_dense_staging_worthwhile(int prefill, int64_t n_vram_cells, int64_t n_tail_cells) {
+  if (n_tail_cells <= 0 || n_vram_cells < 0) return 0;
+  if (prefill) return 1;
+  return n_vram_cells >= 65536 && 5 * n_tail_cells <= n_vram_cells ? 1 : 0;
+}

@@ -54,6 +54,7 @@ SIGNATURES = {
     "kvo_append_kv_tiered": (_int, [_vp, _vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _vp, _vp,
                                     _int, _i64, _i64, _vp]),
     "kvo_staging_worthwhile": (_int, [_i64, _i64, _i64, _i64]),
+    "kvo_dense_staging_worthwhile": (_int, [_int, _i64, _i64]),
     "kvo_attn_sparse_rows_workspace_bytes": (_sz, [_i64] * 8 + [_sz]),
     "kvo_attn_sparse_rows": (_int, [_vp, _int, _i64, _i64, _i64, _i64, _vp, _vp, _int, _i64, _i64,
                                     _vp, _i64, _vp, _i64, _f32, _vp, _sz, _i64, _vp, _vp, _sz, _vp]),
@@ -255,6 +256,10 @@ def kvo_attn_prefill_tiered(q, rows, q_pos0, n_q_heads, n_kv_heads, head_dim, k_
         _p(v_host), kv_dtype, ctx_len, n_vram_cells, scale, _p(arena), arena_bytes,
         rows_per_launch, _p(out), _p(workspace), workspace_bytes, _s(stream)),
         "kvo_attn_prefill_tiered")
+
+
+def kvo_dense_staging_worthwhile(prefill, n_vram_cells, n_tail_cells) -> bool:
+    return bool(load().kvo_dense_staging_worthwhile(int(prefill), n_vram_cells, n_tail_cells))
 
 
 def kvo_staging_worthwhile(rows, k_pad, num_pages_used, page_size) -> bool:

@@ -412,6 +412,34 @@ int kvo_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
                            int64_t page_size);
 
 /* ------------------------------------------------------------------------
+ * kvo_dense_staging_worthwhile -- the staged/direct rule of the dense calls
+ * (kvo_attn_decode_tiered with staging_k/v, kvo_attn_prefill_tiered with an
+ * arena), the measured counterpart of kvo_staging_worthwhile.
+ *
+ * llama.cpp PR #319 "tiered KV cache (--kv-vram-cells)" stages the used host
+ * rows through VRAM by DMA because SM reads of host memory were slow on its
+ * PCIe GPUs; on GB300 the SM kernels read the host tail at the full link
+ * rate, so the choice is measured (staged vs direct, GB300, over host tails
+ * of 1,024 - 176,128 cells and VRAM heads of 8,192 - 94,208 cells for the
+ * q8_0 decode of 48 q / 8 kv heads x 128, and over 1 - 2,048 query rows for
+ * the bf16 prefill of 32 q / 8 kv heads x 128 with a 32 MiB arena):
+ *   prefill != 0: staging wins at every measured row count (9.6 against
+ *     12.8 ms at 1 row, 5.6 against 63.7 ms at 256 rows): the direct prefill
+ *     kernel reads the tail once per query tile of each kv head, on few CTAs.
+ *     Returns 1 whenever n_tail_cells > 0.
+ *   prefill == 0 (decode, one query row per sequence): direct wins unless the
+ *     VRAM head is long enough to hide the copy of the tail: staging pays off
+ *     (by up to 21 %) when n_vram_cells >= 65,536 and 5 * n_tail_cells <=
+ *     n_vram_cells -- the copy then runs while the VRAM cells are decoded.
+ *     Elsewhere direct is faster by up to 20 %, or within a few per cent.
+ *     Against the measured table the rule's choice is never more than 7 %
+ *     slower than the faster mode.
+ * Returns 0 for n_tail_cells <= 0 and for negative sizes.  Pure host
+ * function.
+ * ---------------------------------------------------------------------- */
+int kvo_dense_staging_worthwhile(int prefill, int64_t n_vram_cells, int64_t n_tail_cells);
+
+/* ------------------------------------------------------------------------
  * kvo_attn_sparse_rows -- QSA sparse attention of query rows over a paged,
  * host-resident K/V cache, direct or staged through a VRAM arena.
  *

@@ -201,3 +201,33 @@ def test_shard_range_rejects_bad_ranks(kvo_lib):
         with pytest.raises(kvo.KvoError) as e:
             kvo.kvo_shard_range(*args)
         assert e.value.status == -1
+
+
+def _measured_staging_table():
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "measured", "dense_staging_gb300.txt")
+    rows = []
+    for line in open(path):
+        if line.strip() and not line.startswith("#"):
+            entry, r, n, t, d, s = line.split()
+            rows.append((entry, int(r), int(n), int(t), float(d), float(s)))
+    return rows
+
+
+def test_dense_staging_rule_picks_the_measured_faster_mode(kvo_lib):
+    # The rule's choice may cost at most 10 % against the faster mode of each measured call:
+    # where one mode was faster by more than that on the GB300, the rule must pick it.
+    rows = _measured_staging_table()
+    assert len(rows) >= 30
+    for entry, r, n_vram, n_tail, direct, staged in rows:
+        stage = kvo.kvo_dense_staging_worthwhile(entry == "prefill", n_vram, n_tail)
+        chosen, best = (staged if stage else direct), min(direct, staged)
+        assert chosen <= 1.10 * best, (entry, r, n_vram, n_tail, direct, staged, stage)
+
+
+def test_dense_staging_rule_edges(kvo_lib):
+    assert not kvo.kvo_dense_staging_worthwhile(True, 65536, 0)       # nothing in the host tier
+    assert not kvo.kvo_dense_staging_worthwhile(False, -1, 10)
+    assert kvo.kvo_dense_staging_worthwhile(True, 0, 1)              # prefill: any tail
+    assert kvo.kvo_dense_staging_worthwhile(False, 65535 + 1, 13107)  # decode: head hides the copy
+    assert not kvo.kvo_dense_staging_worthwhile(False, 65536, 13108)
+    assert not kvo.kvo_dense_staging_worthwhile(False, 65535, 1024)  # head too short

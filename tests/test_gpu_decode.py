@@ -88,18 +88,18 @@ def test_batch_with_ragged_and_empty_contexts():
 
 
 def test_staged_copy_in_parts_is_bit_identical():
-    # Four sequences of up to 30,000 cells: 188 chunks of 160 cells each, 752
-    # work items or five waves of CTAs, so the staged call decodes the chunks wholly in VRAM
-    # while the host tail is copied in four parts, and each part's chunks as
-    # it lands.  Ragged lengths: full, inside the VRAM head, ending inside a
-    # part, one short of full.
+    # Four sequences of up to 30,000 cells: 73 chunks of 416 cells each, 292
+    # work items or two waves of CTAs, so the staged call decodes the chunks wholly in VRAM
+    # while the host tail is copied in two parts, and each part's chunks as
+    # it lands (four launches: the VRAM chunks, two parts, the combine).  Ragged lengths:
+    # full, inside the VRAM head, ending inside a part, one short of full.
     g = synth.rng(31, 23)
     B, L, hq, hkv, d, N = 4, 30000, 8, 2, 128, 5000
     k, v = cells(B * L, hkv, d, oracle.BF16, g)
     q, qd = _q(B, hq, d, "bf16", g)
     lens = [L, 2500, 11111, L - 1]
     s = scale_for(d)
-    assert kvo.kvo_attn_decode_launches(B, L, d, N, 1) == 6
+    assert kvo.kvo_attn_decode_launches(B, L, d, N, 1) == 4
     tc = Tiered(k, v, N, batch=B)
     staged = run_decode(tc, qd, kvo.BF16, hq, hkv, d, kvo.BF16, _ctx(lens), s, staging=True)
     direct = run_decode(tc, qd, kvo.BF16, hq, hkv, d, kvo.BF16, _ctx(lens), s)

@@ -169,7 +169,7 @@ def test_noalloc_one_split_per_sequence_f16():
 def test_noalloc_staged_matches_direct_and_the_workspace_call_bit_for_bit():
     # Four sequences of 30,000 cells, 5,000 in VRAM: the partials of the regular splits fit,
     # so the no-workspace call uses the workspace call's splits; staged, it copies the tail
-    # in four parts on the library stream.  Two calls in a row, each bit-identical to the
+    # in two parts on the library stream.  Two calls in a row, each bit-identical to the
     # direct no-workspace call and to the staged workspace call.
     t = torch()
     B, L, hq, hkv, d, N = 4, 30000, 8, 2, 128, 5000
@@ -179,7 +179,7 @@ def test_noalloc_staged_matches_direct_and_the_workspace_call_bit_for_bit():
     lens = [L, 2500, 11111, L - 1]
     ctx = t.tensor(lens, dtype=t.int32, device="cuda")
     scale = 1 / math.sqrt(d)
-    assert kvo.kvo_attn_decode_launches(B, L, d, N, 1) == 6
+    assert kvo.kvo_attn_decode_launches(B, L, d, N, 1) == 4
     for call in range(2):
         q = synth.normal_bits((B, hq, d), "bf16", synth.rng(4325, 10 + call))
         qd = t.from_numpy(q.view(np.int16).reshape(-1).copy()).cuda()
