@@ -484,7 +484,8 @@ decode_split_kernel(const DecodeArgs a, int n_stages) {
     it.cs = it.ce = it.sel0 = 0;
     it.chunk = it.b = 0;
     if (w >= w_end) return it;
-    it.chunk = (int)(w / a.batch);
+    const int c = (int)(w / a.batch);
+    it.chunk = a.interleave ? ((c & 1) ? a.n_splits - 1 - (c >> 1) : (c >> 1)) : c;
     it.b = (int)(w % a.batch);
     int64_t ctx;
     if constexpr (SP) {                      // selection mode: the row's slots sel0 .. sel0 + ctx

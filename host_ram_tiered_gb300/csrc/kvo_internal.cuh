@@ -79,6 +79,11 @@ struct DecodeArgs {
   // phase 0: split kernel then combine; 1: split kernel only; 2: combine only.
   int64_t item_lo = 0, item_hi = -1;
   int phase = 0;
+  // Deal the chunks in the order 0, n-1, 1, n-2, ... instead of 0, 1, 2, ...
+  // (a direct call with host rows): the first wave then mixes VRAM chunks and
+  // host chunks, so the host link is busy while the VRAM chunks are decoded.
+  // Which CTA computes a chunk changes none of its bits.
+  int interleave = 0;
   // Running softmax state folded by the combine kernel (null: plain decode,
   // out = the normalised result).  init: this launch starts the state;
   // finalize: this launch writes out = acc / max(l, 1e-30).
