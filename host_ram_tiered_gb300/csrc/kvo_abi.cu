@@ -627,7 +627,10 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       const uint8_t *ks = (const uint8_t *)k_host + (size_t)(s.c0 - n_lo) * rb;
       const uint8_t *vs = (const uint8_t *)v_host + (size_t)(s.c0 - n_lo) * rb;
       int e = KVO_OK;
+      // the slot is free once both row blocks' launches of its previous bucket
+      // have finished (freed: the caller's stream, done2: the second stream)
       if (bi >= n_slots) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->freed[slot], 0), "cudaStreamWaitEvent");
+      if (!e && bi >= n_slots && two) e = cuda_status(cudaStreamWaitEvent(rg->side, rg->done2[slot], 0), "cudaStreamWaitEvent");
       if (!e) e = cuda_status(cudaMemcpyAsync((void *)k_slot, ks, bytes, cudaMemcpyDefault, rg->side), "arena copy K");
       if (!e) e = cuda_status(cudaMemcpyAsync((void *)v_slot, vs, bytes, cudaMemcpyDefault, rg->side), "arena copy V");
       if (!e) e = cuda_status(cudaEventRecord(rg->ready[slot], rg->side), "cudaEventRecord");
@@ -673,10 +676,7 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
     }
     if (tail && arena) {
       int e = KVO_OK;
-      if (two) {
-        e = cuda_status(cudaEventRecord(rg->done2[slot], rg->comp2), "cudaEventRecord");
-        if (!e) e = cuda_status(cudaStreamWaitEvent(st, rg->done2[slot], 0), "cudaStreamWaitEvent");
-      }
+      if (two) e = cuda_status(cudaEventRecord(rg->done2[slot], rg->comp2), "cudaEventRecord");
       if (!e) e = cuda_status(cudaEventRecord(rg->freed[slot], st), "cudaEventRecord");
       if (e) return e;
       ++bi;
