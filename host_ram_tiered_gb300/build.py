@@ -23,8 +23,8 @@ DECODE_KERNEL_UNITS = [f"decode_k_{m}{dt}_{d}.cu" for m, dts in (("sp_", ("f16",
                        for dt in dts for d in (128, 64)]
 SOURCES = DECODE_KERNEL_UNITS + ["prefill_tc.cu", "prefill_mma.cu", "kvo_abi.cu", "swap_gather.cu", "decode.cu",
                                  "decode_f16.cu", "decode_bf16.cu", "decode_q8_0.cu", "decode_noalloc.cu",
-                                 "append.cu", "sparse_rows.cu", "vmm.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("kvo_internal.cuh", "decode_impl.cuh", "decode_dispatch.cuh")] + \
+                                 "append.cu", "sparse_rows.cu", "vmm.cu", "selftest.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("kvo_internal.cuh", "decode_impl.cuh", "decode_dispatch.cuh", "sync.cuh")] + \
     [os.path.join(ROOT, "include", "kvo.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -48,7 +48,12 @@ Ring *ring(int which);               // nullptr when the streams cannot be creat
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Device-side error bits set by kernels that skipped an out-of-range item.
-enum DeviceErrorBits : uint32_t { kErrGatherSel = 1u, kErrPageTable = 2u };
+enum DeviceErrorBits : uint32_t {
+  kErrGatherSel = 1u,     // a gather selection outside its plane (skipped)
+  kErrPageTable = 2u,     // a page-table entry outside the planes (skipped)
+  kErrWaitTimeout = 4u,   // a bounded barrier wait gave up (the kernel wound down)
+  kErrSmemAlign = 8u      // a CTA could not align its shared memory and exited
+};
 uint32_t *device_error_word();       // address of the per-device word (nullptr on failure)
 
 // Launchers implemented in the kernel translation units.  They assume the

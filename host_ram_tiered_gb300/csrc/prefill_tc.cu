@@ -23,12 +23,14 @@
 // a row block.
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on timeout the
-// waiter sets kErrTimeout in the device error word and the CTA winds down.
+// waiter sets kErrWaitTimeout in the device error word and the CTA winds
+// down, after the copies and MMAs it issued have landed.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
 #include "kvo_internal.cuh"
+#include "sync.cuh"
 
 namespace kvo {
 
@@ -45,7 +47,6 @@ constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;   // S_q at q*128, O_q at 256 + q*128
 constexpr float kLazy = 8.0f;            // rescale when the max grows by > 2^8
-constexpr uint32_t kErrTimeout = 2u;
 
 // shared memory plan (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;                                 // NQ query tiles
@@ -55,53 +56,6 @@ constexpr int kOffBar = kOffV + kStages * kTile;         // mbarriers + TMEM slo
 constexpr int kSlack = 1024;                             // room to align the base to 1024 B
 constexpr int kSmemBytes = kOffBar + 256 + kSlack;
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait: false (and the error bit set) after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err) {
-  if (mbar_try(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 255) == 0 && globaltimer() - t0 > 2000000000ull) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             uint64_t *bar) {
@@ -329,7 +283,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   // misalignment, beyond which the CTA reports and exits.
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > (uint32_t)(kSlack - 256)) {
-    if (threadIdx.x == 0) atomicOr(P.err, kErrTimeout);
+    if (threadIdx.x == 0) atomicOr(P.err, kErrSmemAlign);
     return;
   }
   uint8_t *smem = smem_raw + pad;

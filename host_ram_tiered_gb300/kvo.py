@@ -33,6 +33,7 @@ SIGNATURES = {
     "kvo_status_string": (ctypes.c_char_p, [_int]),
     "kvo_last_error": (ctypes.c_char_p, []),
     "kvo_device_errors": (_int, [_vp, _int]),
+    "kvo_selftest_wait_timeout": (_int, [_u64, _vp]),
     "kvo_sub_block_ptrs": (_int, [_vp, _i64, _i64, _i64, _u64, _i64, _i64, _vp, _i64]),
     "kvo_shard_range": (_int, [_i64, _i64, _i64, _vp, _vp]),
     "kvo_copy_plan": (_int, [_vp] * 6 + [_i64, _int, _vp, _vp, _vp, _i64, _vp]),
@@ -131,6 +132,10 @@ def kvo_device_errors(clear: bool = True) -> int:
     bits = ctypes.c_uint32(0)
     _check(load().kvo_device_errors(ctypes.addressof(bits), int(clear)), "kvo_device_errors")
     return bits.value
+
+
+def kvo_selftest_wait_timeout(limit_ns, stream=None) -> None:
+    _check(load().kvo_selftest_wait_timeout(limit_ns, _s(stream)), "kvo_selftest_wait_timeout")
 
 
 def kvo_sub_block_ptrs(block_ids, n_ids, blocks_per_chunk, skip_count, base, row_stride_bytes,

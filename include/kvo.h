@@ -60,10 +60,26 @@ const char *kvo_status_string(int status);
 /* Detail of the last failing call on this host thread ("" if none). */
 const char *kvo_last_error(void);
 
-/* Bits set by kernels that skipped an out-of-range item (bit 0: a gather
- * selection outside its plane).  Synchronises the device; clears the bits
- * when `clear` is non-zero.  For tests and debugging, not for hot loops. */
+/* Bits set by kernels that met a condition the host could not check:
+ *   bit 0 (1): a gather selection outside its plane (the block was skipped);
+ *   bit 1 (2): a sparse-rows page-table entry outside the planes (its picks
+ *              counted as padding);
+ *   bit 2 (4): a bounded barrier wait gave up (about 2 s without progress;
+ *              the kernel wound down after its own copies and MMAs landed,
+ *              and its output is not valid);
+ *   bit 3 (8): a CTA could not align its shared memory and exited.
+ * Synchronises the device; clears the bits when `clear` is non-zero.  For
+ * tests and debugging, not for hot loops. */
 int kvo_device_errors(uint32_t *bits, int clear);
+
+/* kvo_selftest_wait_timeout -- runs the library's bounded barrier wait (the
+ * one every tensor-core prefill wait uses) on a barrier that nothing
+ * completes, with limit_ns in place of the kernels' ~2 s: the wait gives up,
+ * sets bit 2 of kvo_device_errors() and the kernel returns.  For testing the
+ * failure path without a fault; the context stays usable.  The pages have no
+ * counterpart.  Errors: KVO_ERR_ARG (limit_ns 0 or above 10 s),
+ * KVO_ERR_CUDA. */
+int kvo_selftest_wait_timeout(uint64_t limit_ns, void *stream);
 
 /* ------------------------------------------------------------------------
  * kvo_sub_block_ptrs -- host function, synchronous, no CUDA.

@@ -231,3 +231,10 @@ def test_dense_staging_rule_edges(kvo_lib):
     assert kvo.kvo_dense_staging_worthwhile(False, 65535 + 1, 13107)  # decode: head hides the copy
     assert not kvo.kvo_dense_staging_worthwhile(False, 65536, 13108)
     assert not kvo.kvo_dense_staging_worthwhile(False, 65535, 1024)  # head too short
+
+
+def test_selftest_wait_timeout_rejects_bad_limits(kvo_lib):
+    for limit in (0, 10_000_000_001):
+        with pytest.raises(kvo.KvoError) as e:
+            kvo.kvo_selftest_wait_timeout(limit)
+        assert e.value.status == -1
