@@ -668,8 +668,14 @@ int kvo_attn_prefill_tiered(const void *q, int64_t rows, int64_t q_pos0, int64_t
       } else if (arena) {
         // arena bucket: tensor cores fed by TMA
         e = launch_prefill_tc(a, k_slot, v_slot, s.c1 - s.c0, ls);
+      } else if ((int64_t)a.rows * group >= 512) {
+        // direct, enough query tiles to fill the GPU: the host tail read in
+        // place, tensor cores fed by plain loads (one producer warp per CTA)
+        e = launch_prefill_tc_host(a, ls);
       } else {
-        // direct: host tail read through the mapping by the mma.sync kernel
+        // direct, few query rows: the tensor-core kernel would run one CTA per
+        // kv head, each bound by its one producer warp; the mma.sync kernel's
+        // 16-position tiles give 4x the CTAs, each loading with all threads
         e = launch_prefill(a, ls);
       }
       if (e) return e;

@@ -174,6 +174,9 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t st);  // kvo_status (mma.s
 // rows (c - a.hi_origin) of k_seg / v_seg (seg_rows rows).
 int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg, int64_t seg_rows,
                       cudaStream_t st);
+// tcgen05 path for a host-memory segment (rows (c - a.hi_origin) of a.k_hi /
+// a.v_hi), filled with plain loads.
+int launch_prefill_tc_host(const PrefillArgs &a, cudaStream_t st);
 
 struct AppendArgs {
   const uint8_t *k_new, *v_new;  // [n_new][n_kv_heads][head_dim] of src_dtype

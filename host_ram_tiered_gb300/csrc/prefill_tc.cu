@@ -7,8 +7,12 @@
 // in tiles of 128 cells.
 //   warps 0-3          : softmax + epilogue of tile A (thread = row = TMEM lane)
 //   warps 4-7          : softmax + epilogue of tile B
-//   warp 8  (one lane) : TMA producer, K and V tiles (two 64-dim SW128 boxes
-//                        each) into separate 2-stage rings
+//   warp 8             : producer, K and V tiles into separate 2-stage rings:
+//                        device segments by TMA (one lane, two 64-dim SW128
+//                        boxes per tile); host-memory segments (the tail read
+//                        in place) by the 32 lanes with plain 16-byte loads
+//                        stored in the same SW128 layout -- TMA never reads
+//                        host memory
 //   warp 9  (one lane) : MMA issuer; the warp owns the TMEM allocation.
 // TMEM: S_A, S_B (fp32, 128 columns each) and O_A, O_B (fp32, 128 each).
 // The softmax writes P back over its S columns as a pair hi + lo of the input
@@ -26,6 +30,7 @@
 // waiter sets kErrWaitTimeout in the device error word and the CTA winds
 // down, after the copies and MMAs it issued have landed.
 #include <cuda.h>
+#include <cstring>
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -270,7 +275,35 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
 struct TcParams {
   PrefillArgs a;
   uint32_t *err;
+  // non-null: the segment's K/V rows are host memory, row (c - a.hi_origin)
+  // at host_k / host_v (the tensor maps are unused)
+  const uint8_t *host_k, *host_v;
 };
+
+// Host-memory producer: the 128 cell rows [t0, t0 + 128) of kv head g into a
+// tile of two SW128 halves, 16-byte loads kHostBatch at a time per lane;
+// rows at or past c_end are zero (finite values for the masked PV).
+constexpr int kHostBatch = 16;
+
+__device__ __forceinline__ void host_tile(const uint8_t *base, int64_t row_bytes, int64_t hi_origin, int g,
+                                          int64_t t0, int64_t c_end, uint8_t *dst, int lane) {
+  constexpr int kChunks = BN * 16;                   // 16-byte chunks of the tile (256 B per row)
+  for (int i0 = 0; i0 < kChunks; i0 += 32 * kHostBatch) {
+    int4 v[kHostBatch];
+#pragma unroll
+    for (int u = 0; u < kHostBatch; ++u) {
+      const int i = i0 + u * 32 + lane, r = i >> 4, c = i & 15;
+      const int64_t cell = t0 + r;
+      v[u] = cell < c_end ? *((const int4 *)(base + (cell - hi_origin) * row_bytes + g * (HD * 2)) + c)
+                          : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kHostBatch; ++u) {
+      const int i = i0 + u * 32 + lane, r = i >> 4, c = i & 15;
+      *(int4 *)(dst + sw128(r, c)) = v[u];
+    }
+  }
+}
 
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -333,7 +366,30 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == 8 && P.host_k) {
+    // ---------------------------------------------------------------- host-memory producer
+    // The 32 lanes fill each K and V stage with plain loads; after its stores
+    // every lane fences them into the async proxy, then lane 0 arrives on the
+    // stage's full barrier (nothing is in flight between tiles, so a failed
+    // wait leaves no copy to drain).
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int s = j % kStages;
+      const int64_t t0 = a.c0 + (int64_t)j * BN;
+      if (j >= kStages) ok = __all_sync(0xffffffffu, mbar_wait(&empty_k[s], ((j / kStages) - 1) & 1, P.err));
+      if (!ok) break;
+      host_tile(P.host_k, a.row_bytes, a.hi_origin, g, t0, c_end, smem + kOffK + s * kTile, lane);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_k[s]);
+      if (j >= kStages) ok = __all_sync(0xffffffffu, mbar_wait(&empty_v[s], ((j / kStages) - 1) & 1, P.err));
+      if (!ok) break;
+      host_tile(P.host_v, a.row_bytes, a.hi_origin, g, t0, c_end, smem + kOffV + s * kTile, lane);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full_v[s]);
+    }
+  } else if (warp == 8) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0 && n_tiles > 0) {
       bool ok = true;
@@ -665,6 +721,23 @@ cudaError_t launch_dt(const CUtensorMap &mk, const CUtensorMap &mv, const TcPara
 
 }  // namespace
 
+// Launch over a host-memory segment (the tail read in place): cells [a.c0,
+// a.c1) are rows (c - a.hi_origin) of a.k_hi / a.v_hi, loaded by the producer
+// warp with plain loads.
+int launch_prefill_tc_host(const PrefillArgs &a, cudaStream_t st) {
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  TcParams p;
+  p.a = a;
+  p.err = device_error_word();
+  if (!p.err) return fail(KVO_ERR_CUDA, "device error word unavailable");
+  p.host_k = a.k_hi;
+  p.host_v = a.v_hi;
+  cudaError_t e = a.dtype == KVO_BF16 ? launch_dt<KVO_BF16>(unused, unused, p, st)
+                                      : launch_dt<KVO_F16>(unused, unused, p, st);
+  return cuda_status(e, "tcgen05 prefill launch (host segment)");
+}
+
 // Launch over a device-resident segment: cells [a.c0, a.c1) are rows
 // (c - a.hi_origin) of the buffers k_seg / v_seg, which hold seg_rows rows.
 int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg, int64_t seg_rows,
@@ -679,6 +752,7 @@ int launch_prefill_tc(const PrefillArgs &a, const void *k_seg, const void *v_seg
   p.a = a;
   p.err = device_error_word();
   if (!p.err) return fail(KVO_ERR_CUDA, "device error word unavailable");
+  p.host_k = p.host_v = nullptr;
   cudaError_t e = a.dtype == KVO_BF16 ? launch_dt<KVO_BF16>(mk, mv, p, st) : launch_dt<KVO_F16>(mk, mv, p, st);
   return cuda_status(e, "tcgen05 prefill launch");
 }

@@ -86,6 +86,24 @@ def test_first_row_sees_one_cell():
     assert normwise_rel_err(out, ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("hq,hkv,dt,R", [(8, 2, oracle.BF16, 160), (16, 2, oracle.F16, 80),
+                                          (4, 4, oracle.BF16, 520)])
+def test_direct_tensor_core_path_over_host_rows(hq, hkv, dt, R):
+    # rows x group >= 512: the host tail is read in place by the tensor-core kernel's producer
+    # warp (plain loads into the swizzled tiles); a ragged last tile and rows whose causal range
+    # ends inside the tail
+    G = hq // hkv
+    assert R * G >= 512
+    g = synth.rng(1240, hq * 1000 + R)
+    L, N, d = 1100, 300, 128
+    pos0 = L - R - 7                                    # the last 7 cells lie past every row
+    tc = Tiered(*cells(L, hkv, d, dt, g), N)
+    q = synth.normal_bits((R, hq, d), "f16" if dt == oracle.F16 else "bf16", g)
+    out = _prefill(tc, q, R, pos0, hq, hkv, d, dt, L, 0.09, 0, R)
+    ref = _ref(tc, q, R, pos0, hq, hkv, d, dt, L, 0.09)
+    assert normwise_rel_err(out, ref) <= REL_TOL
+
+
 def test_prefill_argument_errors():
     t = torch()
     x = t.zeros(1 << 16, dtype=t.uint8, device="cuda")
