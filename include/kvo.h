@@ -439,9 +439,10 @@ int kvo_staging_worthwhile(int64_t rows, int64_t k_pad, int64_t num_pages_used,
  * of 1,024 - 176,128 cells and VRAM heads of 8,192 - 94,208 cells for the
  * q8_0 decode of 48 q / 8 kv heads x 128, and over 1 - 2,048 query rows for
  * the bf16 prefill of 32 q / 8 kv heads x 128 with a 32 MiB arena):
- *   prefill != 0: staging wins at every measured row count (9.6 against
- *     12.8 ms at 1 row, 5.6 against 63.7 ms at 256 rows): the direct prefill
- *     kernel reads the tail once per query tile of each kv head, on few CTAs.
+ *   prefill != 0: staging wins at every measured row count (8.7 against
+ *     12.9 ms at 1 row, 5.5 against 25.9 ms at 256 rows, 9.5 against 126 ms
+ *     at 2,048 rows): the direct kernels read the tail once per query tile of
+ *     each kv head, on few CTAs at small row counts.
  *     Returns 1 whenever n_tail_cells > 0.
  *   prefill == 0 (decode, one query row per sequence): direct wins unless the
  *     VRAM head is long enough to hide the copy of the tail: staging pays off
