@@ -352,13 +352,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // Query tiles (all threads): row r of tile q = position q*PB + r/G, head g*G + r%G.
-  for (int i = tid; i < NQ * BM * 16; i += kThreads) {
-    const int q = i / (BM * 16), rr = (i >> 4) % BM, c = i & 15;
-    const int pi = q * PB + rr / G, hh = rr % G;
-    int4 v = make_int4(0, 0, 0, 0);
-    if (pi < n_pos)
-      v = *((const int4 *)(a.q + ((size_t)(i0 + pi) * a.n_q_heads + g * G + hh) * HD) + c);
-    *(int4 *)(smem + kOffQ + q * kTile + sw128(rr, c)) = v;
+  // Loads go out kQBatch at a time per thread, so that their latencies overlap.
+  constexpr int kQChunks = NQ * BM * 16, kQBatch = 8;
+  for (int j0 = tid; j0 < kQChunks; j0 += kThreads * kQBatch) {
+    int4 v[kQBatch];
+#pragma unroll
+    for (int u = 0; u < kQBatch; ++u) {
+      const int i = j0 + u * kThreads;
+      const int q = i / (BM * 16), rr = (i >> 4) % BM, c = i & 15;
+      const int pi = q * PB + rr / G, hh = rr % G;
+      v[u] = make_int4(0, 0, 0, 0);
+      if (i < kQChunks && pi < n_pos)
+        v[u] = *((const int4 *)(a.q + ((size_t)(i0 + pi) * a.n_q_heads + g * G + hh) * HD) + c);
+    }
+#pragma unroll
+    for (int u = 0; u < kQBatch; ++u) {
+      const int i = j0 + u * kThreads;
+      const int q = i / (BM * 16), rr = (i >> 4) % BM, c = i & 15;
+      if (i < kQChunks) *(int4 *)(smem + kOffQ + q * kTile + sw128(rr, c)) = v[u];
+    }
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // Q visible to the tensor core
   tc_fence_before();
@@ -511,16 +523,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       l = a.ml[row_idx * 2 + 1];
     }
     if (!a.init) {
-      // load the running accumulator into TMEM (rows past the launch get zeros)
-      float v[32];
+      // load the running accumulator into TMEM (rows past the launch get zeros),
+      // 64 columns' loads in flight at a time
+      float v[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 4; c += 2) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
+        for (int i = 0; i < 64; i += 4) {
           float4 x = row_ok ? *(const float4 *)(a.acc + row_idx * HD + c * 32 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
           v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
         }
         tmem_st32(o_addr + c * 32, v);
+        tmem_st32(o_addr + (c + 1) * 32, v + 32);
       }
       tmem_wait_st();
     }
