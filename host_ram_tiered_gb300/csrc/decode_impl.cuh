@@ -191,14 +191,38 @@ __device__ __forceinline__ const int4 *row_src(const DecodeArgs &a, int b, int64
 }
 
 // Cell rows [c0, c0 + n) of sequence b, K and V, into one stage: asynchronous
-// 16-byte copies, all in flight at once (device-resident rows only).
+// 16-byte copies, all in flight at once (device-resident rows only).  A tile
+// within one tier (the usual case) walks its chunks from one base pointer
+// per plane with incremental (row, chunk) indices; a tile that straddles the
+// VRAM/tail boundary takes each row's tier.
 __device__ __forceinline__ void fill_async(const DecodeArgs &a, int b, int64_t c0, int n,
                                            uint8_t *sk, uint8_t *sv, int64_t pitch, FastDiv cpr) {
-  const int total = n * (int)cpr.d;
-  for (int i = threadIdx.x; i < 2 * total; i += blockDim.x) {
+  const int cprd = (int)cpr.d;
+  const int total = n * cprd;
+  const int T = blockDim.x;
+  if (c0 + n <= a.n_vram || c0 >= a.n_vram) {
+    const int64_t rb = a.row_bytes;
+    const uint8_t *kb = (const uint8_t *)row_src(a, b, c0, false), *vb = (const uint8_t *)row_src(a, b, c0, true);
+    int r = (int)fdiv((uint32_t)threadIdx.x, cpr), ch = (int)threadIdx.x - r * cprd;
+    const int dr = (int)fdiv((uint32_t)T, cpr), dch = T - dr * cprd;
+    for (int i = threadIdx.x; i < total; i += T) {
+      const uint32_t so = (uint32_t)(r * pitch + ch * 16);
+      const int64_t go = (int64_t)r * rb + ch * 16;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sk) + so), "l"(kb + go) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sv) + so), "l"(vb + go) : "memory");
+      r += dr;
+      ch += dch;
+      if (ch >= cprd) {
+        ch -= cprd;
+        ++r;
+      }
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < 2 * total; i += T) {
     const bool is_v = i >= total;
     const int k = is_v ? i - total : i;
-    const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
+    const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * cprd;
     const uint32_t dst = smem_addr((is_v ? sv : sk) + r * pitch + ch * 16);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
                  "l"(row_src(a, b, c0 + r, is_v) + ch)
