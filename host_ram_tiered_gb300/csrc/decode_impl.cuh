@@ -234,9 +234,45 @@ __device__ __forceinline__ void fill_async(const DecodeArgs &a, int b, int64_t c
 // eight per thread in flight.
 __device__ __forceinline__ void fill_sync(const DecodeArgs &a, int b, int64_t c0, int n,
                                           uint8_t *sk, uint8_t *sv, int64_t pitch, FastDiv cpr) {
-  const int total = n * (int)cpr.d;
+  const int cprd = (int)cpr.d;
+  const int total = n * cprd;
   const int nthr = blockDim.x;
   constexpr int kBatch = 8;
+  if (c0 + n <= a.n_vram || c0 >= a.n_vram) {
+    // one tier: K and V chunk i together, kBatch / 2 chunk pairs in flight,
+    // (row, chunk) indices advanced incrementally as in fill_async
+    constexpr int kPairs = kBatch / 2;
+    const int64_t rb = a.row_bytes;
+    const uint8_t *kb = (const uint8_t *)row_src(a, b, c0, false), *vb = (const uint8_t *)row_src(a, b, c0, true);
+    int r = (int)fdiv((uint32_t)threadIdx.x, cpr), ch = (int)threadIdx.x - r * cprd;
+    const int dr = (int)fdiv((uint32_t)nthr, cpr), dch = nthr - dr * cprd;
+    for (int i0 = threadIdx.x; i0 < total; i0 += kPairs * nthr) {
+      int4 kv[kPairs], vv[kPairs];
+      uint32_t so[kPairs];
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        so[u] = (uint32_t)(r * pitch + ch * 16);
+        if (i0 + u * nthr < total) {
+          const int64_t go = (int64_t)r * rb + ch * 16;
+          kv[u] = *(const int4 *)(kb + go);
+          vv[u] = *(const int4 *)(vb + go);
+        }
+        r += dr;
+        ch += dch;
+        if (ch >= cprd) {
+          ch -= cprd;
+          ++r;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u)
+        if (i0 + u * nthr < total) {
+          *(int4 *)(sk + so[u]) = kv[u];
+          *(int4 *)(sv + so[u]) = vv[u];
+        }
+    }
+    return;
+  }
   for (int base = 0; base < 2 * total; base += kBatch * nthr) {
     int4 v[kBatch];
 #pragma unroll
@@ -245,7 +281,7 @@ __device__ __forceinline__ void fill_sync(const DecodeArgs &a, int b, int64_t c0
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
-        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
+        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * cprd;
         v[u] = row_src(a, b, c0 + r, is_v)[ch];
       }
     }
@@ -255,7 +291,7 @@ __device__ __forceinline__ void fill_sync(const DecodeArgs &a, int b, int64_t c0
       if (i < 2 * total) {
         const bool is_v = i >= total;
         const int k = is_v ? i - total : i;
-        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * (int)cpr.d;
+        const int r = (int)fdiv((uint32_t)k, cpr), ch = k - r * cprd;
         *(int4 *)((is_v ? sv : sk) + r * pitch + ch * 16) = v[u];
       }
     }
