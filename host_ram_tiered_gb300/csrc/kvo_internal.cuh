@@ -52,7 +52,8 @@ enum DeviceErrorBits : uint32_t {
   kErrGatherSel = 1u,     // a gather selection outside its plane (skipped)
   kErrPageTable = 2u,     // a page-table entry outside the planes (skipped)
   kErrWaitTimeout = 4u,   // a bounded barrier wait gave up (the kernel wound down)
-  kErrSmemAlign = 8u      // a CTA could not align its shared memory and exited
+  kErrSmemAlign = 8u,     // a CTA could not align its shared memory and exited
+  kErrF16Range = 16u      // a bf16 V value outside fp16's range met the fp16 PV product
 };
 uint32_t *device_error_word();       // address of the per-device word (nullptr on failure)
 

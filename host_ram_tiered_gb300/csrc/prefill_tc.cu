@@ -14,9 +14,11 @@
 //                        stored in the same SW128 layout -- TMA never reads
 //                        host memory
 //   warp 9  (one lane) : MMA issuer; the warp owns the TMEM allocation.
+//   warps 10-11        : bf16 caches only: each landed V tile rewritten in
+//                        place as fp16 before its PV is issued
 // TMEM: S_A, S_B (fp32, 128 columns each) and O_A, O_B (fp32, 128 each).
-// The softmax writes P back over its S columns as a pair hi + lo of the input
-// type (so the product keeps ~16 bits of P), and O += P V is issued with P
+// The softmax writes P back over its S columns as fp16 (11 significant bits;
+// P is in [0, 2^8]), and O += P V is issued once, both operands fp16, with P
 // read from TMEM.  Issue order S_A S_B | PV_A S_A' PV_B S_B' | ... keeps the
 // tensor core busy with one tile while the other tile's softmax runs.
 // The running max is rescaled lazily (only when the tile max exceeds the
@@ -45,7 +47,7 @@ constexpr int BM = 128;                  // MMA rows per query tile
 constexpr int NQ = 2;                    // query tiles per CTA
 constexpr int BN = 128;                  // cells per tile
 constexpr int HD = 128;                  // head dim
-constexpr int kThreads = 320;            // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kThreads = 384;            // warps 0-7 softmax, 8 TMA, 9 MMA, 10-11 V conversion
 constexpr int kHalf = BM * 128;          // one SW128 half tile: 128 rows x 128 B = 16 KiB
 constexpr int kTile = 2 * kHalf;         // 128 rows x 256 B
 constexpr int kStages = 2;
@@ -232,16 +234,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
-template <int DT>
-__device__ __forceinline__ float2 unpack2(uint32_t u) {
-  if constexpr (DT == KVO_BF16) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-  } else {
-    __half2 h = *reinterpret_cast<__half2 *>(&u);
-    return __half22float2(h);
-  }
-}
-
 // 2^x on the SFU (PTX ex2.approx.ftz.f32; 2^-inf = +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -249,21 +241,10 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Split p0, p1 into a hi pair and a lo pair of the 16-bit input type with
-// p ~= hi + lo to ~2^-16 relative.  bf16: hi is p truncated to its upper 16
-// bits (exact in fp32), lo the rounded residual.  f16: hi rounded, lo the
-// rounded residual.
-template <int DT>
-__device__ __forceinline__ void split2(float p0, float p1, uint32_t &hi, uint32_t &lo) {
-  if constexpr (DT == KVO_BF16) {
-    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(b0), "r"(b1));
-    lo = pack2<DT>(p0 - __uint_as_float(b0 & 0xffff0000u), p1 - __uint_as_float(b1 & 0xffff0000u));
-  } else {
-    hi = pack2<DT>(p0, p1);
-    const float2 hf = unpack2<DT>(hi);
-    lo = pack2<DT>(p0 - hf.x, p1 - hf.y);
-  }
+// Two bf16 values (one word) -> the same two values as fp16, rounded to
+// nearest (bf16 -> fp32 is exact: the bits shifted up).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack2<KVO_F16>(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Byte offset of 16-byte chunk c (0..15 across the 256-byte row) of row r in
@@ -329,7 +310,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   uint64_t *p_full = bar + 10;             // [NQ] softmax -> MMA (128 arrivals)
   uint64_t *o_done = bar + 12;             // [NQ] MMA -> softmax (PV of tile q finished)
   uint64_t *fin = bar + 14;                // MMA teardown
-  uint32_t *tmem_slot = (uint32_t *)(bar + 15);
+  uint64_t *conv_v = bar + 16;             // [kStages] converters -> MMA (bf16: V tile now fp16)
+  uint32_t *tmem_slot = (uint32_t *)(bar + 18);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.y;
@@ -342,6 +324,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   if (tid == 0) {
     for (int i = 0; i < 14; ++i) mbar_init(&bar[i], (i == 10 || i == 11) ? BM : 1);
     mbar_init(fin, 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&conv_v[s], 2);   // one arrival per converter warp
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 9) {
@@ -436,7 +419,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t id_s = idesc<DT>(false);
-      constexpr uint32_t id_o = idesc<DT>(true);
+      constexpr uint32_t id_o = idesc<KVO_F16>(true);       // P and V both fp16
+      // V tile ready for PV: landed (fp16 caches) or converted (bf16 caches)
+      uint64_t *ready_v = DT == KVO_BF16 ? conv_v : full_v;
       uint32_t o_acc = a.init ? 0u : 1u;
       bool ok = true;
       // S_q(j) = Q_q K_j^T into the S columns of tile q
@@ -451,21 +436,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
         }
         umma_commit(&s_full[q]);
       };
-      // O_q += P_q V_j with P_q (hi and lo pairs over the S columns) read from TMEM
+      // O_q += P_q V_j with P_q (fp16 pairs over the S columns) read from TMEM
       auto issue_pv = [&](int q, int j) {
         const uint32_t v_base = smem_u32(smem + kOffV + (j % kStages) * kTile);
         const uint32_t d_o = tmem + kColO + q * 128;
-        // cells 16kk..16kk+15: hi pairs at columns 32*(kk/2) + 8*(kk%2), lo 16 further
+        // cells 16kk..16kk+15: the pairs in columns 8kk..8kk+7
         const uint32_t p_base = tmem + kColS + q * 128;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
-          umma_ts(d_o, p_base + 32 * (kk >> 1) + 8 * (kk & 1), bd, id_o, (kk > 0) || o_acc);
-        }
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = sdesc(v_base + kk * 16 * 128, kHalf, 1024);
-          umma_ts(d_o, p_base + 32 * (kk >> 1) + 16 + 8 * (kk & 1), bd, id_o, 1u);
+          umma_ts(d_o, p_base + 8 * kk, bd, id_o, (kk > 0) || o_acc);
         }
         umma_commit(&o_done[q]);
       };
@@ -478,7 +458,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       }
       for (int j = 0; j < n_tiles && ok; ++j) {
         const int jn = j + 1;
-        ok = mbar_wait(&full_v[j % kStages], (j / kStages) & 1, P.err);
+        ok = mbar_wait(&ready_v[j % kStages], (j / kStages) & 1, P.err);
         if (!ok) break;
         ok = mbar_wait(&p_full[0], j & 1, P.err);
         if (!ok) break;
@@ -504,6 +484,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       // all issued tensor-core work has finished once this arrives
       umma_commit(fin);
       mbar_wait(fin, 0, P.err);
+    }
+  } else if (warp >= 10) {
+    // ---------------------------------------------------------------- V conversion (bf16)
+    // Each landed V tile is rewritten in place as fp16 (the swizzle moves
+    // whole 16-byte chunks, so only the values change), fenced into the async
+    // proxy and handed to the MMA warp.  bf16 -> fp16 is exact for magnitudes
+    // in [2^-14, 65504]; smaller ones round to fp16's subnormal grid (absolute
+    // error <= 2^-25); one that becomes infinite (65520 and above, or an
+    // infinite input) sets kErrF16Range.
+    if constexpr (DT == KVO_BF16) {
+      constexpr int kChunks = kTile / 16, kLanes = 64, kBatch = 8;
+      const int cl = (warp - 10) * 32 + lane;
+      __half2 vmax = __float2half2_rn(0.f);                   // max |v| as fp16
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full_v[s], (j / kStages) & 1, P.err));
+        if (!ok) break;
+        uint4 *vt = (uint4 *)(smem + kOffV + s * kTile);
+#pragma unroll 1
+        for (int i0 = cl; i0 < kChunks; i0 += kLanes * kBatch) {
+          uint4 u[kBatch];
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) u[k] = vt[i0 + k * kLanes];
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) {
+            u[k].x = bf16x2_to_f16x2(u[k].x);
+            u[k].y = bf16x2_to_f16x2(u[k].y);
+            u[k].z = bf16x2_to_f16x2(u[k].z);
+            u[k].w = bf16x2_to_f16x2(u[k].w);
+            const __half2 m01 = __hmax2(__habs2(*(const __half2 *)&u[k].x), __habs2(*(const __half2 *)&u[k].y));
+            const __half2 m23 = __hmax2(__habs2(*(const __half2 *)&u[k].z), __habs2(*(const __half2 *)&u[k].w));
+            vmax = __hmax2(vmax, __hmax2(m01, m23));
+          }
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) vt[i0 + k * kLanes] = u[k];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_v[s]);
+      }
+      const uint32_t mb = *(const uint32_t *)&vmax;
+      if ((mb & 0x7fffu) >= 0x7c00u || ((mb >> 16) & 0x7fffu) >= 0x7c00u) atomicOr(P.err, kErrF16Range);
     }
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
@@ -579,33 +602,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       if (mine) m_used = mt;
       const float nref = m_used == -INFINITY ? 0.f : -m_used;
       // P = 2^(s*scale - ref) from the registers (a masked score is -inf and
-      // gives +0), written back over the S columns it came from: chunk c
-      // (cells 32c..32c+31) -> hi pairs in columns 32c..32c+15, lo pairs in
-      // 32c+16..32c+31.  The PV of the previous tile read these columns before
-      // this tile's S was written into them.  Arguments, sums and residuals
-      // run as packed fp32 pairs.
+      // gives +0), written back as fp16 over the S columns it came from: cells
+      // 2k, 2k+1 -> column k.  The PV of the previous tile read these columns
+      // before this tile's S was written into them.  Arguments and sums run
+      // as packed fp32 pairs; l sums the unrounded p.
       const uint64_t sc2 = pk2(a.scale_log2, a.scale_log2), nr2 = pk2(nref, nref);
       uint64_t sm2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < 32; ++e) {
           float a0, a1;
-          upk2(ffma2(pk2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nr2), a0, a1);
+          upk2(ffma2(pk2(x[64 * c + 2 * e], x[64 * c + 2 * e + 1]), sc2, nr2), a0, a1);
           const float p0 = ex2(a0), p1 = ex2(a1);
-          const uint64_t pp = pk2(p0, p1);
-          sm2[e & 3] = fadd2(sm2[e & 3], pp);
-          if constexpr (DT == KVO_BF16) {
-            // hi: the upper halves (truncation, exact in fp32); lo: the rounded residual
-            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-            asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(w[e]) : "r"(b0), "r"(b1));
-            float r0, r1;
-            upk2(fsub2(pp, pk2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u))), r0, r1);
-            w[16 + e] = pack2<DT>(r0, r1);
-          } else {
-            split2<DT>(p0, p1, w[e], w[16 + e]);
-          }
+          sm2[e & 3] = fadd2(sm2[e & 3], pk2(p0, p1));
+          w[e] = pack2<KVO_F16>(p0, p1);
         }
         tmem_st32u(s_addr + c * 32, w);
       }

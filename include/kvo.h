@@ -67,7 +67,10 @@ const char *kvo_last_error(void);
  *   bit 2 (4): a bounded barrier wait gave up (about 2 s without progress;
  *              the kernel wound down after its own copies and MMAs landed,
  *              and its output is not valid);
- *   bit 3 (8): a CTA could not align its shared memory and exited.
+ *   bit 3 (8): a CTA could not align its shared memory and exited;
+ *   bit 4 (16): the tensor-core prefill over a bf16 cache met a V value of
+ *              magnitude 65520 or more (or infinite), which its fp16 PV
+ *              product cannot hold; that call's output is not valid.
  * Synchronises the device; clears the bits when `clear` is non-zero.  For
  * tests and debugging, not for hot loops. */
 int kvo_device_errors(uint32_t *bits, int clear);
@@ -601,6 +604,10 @@ int kvo_append_kv_tiered(const void *k_new, const void *v_new, int src_dtype,
  * Direct mode (arena == NULL): the kernel reads the tail from host memory
  * for every query tile.
  *
+ * Precision: scores and sums in fp32; the softmax weights enter the PV
+ *   product as fp16 (11 significant bits), and so do the V values of a bf16
+ *   cache (converted on chip: exact for magnitudes in [2^-14, 65504], to
+ *   within 2^-25 below that; larger values set bit 4 of kvo_device_errors()).
  * q: device [rows][n_q_heads][head_dim], dtype = kv_dtype (F16 or BF16:
  *   the tensor-core tiles take one operand type).  head_dim: 128.  Group
  *   size: 1, 2, 4 or 8.  Rows and base pointers 16-byte aligned.

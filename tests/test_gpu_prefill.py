@@ -104,6 +104,24 @@ def test_direct_tensor_core_path_over_host_rows(hq, hkv, dt, R):
     assert normwise_rel_err(out, ref) <= REL_TOL
 
 
+@pytest.mark.parametrize("arena_cells", [256, 0])
+def test_bf16_value_beyond_fp16_range_sets_bit_4(arena_cells):
+    # The PV product takes the weights and the V values of a bf16 cache as fp16: a cached V value
+    # of 65536 cannot be held and must be reported (staged: V tiles by TMA from the arena;
+    # direct, rows x group >= 512: V tiles loaded from host memory by the producer warp)
+    g = synth.rng(1241, arena_cells)
+    R, pos0, L, N, hq, hkv, d = 128, 900, 1000, 600, 8, 2, 128
+    k, v = cells(L, hkv, d, oracle.BF16, g)
+    q = synth.normal_bits((R, hq, d), "bf16", g)
+    kvo.kvo_device_errors(clear=True)
+    _prefill(Tiered(k, v, N), q, R, pos0, hq, hkv, d, kvo.BF16, L, 0.1, arena_cells, R)
+    assert kvo.kvo_device_errors(clear=True) & 16 == 0
+    v_big = v.copy()
+    v_big[700, 2 * d + 6: 2 * d + 8] = (0x80, 0x47)    # cell 700 (host tail), kv head 1, dim 3: 65536
+    _prefill(Tiered(k, v_big, N), q, R, pos0, hq, hkv, d, kvo.BF16, L, 0.1, arena_cells, R)
+    assert kvo.kvo_device_errors(clear=True) & 16
+
+
 def test_prefill_argument_errors():
     t = torch()
     x = t.zeros(1 << 16, dtype=t.uint8, device="cuda")
