@@ -158,16 +158,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Four int8 values (one word) -> two packed fp32 pairs, exact: x ^ 0x80 is
-// x + 128 as an unsigned byte; in the low mantissa byte of 2^23 it reads as
-// 2^23 + x + 128, and subtracting 2^23 + 128 leaves x.
+// Four int8 values (one word) -> two packed fp32 pairs, exact (int8 -> fp32
+// conversions of the sign-extended bytes).
 __device__ __forceinline__ void i8x4_to_f32x2(uint32_t w, uint64_t &p01, uint64_t &p23) {
-  const uint32_t u = w ^ 0x80808080u;
-  const uint64_t bias = 0x4B0000804B000080ull;            // (2^23 + 128, 2^23 + 128)
-  p01 = fsub2(pk2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))), bias);
-  p23 = fsub2(pk2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                  __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))), bias);
+  p01 = pk2(__int2float_rn((int)(int8_t)(w & 0xffu)), __int2float_rn((int)(int8_t)((w >> 8) & 0xffu)));
+  p23 = pk2(__int2float_rn((int)(int8_t)((w >> 16) & 0xffu)), __int2float_rn((int)(int8_t)(w >> 24)));
 }
 
 // ---------------------------------------------------------------- tile fill
@@ -201,20 +196,26 @@ __device__ __forceinline__ void fill_async(const DecodeArgs &a, int b, int64_t c
   const int total = n * cprd;
   const int T = blockDim.x;
   if (c0 + n <= a.n_vram || c0 >= a.n_vram) {
-    const int64_t rb = a.row_bytes;
-    const uint8_t *kb = (const uint8_t *)row_src(a, b, c0, false), *vb = (const uint8_t *)row_src(a, b, c0, true);
-    int r = (int)fdiv((uint32_t)threadIdx.x, cpr), ch = (int)threadIdx.x - r * cprd;
+    // The tile's rows are contiguous in global memory: chunk i is 16 i bytes
+    // from the first row; in shared memory it is r (pitch - row_bytes) further.
+    const uint32_t pad = (uint32_t)(pitch - a.row_bytes);
+    const uint8_t *kp = (const uint8_t *)row_src(a, b, c0, false) + threadIdx.x * 16;
+    const uint8_t *vp = (const uint8_t *)row_src(a, b, c0, true) + threadIdx.x * 16;
+    const int r0 = (int)fdiv((uint32_t)threadIdx.x, cpr);
+    int ch = (int)threadIdx.x - r0 * cprd;
     const int dr = (int)fdiv((uint32_t)T, cpr), dch = T - dr * cprd;
+    uint32_t so = (uint32_t)(threadIdx.x * 16 + r0 * pad);
+    const uint32_t sk0 = smem_addr(sk), sv0 = smem_addr(sv), step = (uint32_t)(T * 16 + dr * pad);
     for (int i = threadIdx.x; i < total; i += T) {
-      const uint32_t so = (uint32_t)(r * pitch + ch * 16);
-      const int64_t go = (int64_t)r * rb + ch * 16;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sk) + so), "l"(kb + go) : "memory");
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sv) + so), "l"(vb + go) : "memory");
-      r += dr;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sk0 + so), "l"(kp) : "memory");
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sv0 + so), "l"(vp) : "memory");
+      kp += T * 16;
+      vp += T * 16;
+      so += step;
       ch += dch;
       if (ch >= cprd) {
         ch -= cprd;
-        ++r;
+        so += pad;
       }
     }
     return;
