@@ -360,7 +360,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
+  // Registers: the block starts at 168 a thread (384 x 168 = 64,512).  Warps
+  // 8-11 (producer, MMA issuer, converters) hand theirs down to 136 and the
+  // two softmax warpgroups take 184 each: 2 x 128 x 184 + 128 x 136 = 64,512,
+  // the launch's own total, so the increase is always satisfied (and the
+  // softmax keeps its whole S row in registers without spilling).
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 136;" ::: "memory");
   if (warp == 8 && P.host_k) {
     // ---------------------------------------------------------------- host-memory producer
     // The 32 lanes fill each K and V stage with plain loads; after its stores
@@ -528,7 +534,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_const
       const uint32_t mb = *(const uint32_t *)&vmax;
       if ((mb & 0x7fffu) >= 0x7c00u || ((mb >> 16) & 0x7fffu) >= 0x7c00u) atomicOr(P.err, kErrF16Range);
     }
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory");
     // ---------------------------------------------------------------- softmax + epilogue
     const int q = warp >> 2;                                  // query tile
     const int r = (warp & 3) * 32 + lane;                     // row = TMEM lane
