@@ -1020,8 +1020,8 @@ def decode_source_sha256():
 # DRAM bytes per launch of the headline decode kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum of decode_split_kernel, one ncu capture of the headline
 # workload), with the sha256 of the decode kernel source it was taken on.
-HEADLINE_TRAFFIC = {"bytes_per_launch": 17925376,
-                    "decode_source_sha256": "689214bcd13a989bd610d4f54b5ebb730a62e91ab8f902c852c5902797889ce7"}
+HEADLINE_TRAFFIC = {"bytes_per_launch": 17925120,
+                    "decode_source_sha256": "ce6b9b6ca3985ed8384b648da8892ac4e2ba2ac65565075709c6ad206dbde2a4"}
 
 
 def profiled_traffic():
