@@ -1020,8 +1020,8 @@ def decode_source_sha256():
 # DRAM bytes per launch of the headline decode kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum of decode_split_kernel, one ncu capture of the headline
 # workload), with the sha256 of the decode kernel source it was taken on.
-HEADLINE_TRAFFIC = {"bytes_per_launch": 17925120,
-                    "decode_source_sha256": "ce6b9b6ca3985ed8384b648da8892ac4e2ba2ac65565075709c6ad206dbde2a4"}
+HEADLINE_TRAFFIC = {"bytes_per_launch": 17925376,
+                    "decode_source_sha256": "f00154269af9cfed0dda27190e9fda47585705971573907408d9ddf9256ae09a"}
 
 
 def profiled_traffic():
