@@ -1020,8 +1020,8 @@ def decode_source_sha256():
 # DRAM bytes per launch of the headline decode kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum of decode_split_kernel, one ncu capture of the headline
 # workload), with the sha256 of the decode kernel source it was taken on.
-HEADLINE_TRAFFIC = {"bytes_per_launch": 17925376,
-                    "decode_source_sha256": "f00154269af9cfed0dda27190e9fda47585705971573907408d9ddf9256ae09a"}
+HEADLINE_TRAFFIC = {"bytes_per_launch": 18083072,
+                    "decode_source_sha256": "949d0ded6b22820a885c80af5437208ec5d52bad15f8156a5fcdfabcb24dc1b1"}
 
 
 def profiled_traffic():
