@@ -30,7 +30,9 @@ constexpr int kGatherThreads = 256;
 // kGatherWideThreads threads that each reserve more than half an SM's shared
 // memory: one per SM, so whichever kernel starts first, the gather never
 // holds more than kGatherSms SMs and the split kernel always finds its own.
-constexpr int kGatherSms = 16;
+// Four SMs of 1024 threads keep a bucket's gather at the link rate behind the
+// split kernel (measured per step: 16 SMs 10.5 ms, 8 10.2, 4 9.2, 2 11.4).
+constexpr int kGatherSms = 4;
 constexpr int kGatherWideThreads = 1024;
 constexpr int kGatherWideSmem = 120 * 1024;
 constexpr size_t kPartitionSmem = 200 * 1024;   // bucket counters per CTA
